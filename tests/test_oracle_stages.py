@@ -1,0 +1,281 @@
+"""Pins of the oracle's FFN stages: closed forms, brute force, invariants and
+library special cases, each chosen so a plausible slip (a dropped term, a
+swapped operand, a transposed scale, an off-by-one row) fails one of them."""
+import numpy as np
+import pytest
+import torch
+from scipy.special import expit
+
+import oracle
+from oracle import (bf16_decode, bf16_encode, combine, e4m3_decode, e4m3_encode,
+                    gemm_block_scaled, gemm_contig, gemm_masked, permute, quant_1x128,
+                    quant_128x128, swiglu, swiglu_quant)
+
+RNG = np.random.default_rng(1234)
+FLOOR_SCALE = np.float32(np.float32(1e-4) / np.float32(448.0))
+
+
+def _bf16(x):
+    return bf16_decode(bf16_encode(x)).astype(np.float32)
+
+
+# ----------------------------------------------------------------------------- quant
+def test_quant_zero_block_uses_floor_scale():
+    x = np.zeros((3, 256), np.float32)
+    x[1, 128:] = RNG.standard_normal(128)
+    q, s = quant_1x128(x)
+    assert s.shape == (2, 3)
+    assert s[0, 0] == FLOOR_SCALE and s[1, 0] == FLOOR_SCALE and s[0, 1] == FLOOR_SCALE
+    assert (q[0] == 0).all() and (q[1, :128] == 0).all()
+
+
+def test_quant_amax_maps_to_448():
+    x = _bf16(RNG.standard_normal((4, 384)))
+    x[2, 130] = 9.0
+    x[3, 300] = -9.0
+    q, s = quant_1x128(x)
+    assert q[2, 130] == 0x7E and q[3, 300] == 0xFE
+    assert s[1, 2] == np.float32(np.float32(9.0) / np.float32(448.0))
+    # every block holds its own max |x| -> exactly one code of magnitude 0x7E per block
+    assert ((q.reshape(4, 3, 128) & 0x7F) == 0x7E).any(axis=2).all()
+
+
+def test_quant_power_of_two_scale_is_exact():
+    # amax = 448 * 2^-5 -> s = 2^-5 exactly; inputs on the E4M3 grid times 2^-5
+    # must come back bit-exactly.
+    codes = RNG.integers(0, 0x7F, size=(2, 256)).astype(np.uint8) | (RNG.integers(0, 2, (2, 256)) << 7).astype(np.uint8)
+    codes[:, 0] = 0x7E
+    codes[:, 128] = 0xFE
+    x = (e4m3_decode(codes) * 2.0 ** -5).astype(np.float32)
+    q, s = quant_1x128(x)
+    assert (s == np.float32(2.0 ** -5)).all()
+    assert np.array_equal(e4m3_decode(q), e4m3_decode(codes))
+
+
+def test_quant_error_bound_and_layout():
+    M, K = 37, 640
+    x = _bf16(RNG.standard_normal((M, K)) * np.exp(RNG.uniform(-6, 6, (M, 1))))
+    q, s = quant_1x128(x)
+    assert s.shape == (K // 128, M)
+    # scale layout: s[kb, m] is row m's block kb
+    amax = np.abs(x.reshape(M, K // 128, 128)).max(axis=2)
+    assert np.array_equal(s, (np.maximum(amax, np.float32(1e-4)) / np.float32(448)).astype(np.float32).T)
+    deq = e4m3_decode(q) * np.repeat(s.T, 128, axis=1)
+    err = np.abs(deq - x)
+    # half an E4M3 ulp: 2^-4 relative for normals, 2^-10 * s absolute below 2^-6 * s
+    bound = np.maximum(np.abs(x) * 2.0 ** -4, np.repeat(s.T, 128, axis=1) * 2.0 ** -10) * (1 + 1e-6)
+    assert (err <= bound).all()
+
+
+def test_quant_128x128_tiles_are_independent():
+    w = _bf16(RNG.standard_normal((256, 384)) * 0.05)
+    q, s = quant_128x128(w)
+    assert s.shape == (2, 3)
+    w2 = w.copy()
+    w2[130, 260] = 7.0                       # tile (1, 2)
+    q2, s2 = quant_128x128(w2)
+    changed = s2 != s
+    assert changed[1, 2] and changed.sum() == 1
+    assert q2[130, 260] == 0x7E
+    assert np.array_equal(q2[:128], q[:128]) and np.array_equal(q2[:, :256], q[:, :256])
+    # tile amax definition
+    tiles = np.abs(w.reshape(2, 128, 3, 128)).max(axis=(1, 3))
+    assert np.array_equal(s, (np.maximum(tiles, np.float32(1e-4)) / np.float32(448)).astype(np.float32))
+
+
+# ----------------------------------------------------------------------------- permute
+def _permute_bruteforce(ids, eb, E, layout, max_m, align=128):
+    T, k = ids.shape
+    per = {e: [] for e in range(E)}
+    for t in range(T):
+        for j in range(k):
+            e = int(ids[t, j]) - eb
+            if 0 <= e < E:
+                per[e].append(t * k + j)
+    dst = [-1] * (T * k)
+    if layout == "masked":
+        for e in range(E):
+            for r, i in enumerate(per[e]):
+                if r < max_m:
+                    dst[i] = e * max_m + r
+        return [min(len(per[e]), max_m) for e in range(E)], dst
+    row = 0
+    for e in range(E):
+        for r, i in enumerate(per[e]):
+            dst[i] = row + r
+        row += -(-len(per[e]) // align) * align
+    return [len(per[e]) for e in range(E)], dst
+
+
+@pytest.mark.parametrize("layout", ["masked", "contig"])
+def test_permute_matches_bruteforce(layout):
+    for trial in range(5):
+        T, k, E, eb = 50, 3, 5, 2
+        ids = RNG.integers(0, 9, (T, k)).astype(np.int32)
+        max_m = 16
+        p = permute(ids, eb, E, layout, max_m=max_m, align=8)
+        counts, dst = _permute_bruteforce(ids, eb, E, layout, max_m, align=8)
+        assert list(p["counts"]) == counts
+        assert list(p["dst_row"]) == dst
+
+
+def test_permute_invariants_and_gather():
+    T, k, E, K = 40, 2, 4, 256
+    ids = np.stack([RNG.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    q = RNG.integers(0, 256, (T, K)).astype(np.uint8)
+    s = RNG.random((K // 128, T)).astype(np.float32)
+    for layout in ("masked", "contig"):
+        p = permute(ids, 0, E, layout, max_m=64, q=q, s=s)
+        assert p["counts"].sum() == T * k                     # all assignments local
+        dst, src = p["dst_row"], p["row_src"]
+        assert (src[dst] == np.arange(T * k)).all()            # mutually inverse
+        assert (np.sort(dst) == np.sort(np.nonzero(src >= 0)[0])).all()
+        for i in range(T * k):
+            assert np.array_equal(p["q"][dst[i]], q[i // k])
+        if layout == "masked":
+            for i in range(T * k):
+                e, r = divmod(dst[i], 64)
+                assert np.array_equal(p["s"][e, :, r], s[:, i // k])
+        else:
+            assert (p["offsets"] % 128 == 0).all()
+            assert np.array_equal(p["s"][:, dst], s[:, np.arange(T * k) // k])
+            mi = p["m_indices"]
+            for e in range(E):
+                seg = mi[p["offsets"][e]:p["offsets"][e + 1]]
+                assert (seg[:p["counts"][e]] == e).all() and (seg[p["counts"][e]:] == -1).all()
+
+
+def test_permute_masked_overflow_and_nonlocal():
+    ids = np.array([[0, 5], [0, 1], [0, 7], [0, 1]], np.int32)  # expert 0 gets 4 > max_m=2
+    p = permute(ids, 0, 2, "masked", max_m=2)
+    assert p["overflow"] and list(p["counts"]) == [2, 2] and list(p["raw_counts"]) == [4, 2]
+    assert list(p["dst_row"]) == [0, -1, 1, 2, -1, -1, -1, 3]
+
+
+# ----------------------------------------------------------------------------- GEMM
+def _rand_codes(shape):
+    c = RNG.integers(0, 256, shape).astype(np.uint8)
+    c[(c & 0x7F) == 0x7F] = 0x3A                              # no NaN codes
+    return c
+
+
+def test_gemm_integer_exact_closed_form():
+    # integers in [-16, 16] are exact in E4M3; with unit scales the result is the
+    # integer matmul.
+    M, N, K = 19, 256, 384
+    a = RNG.integers(-16, 17, (M, K))
+    b = RNG.integers(-16, 17, (N, K))
+    qa, qb = e4m3_encode(a.astype(np.float64)), e4m3_encode(b.astype(np.float64))
+    assert np.array_equal(e4m3_decode(qa), a)
+    D = gemm_block_scaled(qa, np.ones((K // 128, M), np.float32), qb, np.ones((N // 128, K // 128), np.float32))
+    assert np.array_equal(D, (a @ b.T).astype(np.float64))
+
+
+def test_gemm_bruteforce_triple_loop():
+    M, N, K = 3, 256, 256
+    qa, qb = _rand_codes((M, K)), _rand_codes((N, K))
+    sa = RNG.random((K // 128, M)).astype(np.float32) + 0.5
+    sb = RNG.random((N // 128, K // 128)).astype(np.float32) + 0.5
+    D = gemm_block_scaled(qa, sa, qb, sb)
+    A, B = e4m3_decode(qa), e4m3_decode(qb)
+    for m in range(M):
+        for n in range(0, N, 37):
+            ref = 0.0
+            for k in range(K):
+                ref += float(sa[k // 128, m]) * float(sb[n // 128, k // 128]) * A[m, k] * B[n, k]
+            assert abs(D[m, n] - ref) <= 1e-12 * max(1.0, abs(ref))
+
+
+def test_gemm_matches_dequantised_matmul():
+    M, N, K = 33, 384, 512                                   # KB != NB != M/128: transposes show
+    qa, qb = _rand_codes((M, K)), _rand_codes((N, K))
+    sa = (RNG.random((K // 128, M)) * 4).astype(np.float32)
+    sb = (RNG.random((N // 128, K // 128)) * 4).astype(np.float32)
+    D = gemm_block_scaled(qa, sa, qb, sb)
+    A = e4m3_decode(qa) * np.repeat(sa.T.astype(np.float64), 128, axis=1)
+    B = e4m3_decode(qb) * np.kron(sb.astype(np.float64), np.ones((128, 128)))
+    ref = A @ B.T
+    assert np.allclose(D, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def test_gemm_masked_and_contig_wrappers():
+    E, max_m, N, K = 3, 8, 128, 256
+    qa, qb = _rand_codes((E, max_m, K)), _rand_codes((E, N, K))
+    sa = RNG.random((E, K // 128, max_m)).astype(np.float32)
+    sb = RNG.random((E, N // 128, K // 128)).astype(np.float32)
+    counts = np.array([8, 0, 3])
+    D, valid = gemm_masked(qa, sa, qb, sb, counts)
+    assert valid.sum() == 11 and not valid[1].any() and valid[2, :3].all() and not valid[2, 3:].any()
+    ref = bf16_encode(gemm_block_scaled(qa[2, :3], sa[2][:, :3], qb[2], sb[2]))
+    assert np.array_equal(D[2, :3], ref)
+    # contiguous: same rows laid out with padding to 8
+    offsets = np.array([0, 8, 8, 16])
+    mi = np.array([0] * 8 + [2] * 3 + [-1] * 5)
+    qa_c = np.concatenate([qa[0], qa[2]])
+    sa_c = np.concatenate([sa[0], sa[2]], axis=1)
+    Dc, vc = gemm_contig(qa_c, sa_c, qb, sb, offsets, mi)
+    assert np.array_equal(Dc[:8], D[0]) and np.array_equal(Dc[8:11], D[2, :3]) and vc.sum() == 11
+
+
+# ----------------------------------------------------------------------------- SwiGLU
+def test_swiglu_matches_scipy_expit_and_gate_up_order():
+    rows, I = 5, 256
+    y = _bf16(RNG.standard_normal((rows, 2 * I)) * 3)
+    bits = bf16_encode(y.astype(np.float64))
+    h = swiglu(bits)
+    g, u = y[:, :I].astype(np.float64), y[:, I:].astype(np.float64)
+    assert np.array_equal(h, (g * expit(g) * u).astype(np.float32)) or \
+        np.max(np.abs(h - g * expit(g) * u) / (np.abs(g * expit(g) * u) + 1e-30)) < 2 ** -23
+    # order: gate first.  silu(30) * 1 ~ 30, silu(1) * 30 ~ 21.9
+    t = bf16_encode(np.array([[30.0, 1.0]]))
+    assert abs(swiglu(t)[0, 0] - 30.0) < 1e-6
+    t = bf16_encode(np.array([[0.0, 5.0, -3.0, 0.0]]))
+    assert list(swiglu(t)[0]) == [0.0, 0.0]
+
+
+def test_swiglu_quant_is_quant_of_swiglu():
+    y = bf16_encode(RNG.standard_normal((6, 512)))
+    q, s = swiglu_quant(y)
+    q2, s2 = quant_1x128(swiglu(y))
+    assert np.array_equal(q, q2) and np.array_equal(s, s2) and s.shape == (2, 6)
+
+
+# ----------------------------------------------------------------------------- combine
+def test_combine_constant_rows_and_weights_sum_to_one():
+    T, k, H = 16, 4, 256
+    w = RNG.random((T, k)).astype(np.float32)
+    w /= w.sum(axis=1, keepdims=True)
+    c = _bf16(RNG.standard_normal(H))
+    y2 = np.tile(bf16_encode(c.astype(np.float64)), (T * k, 1))
+    dst = RNG.permutation(T * k)
+    out = combine(y2, dst, w)
+    assert np.array_equal(bf16_decode(out), np.tile(c, (T, 1)).astype(np.float64)) or \
+        np.abs(bf16_decode(out) - c).max() <= 2 ** -8 * np.abs(c).max()
+
+
+def test_combine_single_choice_is_a_gather_and_skips_dropped():
+    T, H = 10, 128
+    y2 = bf16_encode(RNG.standard_normal((20, H)))
+    dst = RNG.permutation(20)[:T]
+    out = combine(y2, dst, np.ones((T, 1), np.float32))
+    assert np.array_equal(out, y2[dst])
+    dst2 = dst.copy()
+    dst2[3] = -1
+    out2 = combine(y2, dst2, np.ones((T, 1), np.float32))
+    assert (bf16_decode(out2[3]) == 0).all() and np.array_equal(out2[4:], y2[dst[4:]])
+
+
+def test_combine_bruteforce():
+    T, k, H = 6, 3, 128
+    y2 = bf16_encode(RNG.standard_normal((T * k + 2, H)))
+    dst = RNG.permutation(T * k + 2)[:T * k]
+    dst[4] = -1
+    w = RNG.random((T, k)).astype(np.float32)
+    out = bf16_decode(combine(y2, dst, w))
+    Y = bf16_decode(y2)
+    for t in range(T):
+        ref = np.zeros(H)
+        for j in range(k):
+            if dst[t * k + j] >= 0:
+                ref += float(w[t, j]) * Y[dst[t * k + j]]
+        assert np.array_equal(out[t], bf16_decode(bf16_encode(ref)))
