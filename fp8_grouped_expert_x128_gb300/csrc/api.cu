@@ -1,0 +1,241 @@
+// Host runtime of the library: status codes, device checks, TMA descriptor
+// encoding, and moe_ffn -- the whole routed-expert FFN enqueued on one stream
+// with no host synchronisation (graph-capturable, like the decode path the
+// pages pair with DeepEP's CUDA-Graph-compatible low-latency mode: "Deploying
+// DeepSeek with PD Disaggregation and Large-Scale Expert Parallelism on 96
+// H100 GPUs", section "Expert parallelism based on DeepEP").
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe {
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev < 0 || dev >= 64) return 1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+  }
+  return cache[dev];
+}
+
+int check_device() {
+  static int cache[64];
+  static bool init = false;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!init) {
+    for (int& c : cache) c = 1;  // 1 = unknown
+    init = true;
+  }
+  if (cache[dev] == 1) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    // The kernels are built for sm_103a only.
+    cache[dev] = (major == 10 && minor == 3) ? MOE_OK : MOE_ERR_UNSUPPORTED;
+  }
+  return cache[dev];
+}
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void load_encode() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+}  // namespace
+
+int make_tmap_u8_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                       uint64_t ld_bytes, uint32_t box_rows) {
+  std::call_once(g_encode_once, load_encode);
+  if (g_encode == nullptr) return MOE_ERR_CUDA;
+  if (!aligned16(base) || ld_bytes % 16 != 0 || rows == 0 || cols == 0) return MOE_ERR_INVALID_ARG;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {ld_bytes};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+namespace {
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct FfnPlan {
+  int64_t T_pad, rows, s_ld1, s_ld2;
+  size_t off_qx, off_sx, off_counts, off_offsets, off_mind, off_rowsrc, off_dst, off_a1, off_sa1,
+      off_y1, off_a2, off_sa2, off_y2, total;
+};
+
+int plan_ffn(const moe_ffn_desc* d, FfnPlan* p) {
+  if (d == nullptr) return MOE_ERR_INVALID_ARG;
+  if (d->T < 0 || d->H <= 0 || d->H % 128 || d->I <= 0 || d->I % 128 || d->k < 1 || d->k > 32 ||
+      d->E < 1 || d->E > 1024)
+    return MOE_ERR_INVALID_ARG;
+  const int64_t H = d->H, I = d->I, E = d->E;
+  p->T_pad = (d->T + 3) / 4 * 4;
+  if (d->layout == MOE_LAYOUT_MASKED) {
+    if (d->max_m <= 0) return MOE_ERR_INVALID_ARG;
+    p->rows = E * d->max_m;
+    p->s_ld1 = p->s_ld2 = d->max_m;
+  } else if (d->layout == MOE_LAYOUT_CONTIG) {
+    p->rows = moe_contig_rows_bound(d->T * d->k, d->E);
+    if (p->rows == 0) p->rows = 128;
+    p->s_ld1 = p->s_ld2 = p->rows;
+  } else {
+    return MOE_ERR_INVALID_ARG;
+  }
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  p->off_qx = take(static_cast<size_t>(d->T) * H);
+  p->off_sx = take(sizeof(float) * (H / 128) * p->T_pad);
+  p->off_counts = take(sizeof(int32_t) * E);
+  p->off_offsets = take(sizeof(int32_t) * (E + 1));
+  p->off_mind = take(sizeof(int32_t) * p->rows);
+  p->off_rowsrc = take(sizeof(int32_t) * p->rows);
+  p->off_dst = take(sizeof(int32_t) * d->T * d->k);
+  p->off_a1 = take(static_cast<size_t>(p->rows) * H);
+  p->off_sa1 = take(sizeof(float) * (H / 128) * p->rows);
+  p->off_y1 = take(sizeof(uint16_t) * p->rows * 2 * I);
+  p->off_a2 = take(static_cast<size_t>(p->rows) * I);
+  p->off_sa2 = take(sizeof(float) * (I / 128) * p->rows);
+  p->off_y2 = take(sizeof(uint16_t) * p->rows * H);
+  p->total = o;
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_OVERFLOW: return "MOE_ERR_OVERFLOW";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_BAD_INDEX: return "MOE_ERR_BAD_INDEX";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}
+
+extern "C" int moe_version(void) { return 100; }
+
+extern "C" int moe_read_device_status(int32_t* err, void* stream, int* status_out,
+                                      int32_t* raw_bits_out) {
+  if (err == nullptr || status_out == nullptr) return MOE_ERR_INVALID_ARG;
+  int32_t bits = 0;
+  cudaStream_t st = as_stream(stream);
+  MOE_CUDA_TRY(cudaMemcpyAsync(&bits, err, sizeof(bits), cudaMemcpyDeviceToHost, st));
+  MOE_CUDA_TRY(cudaMemsetAsync(err, 0, sizeof(int32_t), st));
+  MOE_CUDA_TRY(cudaStreamSynchronize(st));
+  if (raw_bits_out) *raw_bits_out = bits;
+  if (bits & MOE_DEV_BAD_INDEX)
+    *status_out = MOE_ERR_BAD_INDEX;
+  else if (bits & MOE_DEV_TIMEOUT)
+    *status_out = MOE_ERR_TIMEOUT;
+  else if (bits & MOE_DEV_OVERFLOW)
+    *status_out = MOE_ERR_OVERFLOW;
+  else
+    *status_out = MOE_OK;
+  return MOE_OK;
+}
+
+extern "C" size_t moe_ffn_workspace_size(const moe_ffn_desc* desc) {
+  FfnPlan p;
+  if (plan_ffn(desc, &p) != MOE_OK) return 0;
+  return p.total;
+}
+
+extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  FfnPlan p;
+  if (int st = plan_ffn(d, &p)) return st;
+  MOE_CHECK_ARG(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255) == 0);
+  MOE_CHECK_ARG(workspace_bytes >= p.total);
+  MOE_CHECK_ARG(d->x && d->topk_ids && d->topk_w && d->w13 && d->w13_s && d->w2 && d->w2_s && d->out);
+  if (int st = check_device()) return st;
+  cudaStream_t st = as_stream(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto at = [&](size_t off) { return static_cast<void*>(ws + off); };
+  uint8_t* qx = static_cast<uint8_t*>(at(p.off_qx));
+  float* sx = static_cast<float*>(at(p.off_sx));
+  int32_t* counts = static_cast<int32_t*>(at(p.off_counts));
+  int32_t* offsets = static_cast<int32_t*>(at(p.off_offsets));
+  int32_t* mind = static_cast<int32_t*>(at(p.off_mind));
+  int32_t* rowsrc = static_cast<int32_t*>(at(p.off_rowsrc));
+  int32_t* dst = static_cast<int32_t*>(at(p.off_dst));
+  uint8_t* a1 = static_cast<uint8_t*>(at(p.off_a1));
+  float* sa1 = static_cast<float*>(at(p.off_sa1));
+  uint16_t* y1 = static_cast<uint16_t*>(at(p.off_y1));
+  uint8_t* a2 = static_cast<uint8_t*>(at(p.off_a2));
+  float* sa2 = static_cast<float*>(at(p.off_sa2));
+  uint16_t* y2 = static_cast<uint16_t*>(at(p.off_y2));
+  const bool masked = d->layout == MOE_LAYOUT_MASKED;
+  cudaEvent_t* ev = reinterpret_cast<cudaEvent_t*>(d->stage_events);
+  auto mark = [&](int i) -> int {
+    if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[i], st));
+    return MOE_OK;
+  };
+  int rc;
+  if ((rc = mark(0))) return rc;
+  if ((rc = moe_quant_fp8(d->x, d->T, d->H, d->H, qx, d->H, sx, p.T_pad, d->err, stream))) return rc;
+  if ((rc = mark(1))) return rc;
+  if ((rc = moe_permute(qx, sx, p.T_pad, d->topk_ids, d->T, d->H, d->k, d->expert_begin, d->E,
+                        d->layout, d->max_m, a1, sa1, p.s_ld1, counts, offsets, mind, rowsrc, dst,
+                        p.rows, d->err, stream)))
+    return rc;
+  if ((rc = mark(2))) return rc;
+  if (masked)
+    rc = moe_gemm_fp8_masked(a1, sa1, d->w13, d->w13_s, counts, d->E, d->max_m, 2 * d->I, d->H,
+                             d->expected_m, y1, d->gemm_flags, d->err, stream);
+  else
+    rc = moe_gemm_fp8_contig(a1, d->H, sa1, p.s_ld1, d->w13, d->w13_s, offsets, mind, p.rows, d->E,
+                             2 * d->I, d->H, y1, 2 * d->I, d->gemm_flags, d->err, stream);
+  if (rc) return rc;
+  if ((rc = mark(3))) return rc;
+  if ((rc = moe_swiglu_quant(y1, p.rows, d->I, masked ? counts : nullptr, d->max_m,
+                             masked ? nullptr : mind, a2, sa2, p.s_ld2, d->err, stream)))
+    return rc;
+  if ((rc = mark(4))) return rc;
+  if (masked)
+    rc = moe_gemm_fp8_masked(a2, sa2, d->w2, d->w2_s, counts, d->E, d->max_m, d->H, d->I,
+                             d->expected_m, y2, d->gemm_flags, d->err, stream);
+  else
+    rc = moe_gemm_fp8_contig(a2, d->I, sa2, p.s_ld2, d->w2, d->w2_s, offsets, mind, p.rows, d->E,
+                             d->H, d->I, y2, d->H, d->gemm_flags, d->err, stream);
+  if (rc) return rc;
+  if ((rc = mark(5))) return rc;
+  if ((rc = moe_combine(y2, d->H, p.rows, dst, d->topk_w, d->T, d->k, d->H, d->out, d->H, d->err,
+                        stream)))
+    return rc;
+  return mark(6);
+}

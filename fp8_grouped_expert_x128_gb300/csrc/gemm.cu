@@ -1,0 +1,402 @@
+// Grouped FP8 GEMM with 1x128 / 128x128 fp32 block scales on sm_103a tensor
+// cores (tcgen05 "UMMA", accumulators in tensor memory).
+//
+// The pages this library follows describe a Blackwell FP8 GEMM built on UMMA
+// whose API quantises and packs the input scales ("Deploying DeepSeek on GB200
+// NVL72 with PD and Large Scale EP (Part I)", section "Implementation
+// details", DeepGEMM bullet), with one grouped variant for prefill and one for
+// decode ("Deploying DeepSeek with PD Disaggregation and Large-Scale Expert
+// Parallelism on 96 H100 GPUs", section "DeepGEMM integration").  The kernel
+// below is this library's own design for GB300:
+//
+//  * persistent: one CTA per SM walks a linear tile list built on the device
+//    from the per-expert row extents (masked counts or contiguous offsets), so
+//    no host synchronisation is needed and skewed experts share the SMs evenly;
+//  * warp-specialised, 10 warps: warp 0 = TMA producer (4-stage ring of
+//    128x128 A and 256x128 B byte tiles, 128-byte swizzle), warp 1 = a single
+//    thread issuing tcgen05.mma (M=128, N=256, K=32 x4 per 128-deep block),
+//    warps 2..9 = epilogue;
+//  * scale promotion: the fp32 scales differ per row (sA) and per 128x128
+//    weight block (sB), so each 128-deep block is accumulated alone into one of
+//    two TMEM buffers (2 x 256 columns), and the epilogue warps read it with
+//    tcgen05.ld, multiply by sA[row, kb] * sB[nb, kb] and accumulate in fp32
+//    registers while the tensor cores fill the other buffer;
+//  * every wait is bounded (see common.cuh): a stalled pipeline flags
+//    MOE_DEV_TIMEOUT and the CTA unwinds, frees its TMEM and returns.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr uint32_t kATileBytes = BM * BK;
+constexpr uint32_t kBTileBytes = BN * BK;
+constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxExperts = 1024;
+
+struct GemmArgs {
+  const float* sA;
+  int64_t sA_G;  // scale group size: masked max_m, contiguous sA_ld
+  const float* sB;
+  const int32_t* counts;     // masked
+  const int32_t* offsets;    // contiguous
+  const int32_t* m_indices;  // contiguous
+  uint16_t* D;
+  int64_t ldd;
+  int32_t E, N, K, max_m, layout;
+  int32_t* err;
+  uint64_t wait_limit_ns;
+  int32_t flags;
+};
+
+struct Sched {
+  int32_t* tile0;  // [E+1] first tile of each expert
+  int32_t* rbase;  // [E]   first A/D row of each expert
+  int32_t* rext;   // [E]   row extent (masked: kept count; contiguous: segment rows)
+};
+
+struct TileCursor {
+  int e = 0;
+  __device__ __forceinline__ void seek(const Sched& s, int t) {
+    while (t >= s.tile0[e + 1]) ++e;
+  }
+};
+
+// Warp 0 builds the tile schedule: each lane owns a contiguous chunk of experts.
+__device__ void build_schedule(const GemmArgs& p, const Sched& s, int n_tiles) {
+  const int lane = threadIdx.x & 31;
+  const int per = (p.E + 31) / 32;
+  const int e0 = min(lane * per, p.E), e1 = min(e0 + per, p.E);
+  int local = 0;
+  bool overflow = false, bad = false;
+  for (int e = e0; e < e1; ++e) {
+    int rb, rx;
+    if (p.layout == MOE_LAYOUT_MASKED) {
+      int c = p.counts[e];
+      if (c > p.max_m) { overflow = true; c = p.max_m; }
+      if (c < 0) { bad = true; c = 0; }
+      rb = e * p.max_m;
+      rx = c;
+    } else {
+      rb = p.offsets[e];
+      rx = p.offsets[e + 1] - rb;
+      if ((rb % BM) != 0 || rx < 0 || (rx % BM) != 0) { bad = true; rx = 0; }
+    }
+    s.rbase[e] = rb;
+    s.rext[e] = rx;
+    local += (rx + BM - 1) / BM * n_tiles;
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int run = incl - local;
+  for (int e = e0; e < e1; ++e) {
+    s.tile0[e] = run;
+    run += (s.rext[e] + BM - 1) / BM * n_tiles;
+  }
+  if (lane == 31) s.tile0[p.E] = incl;
+  if (blockIdx.x == 0) {
+    if (overflow) set_err(p.err, MOE_DEV_OVERFLOW);
+    if (bad) set_err(p.err, MOE_DEV_BAD_INDEX);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_fp8_tokens_m_kernel(const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* a_tiles = smem;
+  uint8_t* b_tiles = smem + kStages * kATileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int32_t* sched_mem = reinterpret_cast<int32_t*>(tmem_slot + 4);
+  const Sched sched{sched_mem, sched_mem + p.E + 1, sched_mem + 2 * p.E + 1};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * kStages;
+  const uint32_t tfull0 = empty0 + 8 * kStages;
+  const uint32_t tempty0 = tfull0 + 16;
+  const int n_tiles = (p.N + BN - 1) / BN;
+  const int KB = p.K / BK;
+  const int NB = p.N / 128;
+  volatile int* abort = abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull0 + 8 * b, 1);
+      mbar_init(tempty0 + 8 * b, kEpiWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    build_schedule(p, sched, n_tiles);
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = sched.tile0[p.E];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && !(p.flags & MOE_GEMM_DEBUG_STALL)) {
+      uint32_t it = 0;
+      TileCursor cur;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        cur.seek(sched, t);
+        const int l = t - sched.tile0[cur.e];
+        const int a_row = sched.rbase[cur.e] + (l / n_tiles) * BM;
+        const int b_row = cur.e * p.N + (l % n_tiles) * BN;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+          if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, p.err, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full0 + 8 * s, kStageBytes);
+          tma_load_2d(smem_u32(a_tiles + s * kATileBytes), &tmA, full0 + 8 * s, kb * BK, a_row);
+          tma_load_2d(smem_u32(b_tiles + s * kBTileBytes), &tmB, full0 + 8 * s, kb * BK, b_row);
+        }
+      }
+      if (!ok) {
+        // drain: let the copies already issued land before the CTA exits
+        const uint32_t first = it > kStages ? it - kStages : 0;
+        for (uint32_t j = first; j < it; ++j) {
+          int dummy = 0;
+          mbar_wait_bounded(full0 + 8 * (j % kStages), (j / kStages) & 1, &dummy, nullptr,
+                            p.wait_limit_ns / 10);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, acc = 0;
+      TileCursor cur;
+      bool ok = true;
+      const uint32_t id_full = idesc_e4m3_f32(BM, BN);
+      const uint32_t id_half = idesc_e4m3_f32(BM, BN / 2);
+      for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        cur.seek(sched, t);
+        const int nt = (t - sched.tile0[cur.e]) % n_tiles;
+        const bool half = (nt == n_tiles - 1) && (p.N % BN) != 0;
+        const uint32_t idesc = half ? id_half : id_full;
+        for (int kb = 0; kb < KB; ++kb, ++it, ++acc) {
+          const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+          const uint32_t b = acc & 1, tph = (acc >> 1) & 1;
+          if (!mbar_wait_bounded(tempty0 + 8 * b, tph ^ 1, abort, p.err, p.wait_limit_ns) ||
+              !mbar_wait_bounded(full0 + 8 * s, ph, abort, p.err, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(a_tiles + s * kATileBytes));
+          const uint64_t bd = sdesc_kmajor_sw128(smem_u32(b_tiles + s * kBTileBytes));
+          const uint32_t d_tmem = tmem_base + b * BN;
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)  // 32 bytes of K per MMA: +2 in the 16-byte address field
+            umma_e4m3(d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
+          umma_commit(empty0 + 8 * s);
+          umma_commit(tfull0 + 8 * b);
+        }
+      }
+      if (!ok && acc > 0) {  // wait for the MMAs in flight before TMEM is freed
+        int dummy = 0;
+        mbar_wait_bounded(tfull0 + 8 * ((acc - 1) & 1), ((acc - 1) >> 1) & 1, &dummy, nullptr,
+                          p.wait_limit_ns / 10);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                // TMEM lane quadrant of this warp
+    const int g = (warp - 2) >> 2;         // column half of the 256-wide tile
+    uint32_t acc_it = 0;
+    TileCursor cur;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+      cur.seek(sched, t);
+      const int e = cur.e;
+      const int l = t - sched.tile0[e];
+      const int mt = l / n_tiles, nt = l % n_tiles;
+      const bool half = (nt == n_tiles - 1) && (p.N % BN) != 0;
+      const bool active = !(half && g == 1);
+      const int r_local = mt * BM + q * 32 + lane;
+      const int64_t gr = static_cast<int64_t>(sched.rbase[e]) + r_local;
+      bool row_ok = r_local < sched.rext[e];
+      if (row_ok && p.layout == MOE_LAYOUT_CONTIG) row_ok = __ldg(p.m_indices + gr) >= 0;
+      const int n0 = nt * BN + g * 128;
+      const int64_t grp = gr / p.sA_G, pos = gr - grp * p.sA_G;
+      const float* sa_ptr = p.sA + grp * KB * p.sA_G + pos;
+      const float* sb_ptr = p.sB + (static_cast<int64_t>(e) * NB + (active ? n0 / 128 : 0)) * KB;
+      float acc[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) acc[i] = 0.f;
+      for (int kb = 0; kb < KB; ++kb, ++acc_it) {
+        const uint32_t b = acc_it & 1, tph = (acc_it >> 1) & 1;
+        const float sa = row_ok ? __ldg(sa_ptr + static_cast<int64_t>(kb) * p.sA_G) : 0.f;
+        const float sb = __ldg(sb_ptr + kb);
+        const float sc = sa * sb;
+        // one lane waits, the warp follows it: tcgen05.ld is warp-collective
+        int got = 1;
+        if (lane == 0) got = mbar_wait_bounded(tfull0 + 8 * b, tph, abort, p.err, p.wait_limit_ns);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (active) {
+          const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + g * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(sc, __uint_as_float(r[i]), acc[c * 32 + i]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty0 + 8 * b);
+      }
+      if (!ok) break;
+      if (active && row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(p.D + gr * p.ldd + n0);
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+          uint32_t o[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const __nv_bfloat162 bb = __floats2bfloat162_rn(acc[v * 8 + 2 * h], acc[v * 8 + 2 * h + 1]);
+            o[h] = *reinterpret_cast<const uint32_t*>(&bb);
+          }
+          dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+size_t tokens_m_smem_bytes(int E) {
+  return 1024 + static_cast<size_t>(kStages) * kStageBytes + (2 * kStages + 4) * 8 + 16 +
+         sizeof(int32_t) * (3 * E + 1);
+}
+
+int launch_tokens_m(const uint8_t* A, int64_t a_rows, int64_t lda, const uint8_t* B,
+                    int64_t tiles_upper, GemmArgs& args, cudaStream_t stream) {
+  CUtensorMap tmA, tmB;
+  if (int st = make_tmap_u8_sw128(&tmA, A, a_rows, args.K, lda, BM)) return st;
+  if (int st = make_tmap_u8_sw128(&tmB, B, static_cast<uint64_t>(args.E) * args.N, args.K, args.K, BN))
+    return st;
+  const size_t smem = tokens_m_smem_bytes(args.E);
+  MOE_CUDA_TRY(cudaFuncSetAttribute(gemm_fp8_tokens_m_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem)));
+  if (args.wait_limit_ns == 0) args.wait_limit_ns = kWaitLimitNs;
+  int64_t grid = num_sms();
+  if (tiles_upper < grid) grid = tiles_upper;
+  if (grid < 1) grid = 1;
+  gemm_fp8_tokens_m_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, args);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_gemm_fp8_contig(const uint8_t* A, int64_t lda, const float* sA, int64_t sA_ld,
+                                   const uint8_t* B, const float* sB, const int32_t* offsets,
+                                   const int32_t* m_indices, int64_t M_capacity, int32_t E,
+                                   int32_t N, int32_t K, uint16_t* D, int64_t ldd, int32_t flags,
+                                   int32_t* err, void* stream) {
+  MOE_CHECK_ARG(E >= 1 && E <= kMaxExperts && N > 0 && N % 128 == 0 && K > 0 && K % 128 == 0);
+  MOE_CHECK_ARG(M_capacity >= 0 && M_capacity % BM == 0 && M_capacity < (1ll << 31));
+  if (M_capacity == 0) return MOE_OK;
+  MOE_CHECK_ARG(A && sA && B && sB && offsets && m_indices && D);
+  MOE_CHECK_ARG(aligned16(A) && aligned16(B) && aligned16(D) && aligned16(sA));
+  MOE_CHECK_ARG(lda >= K && lda % 16 == 0 && sA_ld >= M_capacity && ldd >= N && ldd % 8 == 0);
+  MOE_CHECK_ARG(static_cast<int64_t>(E) * N < (1ll << 31));
+  if (int st = check_device()) return st;
+  GemmArgs a{};
+  a.sA = sA;
+  a.sA_G = sA_ld;
+  a.sB = sB;
+  a.offsets = offsets;
+  a.m_indices = m_indices;
+  a.D = D;
+  a.ldd = ldd;
+  a.E = E;
+  a.N = N;
+  a.K = K;
+  a.layout = MOE_LAYOUT_CONTIG;
+  a.err = err;
+  a.flags = flags;
+  const int64_t tiles = (M_capacity / BM) * ((N + BN - 1) / BN);
+  return launch_tokens_m(A, M_capacity, lda, B, tiles, a, as_stream(stream));
+}
+
+extern "C" int moe_gemm_fp8_masked(const uint8_t* A, const float* sA, const uint8_t* B,
+                                   const float* sB, const int32_t* counts, int32_t E,
+                                   int32_t max_m, int32_t N, int32_t K, int32_t expected_m,
+                                   uint16_t* D, int32_t flags, int32_t* err, void* stream) {
+  (void)expected_m;
+  MOE_CHECK_ARG(E >= 1 && E <= kMaxExperts && N > 0 && N % 128 == 0 && K > 0 && K % 128 == 0);
+  MOE_CHECK_ARG(max_m > 0 && static_cast<int64_t>(E) * max_m < (1ll << 31));
+  MOE_CHECK_ARG(A && sA && B && sB && counts && D);
+  MOE_CHECK_ARG(aligned16(A) && aligned16(B) && aligned16(D) && aligned16(sA));
+  MOE_CHECK_ARG(static_cast<int64_t>(E) * N < (1ll << 31));
+  if (int st = check_device()) return st;
+  GemmArgs a{};
+  a.sA = sA;
+  a.sA_G = max_m;
+  a.sB = sB;
+  a.counts = counts;
+  a.D = D;
+  a.ldd = N;
+  a.E = E;
+  a.N = N;
+  a.K = K;
+  a.max_m = max_m;
+  a.layout = MOE_LAYOUT_MASKED;
+  a.err = err;
+  a.flags = flags;
+  if (flags & MOE_GEMM_DEBUG_STALL) a.wait_limit_ns = 200ull * 1000ull * 1000ull;
+  const int64_t tiles = static_cast<int64_t>(E) * ((max_m + BM - 1) / BM) * ((N + BN - 1) / BN);
+  return launch_tokens_m(A, static_cast<int64_t>(E) * max_m, K, B, tiles, a, as_stream(stream));
+}

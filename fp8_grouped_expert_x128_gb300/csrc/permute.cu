@@ -1,0 +1,262 @@
+// Permute token-order FP8 rows into the grouped expert layouts, and combine
+// expert outputs back into token order.
+//
+// The grouped layouts are the inputs of the two grouped GEMMs of "Deploying
+// DeepSeek with PD Disaggregation and Large-Scale Expert Parallelism on 96 H100
+// GPUs", section "DeepGEMM integration": contiguous segments for prefill (after
+// DeepEP's normal dispatch) and a fixed-capacity slab per expert with
+// device-side counts for decode (after the CUDA-Graph-compatible low-latency
+// dispatch; same page, section "Expert parallelism based on DeepEP").  Here the
+// cross-GPU shuffle is absent: tokens are already resident, and the permute is
+// the local half of a dispatch.
+//
+// permute: one CTA of 1024 threads assigns every routed row a destination in
+// ascending assignment order (deterministic), counting with warp match masks
+// and a per-warp table in shared memory; a second kernel copies the 1-byte
+// rows (16-byte vectors, one warp per row) and gathers their fp32 scales.
+// combine: one CTA per token, fp32 accumulation over the k choices in order.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kIdxThreads = 1024;
+constexpr int kIdxWarps = kIdxThreads / 32;
+constexpr int kMaxExperts = 1024;
+
+struct IndexParams {
+  const int32_t* topk_ids;
+  int64_t n_assign;  // T * k
+  int32_t expert_begin, E, layout, max_m;
+  int64_t rows_capacity;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* m_indices;
+  int32_t* row_src;
+  int32_t* dst_row;
+  int32_t* err;
+};
+
+// dynamic smem: cnt[E] | base[E] | wc[kIdxWarps][E]
+__global__ void __launch_bounds__(kIdxThreads) permute_index_kernel(IndexParams p) {
+  extern __shared__ int32_t sm[];
+  const int E = p.E;
+  int32_t* cnt = sm;
+  int32_t* base = sm + E;
+  int32_t* wc = sm + 2 * E;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // 1. histogram (order-free)
+  for (int e = tid; e < E; e += kIdxThreads) cnt[e] = 0;
+  __syncthreads();
+  for (int64_t i = tid; i < p.n_assign; i += kIdxThreads) {
+    const int e = p.topk_ids[i] - p.expert_begin;
+    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+  }
+  __syncthreads();
+
+  // 2. segment bases, counts, offsets; fill row maps with -1
+  if (tid == 0) {
+    int64_t row = 0;
+    bool overflow = false;
+    for (int e = 0; e < E; ++e) {
+      if (p.layout == MOE_LAYOUT_MASKED) {
+        base[e] = e * p.max_m;
+        const int c = cnt[e];
+        overflow |= c > p.max_m;
+        p.counts[e] = c < p.max_m ? c : p.max_m;
+      } else {
+        base[e] = static_cast<int32_t>(row);
+        p.offsets[e] = static_cast<int32_t>(row);
+        p.counts[e] = cnt[e];
+        row += (cnt[e] + 127) / 128 * 128;
+      }
+    }
+    if (p.layout == MOE_LAYOUT_CONTIG) p.offsets[E] = static_cast<int32_t>(row);
+    if (overflow) set_err(p.err, MOE_DEV_OVERFLOW);
+    if (row > p.rows_capacity) set_err(p.err, MOE_DEV_BAD_INDEX);
+  }
+  __syncthreads();
+  const int64_t map_rows =
+      p.layout == MOE_LAYOUT_MASKED ? static_cast<int64_t>(E) * p.max_m : p.rows_capacity;
+  for (int64_t r = tid; r < map_rows; r += kIdxThreads) {
+    p.row_src[r] = -1;
+    if (p.layout == MOE_LAYOUT_CONTIG) p.m_indices[r] = -1;
+  }
+  for (int e = tid; e < E; e += kIdxThreads) cnt[e] = 0;  // becomes the running rank
+  __syncthreads();
+
+  // 3. ranks in ascending assignment order, chunk by chunk
+  for (int64_t c0 = 0; c0 < p.n_assign; c0 += kIdxThreads) {
+    const int64_t i = c0 + tid;
+    int e = -1;
+    if (i < p.n_assign) {
+      e = p.topk_ids[i] - p.expert_begin;
+      if (e < 0 || e >= E) e = -1;
+    }
+    for (int x = tid; x < kIdxWarps * E; x += kIdxThreads) wc[x] = 0;
+    __syncthreads();
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    const int rank_in_warp = __popc(same & ((1u << lane) - 1u));
+    if (e >= 0 && rank_in_warp == 0) wc[warp * E + e] = __popc(same);
+    __syncthreads();
+    for (int ee = tid; ee < E; ee += kIdxThreads) {  // exclusive scan over warps
+      int run = cnt[ee];
+      for (int w = 0; w < kIdxWarps; ++w) {
+        const int v = wc[w * E + ee];
+        wc[w * E + ee] = run;
+        run += v;
+      }
+      cnt[ee] = run;
+    }
+    __syncthreads();
+    if (e >= 0) {
+      const int rank = wc[warp * E + e] + rank_in_warp;
+      int32_t dst = -1;
+      if (p.layout == MOE_LAYOUT_CONTIG || rank < p.max_m) {
+        const int64_t row = static_cast<int64_t>(base[e]) + rank;
+        if (row < map_rows) {
+          dst = static_cast<int32_t>(row);
+          p.row_src[row] = static_cast<int32_t>(i);
+          if (p.layout == MOE_LAYOUT_CONTIG) p.m_indices[row] = e;
+        }
+      }
+      p.dst_row[i] = dst;
+    } else if (i < p.n_assign) {
+      p.dst_row[i] = -1;
+    }
+    __syncthreads();
+  }
+}
+
+// One warp per assignment: copy the FP8 row and gather its scales.
+__global__ void __launch_bounds__(128) permute_scatter_kernel(
+    const uint8_t* __restrict__ q, const float* __restrict__ s, int64_t s_ld,
+    const int32_t* __restrict__ dst_row, int64_t n_assign, int32_t k, int64_t H,
+    uint8_t* __restrict__ q_out, float* __restrict__ s_out, int64_t G) {
+  const int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (i >= n_assign) return;
+  const int32_t dst = __ldg(dst_row + i);
+  if (dst < 0) return;
+  const int64_t t = i / k;
+  const uint4* src = reinterpret_cast<const uint4*>(q + t * H);
+  uint4* out = reinterpret_cast<uint4*>(q_out + static_cast<int64_t>(dst) * H);
+  const int64_t n16 = H / 16;
+  for (int64_t v = lane; v < n16; v += 32) out[v] = __ldg(src + v);
+  const int64_t KB = H / 128;
+  const int64_t grp = dst / G, pos = dst - grp * G;
+  for (int64_t kb = lane; kb < KB; kb += 32) s_out[(grp * KB + kb) * G + pos] = __ldg(s + kb * s_ld + t);
+}
+
+// One CTA per token; each thread owns 8 consecutive columns per step.
+__global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict__ y2, int64_t ldy,
+                                                      int64_t y_rows,
+                                                      const int32_t* __restrict__ dst_row,
+                                                      const float* __restrict__ topk_w, int32_t k,
+                                                      int64_t H, uint16_t* __restrict__ out,
+                                                      int64_t ldo, int32_t* err) {
+  __shared__ int32_t s_dst[32];
+  __shared__ float s_w[32];
+  const int64_t t = blockIdx.x;
+  if (threadIdx.x < k) {
+    int32_t d = dst_row[t * k + threadIdx.x];
+    if (d >= y_rows) {
+      set_err(err, MOE_DEV_BAD_INDEX);
+      d = -1;
+    }
+    s_dst[threadIdx.x] = d;
+    s_w[threadIdx.x] = topk_w[t * k + threadIdx.x];
+  }
+  __syncthreads();
+  for (int64_t c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int j = 0; j < k; ++j) {
+      const int32_t d = s_dst[j];
+      if (d < 0) continue;
+      const float w = s_w[j];
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(y2 + static_cast<int64_t>(d) * ldy + c));
+      const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        acc[2 * h] = fmaf(w, __uint_as_float(v[h] << 16), acc[2 * h]);
+        acc[2 * h + 1] = fmaf(w, __uint_as_float(v[h] & 0xFFFF0000u), acc[2 * h + 1]);
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * h], acc[2 * h + 1]);
+      o[h] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(out + t * ldo + c) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int64_t moe_contig_rows_bound(int64_t assignments, int32_t E) {
+  if (assignments < 0 || E < 0) return -1;
+  return (assignments + 127ll * E) / 128 * 128;
+}
+
+extern "C" int moe_permute(const uint8_t* q, const float* s, int64_t s_ld, const int32_t* topk_ids,
+                           int64_t T, int32_t H, int32_t k, int32_t expert_begin, int32_t E,
+                           int32_t layout, int32_t max_m, uint8_t* q_out, float* s_out,
+                           int64_t s_out_ld, int32_t* counts, int32_t* offsets,
+                           int32_t* m_indices, int32_t* row_src, int32_t* dst_row,
+                           int64_t rows_capacity, int32_t* err, void* stream) {
+  MOE_CHECK_ARG(T >= 0 && H > 0 && H % 128 == 0 && k >= 1 && k <= 32);
+  MOE_CHECK_ARG(E >= 1 && E <= kMaxExperts);
+  MOE_CHECK_ARG(layout == MOE_LAYOUT_MASKED || layout == MOE_LAYOUT_CONTIG);
+  MOE_CHECK_ARG(counts && row_src && q_out && s_out);
+  MOE_CHECK_ARG(aligned16(q_out) && aligned16(s_out));
+  int64_t G;
+  if (layout == MOE_LAYOUT_MASKED) {
+    MOE_CHECK_ARG(max_m > 0 && static_cast<int64_t>(E) * max_m < (1ll << 31));
+    G = max_m;
+  } else {
+    MOE_CHECK_ARG(offsets && m_indices && rows_capacity >= 0 && rows_capacity < (1ll << 31));
+    MOE_CHECK_ARG(rows_capacity >= moe_contig_rows_bound(T * k, E));
+    MOE_CHECK_ARG(s_out_ld >= rows_capacity);
+    G = s_out_ld;
+  }
+  if (T > 0) {
+    MOE_CHECK_ARG(q && s && topk_ids && dst_row && aligned16(q) && s_ld >= T);
+  }
+  MOE_CHECK_ARG(T * k < (1ll << 31));
+  if (int st = check_device()) return st;
+  cudaStream_t st = as_stream(stream);
+  IndexParams p{topk_ids, T * k, expert_begin, E, layout, max_m, rows_capacity,
+                counts, offsets, m_indices, row_src, dst_row, err};
+  const size_t smem = sizeof(int32_t) * (2 * E + kIdxWarps * E);
+  if (smem > 48 * 1024) {
+    MOE_CUDA_TRY(cudaFuncSetAttribute(permute_index_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(smem)));
+  }
+  permute_index_kernel<<<1, kIdxThreads, smem, st>>>(p);
+  if (int rc = launch_status()) return rc;
+  if (T == 0) return MOE_OK;
+  const int64_t n = T * k;
+  permute_scatter_kernel<<<static_cast<unsigned>((n + 3) / 4), 128, 0, st>>>(
+      q, s, s_ld, dst_row, n, k, H, q_out, s_out, G);
+  return launch_status();
+}
+
+extern "C" int moe_combine(const uint16_t* Y2, int64_t ldy, int64_t y_rows, const int32_t* dst_row,
+                           const float* topk_w, int64_t T, int32_t k, int32_t H, uint16_t* out,
+                           int64_t ldo, int32_t* err, void* stream) {
+  MOE_CHECK_ARG(T >= 0 && k >= 1 && k <= 32 && H > 0 && H % 8 == 0);
+  if (T == 0) return MOE_OK;
+  MOE_CHECK_ARG(Y2 && dst_row && topk_w && out && aligned16(Y2) && aligned16(out));
+  MOE_CHECK_ARG(ldy >= H && ldy % 8 == 0 && ldo >= H && ldo % 8 == 0 && y_rows >= 0);
+  MOE_CHECK_ARG(T < (1ll << 31));
+  if (int st = check_device()) return st;
+  combine_kernel<<<static_cast<unsigned>(T), 128, 0, as_stream(stream)>>>(
+      Y2, ldy, y_rows, dst_row, topk_w, k, H, out, ldo, err);
+  return launch_status();
+}

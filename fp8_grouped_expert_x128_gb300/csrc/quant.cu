@@ -1,0 +1,221 @@
+// 1x128 activation quantisation, 128x128 weight quantisation and the fused
+// SwiGLU + requantisation.  All three are HBM-bound streaming kernels: 16-byte
+// vector loads, one half-warp per 128-element block (8 elements per lane), the
+// block amax reduced with shuffles inside the half-warp, IEEE fp32 divisions
+// (so the bytes match the definition exactly), and a saturating
+// round-to-nearest-even E4M3 conversion in hardware.
+//
+// Definition: per 128-element block, s = fp32(max(amax, 1e-4) / 448) and
+// q = e4m3(fp32(x / s)); the scale array is "packed" MN-major (see moe_fp8.h).
+// The FP8 GEMM of "Deploying DeepSeek on GB200 NVL72 with PD and Large Scale
+// EP (Part I)", section "Implementation details" (DeepGEMM bullet), consumes
+// exactly these quantised inputs with their packed scales.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr float kFloor = 1e-4f;
+constexpr float kE4M3Max = 448.0f;
+
+__device__ __forceinline__ float half_warp_max(float v) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// Quantise 8 values with scale s into 8 E4M3 bytes (element 0 in the low byte).
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t a = e4m3x2_rn_satfinite(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
+    const uint32_t b =
+        e4m3x2_rn_satfinite(__fdiv_rn(f[4 + 2 * i], s), __fdiv_rn(f[4 + 2 * i + 1], s));
+    lo |= a << (16 * i);
+    hi |= b << (16 * i);
+  }
+  return make_uint2(lo, hi);
+}
+
+__device__ __forceinline__ float block_scale(float amax) {
+  return __fdiv_rn(fmaxf(amax, kFloor), kE4M3Max);
+}
+
+// ---------------------------------------------------------------- a1
+// One warp covers 256 columns of one row: lanes 0-15 block 2w, 16-31 block 2w+1.
+__global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __restrict__ x,
+                                                          int64_t M, int64_t KB, int64_t ldx,
+                                                          uint8_t* __restrict__ q, int64_t ldq,
+                                                          float* __restrict__ s, int64_t s_ld) {
+  const int64_t warps_per_row = (KB + 1) / 2;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t m = gw / warps_per_row;
+  if (m >= M) return;
+  const int64_t kb = (gw % warps_per_row) * 2 + (lane >> 4);
+  const bool active = kb < KB;
+  float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  const int64_t col = kb * 128 + (lane & 15) * 8;
+  if (active) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(x + m * ldx + col));
+    unpack_bf16x8(u, f);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  amax = half_warp_max(amax);
+  if (!active) return;
+  const float sc = block_scale(amax);
+  *reinterpret_cast<uint2*>(q + m * ldq + col) = quant8(f, sc);
+  if ((lane & 15) == 0) s[kb * s_ld + m] = sc;
+}
+
+// ---------------------------------------------------------------- a3
+// One CTA of 256 threads per 128x128 tile; thread t covers columns
+// (t % 16) * 8 .. +7 of rows t/16 + 16 i, i = 0..7.
+__global__ void __launch_bounds__(256) quant_128x128_kernel(const uint16_t* __restrict__ w,
+                                                            int64_t N, int64_t K,
+                                                            uint8_t* __restrict__ q,
+                                                            float* __restrict__ s) {
+  const int64_t NB = N / 128, KB = K / 128;
+  const int64_t tile = blockIdx.x;  // over E * NB * KB
+  const int64_t e = tile / (NB * KB);
+  const int64_t nb = (tile / KB) % NB;
+  const int64_t kb = tile % KB;
+  const int t = threadIdx.x;
+  const int c8 = t & 15, r0 = t >> 4;
+  const uint16_t* base = w + (e * N + nb * 128) * K + kb * 128 + c8 * 8;
+  float f[8][8];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(base + (r0 + 16 * i) * K));
+    unpack_bf16x8(u, f[i]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[i][j]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  __shared__ float red[8];
+  if ((t & 31) == 0) red[t >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+  const float sc = block_scale(amax);
+  uint8_t* qb = q + (e * N + nb * 128) * K + kb * 128 + c8 * 8;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(qb + (r0 + 16 * i) * K) = quant8(f[i], sc);
+  if (t == 0) s[(e * NB + nb) * KB + kb] = sc;
+}
+
+// ---------------------------------------------------------------- a5
+// h = silu(g) * u in fp32, quantised by the a1 rule.  Row selection by masked
+// counts or by contiguous m_indices.
+__global__ void __launch_bounds__(256) swiglu_quant_kernel(
+    const uint16_t* __restrict__ y1, int64_t rows, int64_t I, const int32_t* __restrict__ counts,
+    int64_t max_m, const int32_t* __restrict__ m_indices, uint8_t* __restrict__ q,
+    float* __restrict__ s, int64_t G) {
+  const int64_t KB = I / 128;
+  const int64_t warps_per_row = (KB + 1) / 2;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t r = gw / warps_per_row;
+  if (r >= rows) return;
+  if (counts != nullptr) {
+    const int64_t e = r / max_m;
+    if (r - e * max_m >= static_cast<int64_t>(__ldg(counts + e))) return;
+  } else if (m_indices != nullptr) {
+    if (__ldg(m_indices + r) < 0) return;
+  }
+  const int64_t kb = (gw % warps_per_row) * 2 + (lane >> 4);
+  const bool active = kb < KB;
+  float h[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  const int64_t col = kb * 128 + (lane & 15) * 8;
+  if (active) {
+    const uint16_t* row = y1 + r * 2 * I;
+    float g[8], u[8];
+    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(row + col)), g);
+    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(row + I + col)), u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = __fdiv_rn(g[i], 1.0f + expf(-g[i])) * u[i];
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(h[i]));
+  amax = half_warp_max(amax);
+  if (!active) return;
+  const float sc = block_scale(amax);
+  *reinterpret_cast<uint2*>(q + r * I + col) = quant8(h, sc);
+  if ((lane & 15) == 0) {
+    const int64_t grp = r / G, pos = r - grp * G;
+    s[(grp * KB + kb) * G + pos] = sc;
+  }
+}
+
+inline unsigned grid_for_warps(int64_t warps) {
+  return static_cast<unsigned>((warps * 32 + 255) / 256);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_quant_fp8(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                             int64_t ldq, float* s, int64_t s_ld, int32_t* err, void* stream) {
+  (void)err;
+  MOE_CHECK_ARG(M >= 0 && K > 0 && K % 128 == 0);
+  if (M == 0) return MOE_OK;
+  MOE_CHECK_ARG(x && q && s && aligned16(x) && aligned16(q) && aligned16(s));
+  MOE_CHECK_ARG(ldx >= K && ldx % 8 == 0 && ldq >= K && ldq % 16 == 0 && s_ld >= M);
+  if (int st = check_device()) return st;
+  const int64_t warps = M * ((K / 128 + 1) / 2);
+  quant_1x128_kernel<<<grid_for_warps(warps), 256, 0, as_stream(stream)>>>(x, M, K / 128, ldx, q,
+                                                                          ldq, s, s_ld);
+  return launch_status();
+}
+
+extern "C" int moe_quant_weight_fp8(const uint16_t* w, int64_t E, int64_t N, int64_t K, uint8_t* q,
+                                    float* s, void* stream) {
+  MOE_CHECK_ARG(E >= 0 && N > 0 && K > 0 && N % 128 == 0 && K % 128 == 0);
+  if (E == 0) return MOE_OK;
+  MOE_CHECK_ARG(w && q && s && aligned16(w) && aligned16(q) && aligned16(s));
+  if (int st = check_device()) return st;
+  const int64_t tiles = E * (N / 128) * (K / 128);
+  MOE_CHECK_ARG(tiles < (1ll << 31));
+  quant_128x128_kernel<<<static_cast<unsigned>(tiles), 256, 0, as_stream(stream)>>>(w, N, K, q, s);
+  return launch_status();
+}
+
+extern "C" int moe_swiglu_quant(const uint16_t* Y1, int64_t rows, int32_t I, const int32_t* counts,
+                                int32_t max_m, const int32_t* m_indices, uint8_t* q, float* s,
+                                int64_t s_ld, int32_t* err, void* stream) {
+  (void)err;
+  MOE_CHECK_ARG(rows >= 0 && I > 0 && I % 128 == 0);
+  if (rows == 0) return MOE_OK;
+  MOE_CHECK_ARG(Y1 && q && s && aligned16(Y1) && aligned16(q) && aligned16(s));
+  int64_t G;
+  if (counts != nullptr) {
+    MOE_CHECK_ARG(max_m > 0 && rows % max_m == 0);
+    G = max_m;
+  } else {
+    MOE_CHECK_ARG(s_ld >= rows);
+    G = s_ld;
+  }
+  if (int st = check_device()) return st;
+  const int64_t warps = rows * ((I / 128 + 1) / 2);
+  swiglu_quant_kernel<<<grid_for_warps(warps), 256, 0, as_stream(stream)>>>(
+      Y1, rows, I, counts, max_m, counts ? nullptr : m_indices, q, s, G);
+  return launch_status();
+}

@@ -1,0 +1,255 @@
+/*
+ * moe_fp8.h -- C ABI of the GB300 (sm_103a) routed-expert FP8 MoE FFN library.
+ *
+ * The hot path of DeepSeek-style MoE serving on one GPU: 1x128 E4M3 activation
+ * quantisation with fp32 scales, permutation into a grouped layout, a grouped
+ * FP8 GEMM against 128x128 block-scaled E4M3 expert weights, SwiGLU with FP8
+ * requantisation, a second grouped GEMM, and the top-k-weighted combine back to
+ * token order.
+ *
+ * Sources.  "Deploying DeepSeek on GB200 NVL72 with PD and Large Scale EP
+ * (Part I)", section "Implementation details", DeepGEMM bullet: an FP8 GEMM
+ * library for Blackwell built on UMMA whose API quantises and packs the input
+ * scales.  "Deploying DeepSeek with PD Disaggregation and Large-Scale Expert
+ * Parallelism on 96 H100 GPUs", section "DeepGEMM integration": two grouped
+ * GEMMs for MoE, one for prefill (fed by DeepEP's normal dispatch -> the
+ * contiguous layout here) and one for decode (fed by the CUDA-Graph-compatible
+ * low-latency dispatch -> the masked layout here).  The pages give no formulas;
+ * the definitions below are this library's, each stated where it applies.
+ *
+ * Conventions for every call:
+ *  - Pointers marked "device" are device pointers, allocated and owned by the
+ *    caller.  The library never allocates device memory and never synchronises,
+ *    except moe_read_device_status.  Work is enqueued on `stream` (a
+ *    cudaStream_t passed as void*; NULL = the legacy default stream), so a call
+ *    sequence can be captured in a CUDA graph.
+ *  - bf16 tensors are passed as uint16_t bit patterns; FP8 tensors are uint8_t
+ *    OCP E4M3FN codes (bias 7, max 448, NaN 0x7F/0xFF).
+ *  - Every base pointer must be 16-byte aligned; K, H and I are multiples of 128.
+ *  - Return value: MOE_OK or a negative MOE_ERR_*.  Argument errors are found on
+ *    the host before anything is enqueued (nothing is launched then).  Errors
+ *    only the GPU can see (a count above max_m, an expert id or row index out of
+ *    range, a pipeline wait that ran past its time limit) are OR-ed as
+ *    MOE_DEV_* bits into the caller's device word `err` (may be NULL to
+ *    ignore); read them with moe_read_device_status.  No kernel traps.
+ *  - Scale layout ("packed", MN-major): for a tensor with rows r and 128-column
+ *    blocks kb, rows are split into groups of G rows; the fp32 scale of (r, kb)
+ *    sits at s[((r / G) * KB + kb) * G + r % G].  The masked layout uses
+ *    G = max_m (one group per expert: s[e][kb][m]); the token-order and
+ *    contiguous layouts use one group, G = s_ld >= rows (s[kb][r]).
+ */
+#ifndef MOE_FP8_H_
+#define MOE_FP8_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status ------------------------------------------------------------ */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)  /* null/misaligned pointer, bad size or stride      */
+#define MOE_ERR_UNSUPPORTED (-2)  /* not an sm_103/sm_100-family device, shape limits  */
+#define MOE_ERR_CUDA (-3)         /* a CUDA runtime/driver call failed                 */
+#define MOE_ERR_OVERFLOW (-4)     /* device: a masked count exceeded max_m (clamped)   */
+#define MOE_ERR_TIMEOUT (-5)      /* device: a pipeline wait ran past its time limit   */
+#define MOE_ERR_BAD_INDEX (-6)    /* device: an expert id / row index out of range     */
+
+/* bits of the device error word */
+#define MOE_DEV_OVERFLOW 0x1
+#define MOE_DEV_TIMEOUT 0x2
+#define MOE_DEV_BAD_INDEX 0x4
+
+#define MOE_LAYOUT_MASKED 0
+#define MOE_LAYOUT_CONTIG 1
+
+/* GEMM flags */
+#define MOE_GEMM_DEFAULT 0
+#define MOE_GEMM_FORCE_TOKENS_M 0x1   /* masked: force the tokens-as-M tile kernel      */
+#define MOE_GEMM_FORCE_WEIGHTS_M 0x2  /* masked: force the weights-as-M (swap AB) kernel */
+#define MOE_GEMM_DEBUG_STALL 0x100    /* test only: the TMA producer never issues, so the
+                                         consumer's bounded wait expires and the call
+                                         reports MOE_DEV_TIMEOUT (no hang, no trap)      */
+
+/* Human-readable name of a status code. Never NULL. */
+const char *moe_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int moe_version(void);
+
+/*
+ * Synchronise `stream`, read the device error word `err` (device, int32),
+ * clear it to 0, and return in *status_out the most severe MOE_ERR_* it held
+ * (BAD_INDEX over TIMEOUT over OVERFLOW; MOE_OK if clear).  *raw_bits_out (may
+ * be NULL) receives the raw MOE_DEV_* bits.  The only call that synchronises.
+ */
+int moe_read_device_status(int32_t *err, void *stream, int *status_out, int32_t *raw_bits_out);
+
+/*
+ * a1 -- 1x128 activation quantisation (moe_quant_fp8).
+ * Per row m and 128-column block kb of x:
+ *   amax = max |x[m, kb*128 .. kb*128+127]|
+ *   s    = fp32( max(amax, 1e-4) / 448 )            (IEEE float32 division)
+ *   q    = e4m3_rne_satfinite( fp32( x / s ) )       (IEEE float32 division)
+ * x  : device bf16 [M, K], row stride ldx (elements).
+ * q  : device uint8 [M, K], row stride ldq (bytes).
+ * s  : device fp32, one group: s[kb * s_ld + m], s_ld >= M.
+ * M may be 0 (nothing is launched).
+ */
+int moe_quant_fp8(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                  uint8_t *q, int64_t ldq, float *s, int64_t s_ld,
+                  int32_t *err, void *stream);
+
+/*
+ * a3 -- 128x128 block weight quantisation (set-up, not on the timed path).
+ * The a1 rule with amax taken over each 128x128 tile.
+ * w : device bf16 [E, N, K] (K-major: the GEMM's B operand, out x in).
+ * q : device uint8 [E, N, K];  s : device fp32 [E, N/128, K/128].
+ */
+int moe_quant_weight_fp8(const uint16_t *w, int64_t E, int64_t N, int64_t K,
+                         uint8_t *q, float *s, void *stream);
+
+/*
+ * Rows a contiguous-layout buffer must be able to hold for `assignments`
+ * routed rows over E experts when each segment is padded to a multiple of 128.
+ */
+int64_t moe_contig_rows_bound(int64_t assignments, int32_t E);
+
+/*
+ * a2 -- permute token-order FP8 rows into the grouped layout (moe_permute).
+ * Assignment i = t*k + j goes to local expert e = topk_ids[t, j] - expert_begin
+ * when 0 <= e < E (other ids are another rank's experts and are skipped).
+ * Within an expert, rows keep ascending i (deterministic, stable).
+ *
+ * q, s      : device, token order, as written by moe_quant_fp8 (rows T, row
+ *             stride H bytes; s[kb * s_ld + t]).
+ * topk_ids  : device int32 [T, k].
+ * layout = MOE_LAYOUT_MASKED: expert e owns rows [e*max_m, (e+1)*max_m) of
+ *   q_out (device uint8 [E*max_m, H]) and s_out (device fp32 [E, H/128, max_m]).
+ *   counts[e] (device int32 [E]) = rows kept = min(arrivals, max_m); arrivals past
+ *   max_m get dst_row = -1 and set MOE_DEV_OVERFLOW.  row_src: [E*max_m].
+ *   Rows >= counts[e] of q_out/s_out are left untouched.  rows_capacity is
+ *   ignored; offsets and m_indices may be NULL.
+ * layout = MOE_LAYOUT_CONTIG: expert segments follow each other, each padded to
+ *   a multiple of 128 rows.  offsets (device int32 [E+1]): first row of each
+ *   segment, offsets[E] = rows used.  m_indices (device int32 [rows_capacity]):
+ *   owning expert of each real row, -1 on padding and past offsets[E].
+ *   q_out: [rows_capacity, H]; s_out: s_out[kb * s_out_ld + row], s_out_ld >=
+ *   rows_capacity.  counts[e] = arrivals.  rows_capacity must be at least
+ *   moe_contig_rows_bound(T*k, E).  row_src: [rows_capacity].  Padding rows of
+ *   q_out/s_out are left untouched.
+ * row_src[row] = i of the assignment stored there, -1 elsewhere.
+ * dst_row[i]   (device int32 [T*k]) = destination row, -1 if not stored.
+ * Limits: E <= 1024, k <= 32.
+ */
+int moe_permute(const uint8_t *q, const float *s, int64_t s_ld,
+                const int32_t *topk_ids, int64_t T, int32_t H, int32_t k,
+                int32_t expert_begin, int32_t E, int32_t layout, int32_t max_m,
+                uint8_t *q_out, float *s_out, int64_t s_out_ld,
+                int32_t *counts, int32_t *offsets, int32_t *m_indices,
+                int32_t *row_src, int32_t *dst_row, int64_t rows_capacity,
+                int32_t *err, void *stream);
+
+/*
+ * a4 / a6 -- grouped FP8 GEMM with block-scaled operands.
+ *   D[r, n] = bf16_rne( sum_kb  sA[r, kb] * sB[e, n/128, kb]
+ *                              * sum_{k in kb} A[r, k] * B[e, n, k] )
+ * where e is the expert owning row r.  E4M3 products are exact; the inner sum
+ * runs on the tcgen05 tensor cores into TMEM, and each 128-deep block partial
+ * is scaled and accumulated in fp32 by the epilogue warps.
+ * B  : device uint8 [E, N, K] (K-major), sB: device fp32 [E, N/128, K/128].
+ * N % 128 == 0, K % 128 == 0.
+ *
+ * moe_gemm_fp8_contig -- contiguous (prefill) layout, as moe_permute writes it:
+ *   A [M_capacity, K] (row stride lda), sA[kb * sA_ld + r], offsets [E+1],
+ *   m_indices [M_capacity]; D row stride ldd.  Rows with m_indices == -1 and
+ *   rows >= offsets[E] are not written.  Segments must start at multiples of 128.
+ */
+int moe_gemm_fp8_contig(const uint8_t *A, int64_t lda, const float *sA, int64_t sA_ld,
+                        const uint8_t *B, const float *sB,
+                        const int32_t *offsets, const int32_t *m_indices, int64_t M_capacity,
+                        int32_t E, int32_t N, int32_t K,
+                        uint16_t *D, int64_t ldd, int32_t flags, int32_t *err, void *stream);
+
+/*
+ * moe_gemm_fp8_masked -- masked (decode) layout, as moe_permute writes it:
+ *   A [E, max_m, K], sA [E, K/128, max_m], counts [E] (device; read on the
+ *   GPU only, so the call is graph-capturable), D [E, max_m, N].
+ *   Rows >= counts[e] of D are left untouched; counts[e] > max_m is clamped
+ *   and sets MOE_DEV_OVERFLOW.  expected_m (>= 0) is a host-side hint of the
+ *   typical count used to pick the tile kernel (0 = unknown).
+ */
+int moe_gemm_fp8_masked(const uint8_t *A, const float *sA, const uint8_t *B, const float *sB,
+                        const int32_t *counts, int32_t E, int32_t max_m, int32_t N, int32_t K,
+                        int32_t expected_m, uint16_t *D, int32_t flags, int32_t *err,
+                        void *stream);
+
+/*
+ * a5 -- fused SwiGLU + 1x128 requantisation (moe_swiglu_quant).
+ *   h[r, i] = silu(g) * u,  g = Y1[r, i], u = Y1[r, I + i]   (gate first, then up)
+ * computed in fp32 (silu(g) = g / (1 + exp(-g))), never rounded to bf16, then
+ * quantised by the a1 rule into q [rows, I] (row stride I) and s (groups of G rows).
+ * Y1 : device bf16 [rows, 2I] (row stride 2I).
+ * Row selection: masked -> counts != NULL, G = max_m, row r is processed iff
+ *   r % max_m < counts[r / max_m]; contig -> counts == NULL, m_indices != NULL,
+ *   G = s_ld, row r processed iff r < rows and m_indices[r] >= 0.
+ * Unprocessed rows of q and s are left untouched.
+ */
+int moe_swiglu_quant(const uint16_t *Y1, int64_t rows, int32_t I,
+                     const int32_t *counts, int32_t max_m, const int32_t *m_indices,
+                     uint8_t *q, float *s, int64_t s_ld, int32_t *err, void *stream);
+
+/*
+ * a7 -- top-k-weighted combine back to token order (moe_combine).
+ *   out[t, :] = bf16_rne( sum_j  w[t, j] * Y2[dst_row[t*k + j], :] )
+ * fp32 accumulation in j order; entries with dst_row == -1 are skipped (a token
+ * with none gets zeros).  Y2: device bf16 rows of H (row stride ldy),
+ * dst_row: device int32 [T*k], topk_w: device fp32 [T, k], out: device bf16
+ * [T, H] (row stride ldo).  dst_row values must be < y_rows (else
+ * MOE_DEV_BAD_INDEX and the entry is skipped).
+ */
+int moe_combine(const uint16_t *Y2, int64_t ldy, int64_t y_rows,
+                const int32_t *dst_row, const float *topk_w, int64_t T, int32_t k, int32_t H,
+                uint16_t *out, int64_t ldo, int32_t *err, void *stream);
+
+/*
+ * a8 -- the whole routed-expert FFN on one stream, no host synchronisation:
+ *   moe_quant_fp8 -> moe_permute -> GEMM1 (W13) -> moe_swiglu_quant -> GEMM2 (W2)
+ *   -> moe_combine.
+ * Weights: w13 [E, 2I, H] (gate rows [0, I), up rows [I, 2I)) with w13_s
+ * [E, 2I/128, H/128]; w2 [E, H, I] with w2_s [E, H/128, I/128] (device).
+ * workspace: device, at least moe_ffn_workspace_size(desc) bytes, 256-byte
+ * aligned; holds every intermediate.  stage_events (optional, may be NULL):
+ * 7 cudaEvent_t handles recorded on `stream` before stage 1 and after each of
+ * the six stages, for per-stage timing.
+ */
+typedef struct moe_ffn_desc {
+  int64_t T;              /* tokens (rows of x and out)                 */
+  int32_t H, I, k;        /* hidden, intermediate, routing slots/token  */
+  int32_t expert_begin;   /* global id of local expert 0               */
+  int32_t E;              /* local experts                              */
+  int32_t layout;         /* MOE_LAYOUT_MASKED / MOE_LAYOUT_CONTIG      */
+  int32_t max_m;          /* masked: rows per expert                    */
+  int32_t expected_m;     /* masked: count hint for tile selection (0)  */
+  int32_t gemm_flags;     /* MOE_GEMM_* for both GEMMs                  */
+  const uint16_t *x;      /* [T, H] bf16                                */
+  const int32_t *topk_ids;/* [T, k]                                     */
+  const float *topk_w;    /* [T, k]                                     */
+  const uint8_t *w13;
+  const float *w13_s;
+  const uint8_t *w2;
+  const float *w2_s;
+  uint16_t *out;          /* [T, H] bf16                                */
+  int32_t *err;           /* device error word (may be NULL)            */
+  void **stage_events;    /* optional 7 cudaEvent_t                     */
+} moe_ffn_desc;
+
+size_t moe_ffn_workspace_size(const moe_ffn_desc *desc);
+int moe_ffn(const moe_ffn_desc *desc, void *workspace, size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_FP8_H_ */

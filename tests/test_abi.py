@@ -1,0 +1,93 @@
+"""The C-ABI library: it builds, loads without a GPU, exports every entry point
+include/moe_fp8.h declares, and rejects bad arguments on the host before any
+CUDA call (no compute is attempted here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def so():
+    from fp8_grouped_expert_x128_gb300 import _build
+    path = _build.build()
+    return ctypes.CDLL(path), path
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_hot_path(so):
+    names = _declared_functions()
+    for required in ("moe_quant_fp8", "moe_permute", "moe_gemm_fp8_contig", "moe_gemm_fp8_masked",
+                     "moe_swiglu_quant", "moe_combine", "moe_ffn", "moe_ffn_workspace_size",
+                     "moe_read_device_status", "moe_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(so):
+    lib, path = so
+    missing = [n for n in sorted(_declared_functions()) if not hasattr(lib, n)]
+    assert not missing, missing
+    import fp8_grouped_expert_x128_gb300 as moe
+    assert set(moe.EXPORTED) <= _declared_functions()
+
+
+def test_status_strings_and_version(so):
+    import fp8_grouped_expert_x128_gb300 as moe
+    assert moe.moe_status_string(0) == "MOE_OK"
+    assert moe.moe_status_string(-5) == "MOE_ERR_TIMEOUT"
+    assert moe.moe_status_string(12345) == "MOE_ERR_UNKNOWN"
+    assert moe.moe_version() >= 100
+
+
+def test_host_side_argument_validation(so):
+    lib, _ = so
+    lib.moe_quant_fp8.restype = ctypes.c_int
+    i64, p = ctypes.c_int64, ctypes.c_void_p
+    # K not a multiple of 128 -> rejected before any CUDA call
+    rc = lib.moe_quant_fp8(p(16), i64(4), i64(100), i64(100), p(16), i64(100), p(16), i64(4), None, None)
+    assert rc == -1
+    # null pointers
+    rc = lib.moe_quant_fp8(None, i64(4), i64(128), i64(128), None, i64(128), None, i64(4), None, None)
+    assert rc == -1
+    # misaligned pointer
+    rc = lib.moe_quant_fp8(p(18), i64(4), i64(128), i64(128), p(16), i64(128), p(16), i64(4), None, None)
+    assert rc == -1
+    # empty input is a no-op
+    rc = lib.moe_quant_fp8(None, i64(0), i64(128), i64(128), None, i64(128), None, i64(0), None, None)
+    assert rc == 0
+    lib.moe_gemm_fp8_masked.restype = ctypes.c_int
+    i32 = ctypes.c_int32
+    rc = lib.moe_gemm_fp8_masked(p(16), p(16), p(16), p(16), p(16), i32(4), i32(128), i32(200),
+                                 i32(256), i32(0), p(16), i32(0), None, None)
+    assert rc == -1                                   # N % 128 != 0
+    rc = lib.moe_permute(p(16), p(16), i64(4), p(16), i64(4), ctypes.c_int32(256), ctypes.c_int32(2),
+                         i32(0), i32(2000), i32(0), i32(128), p(16), p(16), i64(128), p(16), None,
+                         None, p(16), p(16), i64(0), None, None)
+    assert rc == -1                                   # E above the 1024 limit
+
+
+def test_contig_bound_and_workspace_plan(so):
+    import fp8_grouped_expert_x128_gb300 as moe
+    assert moe.moe_contig_rows_bound(0, 4) == 3 * 128
+    assert moe.moe_contig_rows_bound(32768, 9) == (32768 + 9 * 127) // 128 * 128
+    d = moe.moe_ffn_desc(T=64, H=256, I=128, k=2, expert_begin=0, E=4, layout=0, max_m=128)
+    ws = moe.moe_ffn_workspace_size(d)
+    rows = 4 * 128
+    assert ws >= rows * 256 + rows * 256 * 2 + rows * 128 + rows * 256 * 2
+    assert ws % 256 == 0
+    d.H = 200
+    assert moe.moe_ffn_workspace_size(d) == 0         # invalid descriptor

@@ -1,0 +1,138 @@
+"""End-to-end parity of moe_ffn with the oracle chain on the configs, plus the
+stage-fed check: each GPU stage fed the oracle's previous-stage output and
+compared with the oracle's own next stage.
+
+Configs: the tiny masked config in full; the EP72-like and 48-GPU-domain
+decode configs in full (every routed row); the all-experts decode layer and the
+prefill (contiguous) config on sampled tokens, each sampled token's output
+computed by the oracle alone from x, its routing and its experts' weights."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from bench import build_workload, make_desc
+from tests.gpu_common import (bits, check_tol, from_bits, oracle_weights, to_dev, u8)
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_ffn(lib, wl):
+    T, H = wl["T"], wl["cfg"].H
+    out = torch.full((T, H), 0x7E57, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    err = lib.new_error_word()
+    desc = make_desc(wl, out, err=err)
+    ws = lib.alloc_workspace(desc)
+    lib.moe_ffn(desc, ws)
+    st, _ = lib.moe_read_device_status(err)
+    return bits(out), st
+
+
+def _oracle_full(name, wl):
+    cfg = wl["cfg"]
+    r = wl["routing"]
+    e_all = tuple(range(cfg.E))
+    w13q, w13s = oracle_weights(name, "w13", e_all)
+    w2q, w2s = oracle_weights(name, "w2", e_all)
+    return oracle.ffn_chain(bits(wl["x"]), r["topk_ids"], r["topk_w"], r["expert_begin"], cfg.E,
+                            cfg.layout, cfg.max_m, w13q, w13s, w2q, w2s), (w13q, w13s, w2q, w2s)
+
+
+def _oracle_tokens(name, wl, tokens):
+    """The oracle chain restricted to `tokens` (rows are independent)."""
+    cfg = wl["cfg"]
+    r = wl["routing"]
+    xb = bits(wl["x"])[tokens]
+    q, s = oracle.quant_1x128(oracle.bf16_decode(xb).astype(np.float32))
+    ids = r["topk_ids"][tokens] - r["expert_begin"]
+    need = tuple(sorted({int(e) for e in ids.reshape(-1) if 0 <= e < cfg.E}))
+    w13q, w13s = oracle_weights(name, "w13", need)
+    w2q, w2s = oracle_weights(name, "w2", need)
+    slot = {e: i for i, e in enumerate(need)}
+    out = []
+    for i, t in enumerate(tokens):
+        y2, w = [], []
+        for j in range(r["k"]):
+            e = int(r["topk_ids"][t, j]) - r["expert_begin"]
+            if not 0 <= e < cfg.E:
+                continue
+            n = slot[e]
+            y1 = oracle.bf16_encode(oracle.gemm_block_scaled(q[i:i + 1], s[:, i:i + 1], w13q[n], w13s[n]))
+            q2, s2 = oracle.swiglu_quant(y1)
+            y2.append(oracle.bf16_encode(oracle.gemm_block_scaled(q2, s2, w2q[n], w2s[n]))[0])
+            w.append(float(r["topk_w"][t, j]))
+        out.append(oracle.combine(np.stack(y2), np.arange(len(w)), np.array([w], np.float32))[0])
+    return np.stack(out)
+
+
+def test_ffn_tiny_config_end_to_end(lib):
+    wl = build_workload("c1")
+    got, st = _gpu_ffn(lib, wl)
+    assert st == 0
+    ref, _ = _oracle_full("c1", wl)
+    check_tol(got, ref["out"], "c1 ffn")
+
+
+def test_ffn_tiny_config_stage_fed(lib):
+    """Each GPU stage on the oracle's previous-stage output."""
+    wl = build_workload("c1")
+    cfg = wl["cfg"]
+    ref, (w13q, w13s, w2q, w2s) = _oracle_full("c1", wl)
+    E, M, I, H = cfg.E, cfg.max_m, cfg.I, cfg.H
+    counts = to_dev(ref["perm"]["counts"].astype(np.int32))
+    # GEMM1 on the oracle's permuted activations
+    y1 = torch.empty((E, M, 2 * I), dtype=torch.bfloat16, device="cuda")
+    lib.moe_gemm_fp8_masked(to_dev(ref["perm"]["q"].reshape(E, M, H)), to_dev(ref["perm"]["s"]),
+                            to_dev(w13q), to_dev(w13s), counts, y1)
+    v = ref["valid"]
+    check_tol(bits(y1).reshape(E * M, -1)[v], ref["y1"][v], "stage GEMM1")
+    # SwiGLU+quant on the oracle's GEMM1 output: bytes/scales as in test_gpu_swiglu_combine
+    q2 = torch.empty((E * M, I), dtype=torch.uint8, device="cuda")
+    s2 = torch.empty((E, I // 128, M), dtype=torch.float32, device="cuda")
+    lib.moe_swiglu_quant(from_bits(ref["y1"]), q2, s2, counts=counts, max_m=M)
+    torch.cuda.synchronize()
+    mism = (u8(q2)[v] != ref["q2"][v]).mean()
+    assert mism < 1e-3
+    # GEMM2 on the oracle's requantised activations
+    y2 = torch.empty((E, M, H), dtype=torch.bfloat16, device="cuda")
+    lib.moe_gemm_fp8_masked(to_dev(ref["q2"].reshape(E, M, I)), to_dev(ref["s2"]), to_dev(w2q),
+                            to_dev(w2s), counts, y2)
+    check_tol(bits(y2).reshape(E * M, -1)[v], ref["y2"][v], "stage GEMM2")
+    # combine on the oracle's GEMM2 output
+    out = torch.empty((wl["T"], H), dtype=torch.bfloat16, device="cuda")
+    lib.moe_combine(from_bits(ref["y2"]), to_dev(ref["perm"]["dst_row"].astype(np.int32)),
+                    wl["topk_w"], out)
+    check_tol(bits(out), ref["out"], "stage combine")
+
+
+@pytest.mark.parametrize("name", ["c2", "c4"])
+def test_ffn_decode_configs_full(lib, name):
+    wl = build_workload(name)
+    got, st = _gpu_ffn(lib, wl)
+    assert st in (0, lib.MOE_ERR_OVERFLOW)
+    ref, _ = _oracle_full(name, wl)
+    assert (st == lib.MOE_ERR_OVERFLOW) == bool(ref["perm"]["overflow"])
+    check_tol(got, ref["out"], f"{name} ffn")
+
+
+def test_ffn_all_experts_layer_sampled_tokens(lib):
+    wl = build_workload("c5")
+    got, st = _gpu_ffn(lib, wl)
+    assert st == 0
+    tokens = [0, 63]
+    check_tol(got[tokens], _oracle_tokens("c5", wl, tokens), "c5 ffn tokens")
+    assert np.isfinite(oracle.bf16_decode(got)).all()
+
+
+def test_ffn_prefill_contiguous_sampled_tokens(lib):
+    wl = build_workload("c3")
+    got, st = _gpu_ffn(lib, wl)
+    assert st == 0
+    r = wl["routing"]
+    rng = np.random.default_rng(21)
+    tokens = []
+    for e in range(wl["cfg"].E):                 # a few tokens of every expert
+        tokens += list(rng.choice(np.nonzero(r["topk_ids"][:, 0] == e)[0], 3, replace=False))
+    tokens = sorted(tokens)
+    check_tol(got[tokens], _oracle_tokens("c3", wl, tokens), "c3 ffn tokens")

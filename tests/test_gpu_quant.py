@@ -1,0 +1,109 @@
+"""Parity of the quantisation kernels with the oracle: bit-exact FP8 bytes and
+scales (the GPU divides with IEEE float32 like the definition)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.gpu_common import (SENTINEL_F32, SENTINEL_U8, activations_bits, bits, from_bits,
+                              oracle_weights, to_dev, u8)
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_quant(lib, xbits, s_ld=None):
+    M, K = xbits.shape
+    x = from_bits(xbits)
+    s_ld = s_ld or max(4, (M + 3) // 4 * 4)
+    q = torch.full((M, K), SENTINEL_U8, dtype=torch.uint8, device="cuda")
+    s = torch.full((K // 128, s_ld), SENTINEL_F32, dtype=torch.float32, device="cuda")
+    lib.moe_quant_fp8(x, q, s, s_ld)
+    torch.cuda.synchronize()
+    return u8(q), s.cpu().numpy()
+
+
+def _assert_quant_equal(lib, xbits):
+    q, s = _gpu_quant(lib, xbits)
+    rq, rs = oracle.quant_1x128(oracle.bf16_decode(xbits).astype(np.float32))
+    M = xbits.shape[0]
+    assert np.array_equal(s[:, :M], rs), "scales differ"
+    assert (s[:, M:] == SENTINEL_F32).all(), "scale padding columns were written"
+    mism = np.nonzero(q != rq)
+    assert mism[0].size == 0, f"{mism[0].size} codes differ, first at {mism[0][0]},{mism[1][0]}"
+
+
+def test_quant_tiny_config_bitexact(lib):
+    _assert_quant_equal(lib, activations_bits("c1", 64))
+
+
+def test_quant_every_bf16_value(lib):
+    # Every finite bf16 value with |v| <= 448 (the range a block can hold once its
+    # amax is 448), 127 per block next to a 448 that pins s = 1, so q = e4m3(v).
+    allv = oracle.bf16_decode(np.arange(65536, dtype=np.uint32).astype(np.uint16))
+    keep = np.isfinite(allv) & (np.abs(allv) <= 448.0)
+    vals = np.arange(65536, dtype=np.uint32).astype(np.uint16)[keep]
+    n_blocks = -(-vals.size // 127)
+    blocks = np.full((n_blocks, 128), 0, dtype=np.uint16)
+    blocks[:, 0] = oracle.bf16_encode(np.array([448.0]))[0]
+    flat = blocks[:, 1:].reshape(-1)
+    flat[:vals.size] = vals
+    blocks[:, 1:] = flat.reshape(n_blocks, 127)
+    rows = -(-n_blocks // 4)
+    xb = np.zeros((rows * 4, 128), dtype=np.uint16)
+    xb[:n_blocks] = blocks
+    xb = xb.reshape(rows, 512)
+    q, s = _gpu_quant(lib, xb)
+    assert (s[:, :n_blocks // 4] == 1.0).all()
+    ref = oracle.e4m3_encode(oracle.bf16_decode(xb))
+    assert np.array_equal(q, ref)
+
+
+def test_quant_edge_cases(lib):
+    rng = np.random.default_rng(5)
+    M, K = 37, 384                     # M not a multiple of 4, three blocks
+    x = rng.standard_normal((M, K))
+    x[0] = 0.0                          # all-zero row: floor scale, zero codes
+    x[1, :128] = -0.0                   # negative zeros keep their sign
+    x[2] *= 1e-30                       # below the floor: amax < 1e-4
+    x[3] *= 1e4                         # large values
+    x[4, 5] = 3.0e38                    # near the bf16 maximum
+    x[5, :] = 2.0 ** -20                # constant block
+    x[6, 130] = -7.0                    # negative amax
+    xb = oracle.bf16_encode(x)
+    _assert_quant_equal(lib, xb)
+    q, s = _gpu_quant(lib, xb)
+    assert (q[0] == 0).all() and (q[1, :128] == 0x80).all()
+    assert q[6, 130] == 0xFE
+
+
+def test_quant_decode_batch_full_size(lib):
+    r = synth.make_routing(synth.get_config("c4"))
+    _assert_quant_equal(lib, activations_bits("c4", r["T"]))
+
+
+def test_quant_prefill_outliers_sample(lib):
+    # the prefill activations carry 1% outliers at 20x
+    _assert_quant_equal(lib, activations_bits("c3", 1000))
+
+
+def test_weight_quant_bitexact(lib):
+    cfg = synth.get_config("c1")
+    w = torch.stack([synth.make_expert_weights(cfg, "w13", e, device="cuda") for e in range(cfg.E)])
+    q = torch.empty(w.shape, dtype=torch.uint8, device="cuda")
+    s = torch.empty((cfg.E, w.shape[1] // 128, w.shape[2] // 128), dtype=torch.float32, device="cuda")
+    lib.moe_quant_weight_fp8(w, q, s)
+    rq, rs = oracle_weights("c1", "w13", tuple(range(cfg.E)))
+    assert np.array_equal(s.cpu().numpy(), rs)
+    assert np.array_equal(u8(q), rq)
+
+
+def test_weight_quant_full_size_expert(lib):
+    cfg = synth.get_config("c2")
+    w = synth.make_expert_weights(cfg, "w2", 1, device="cuda")[None]
+    q = torch.empty(w.shape, dtype=torch.uint8, device="cuda")
+    s = torch.empty((1, cfg.H // 128, cfg.I // 128), dtype=torch.float32, device="cuda")
+    lib.moe_quant_weight_fp8(w, q, s)
+    rq, rs = oracle_weights("c2", "w2", (1,))
+    assert np.array_equal(s.cpu().numpy(), rs)
+    assert np.array_equal(u8(q), rq)

@@ -1,0 +1,128 @@
+"""Parity of moe_swiglu_quant and moe_combine with the oracle.
+
+SwiGLU: the GPU's expf is not correctly rounded, so h may differ from the
+oracle's float64-then-float32 value by a few float32 ulps.  Acceptance: scales
+within 4 ulp; an FP8 code may differ only by one step, only where the oracle's
+value of h/s lies within 2^-19 (relative) of the rounding midpoint between
+the two codes (or the scale moved), and on fewer than 1e-4 of the codes.
+Combine: the acceptance bound; k=1 at weight 1 is a pure gather (bit-exact);
+constant expert rows come back unchanged; dropped entries are skipped."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.gpu_common import (SENTINEL_BF16, SENTINEL_F32, SENTINEL_U8, bits, check_tol,
+                              from_bits, to_dev, u8)
+
+pytestmark = pytest.mark.gpu
+
+
+def _y1(rows, I, seed, scale=2.0):
+    z = synth.counter_normal(rows * 2 * I, seed, 77, device="cuda") * scale
+    return bits(z.to(torch.bfloat16).reshape(rows, 2 * I))
+
+
+def _check_swiglu(q, s, y1_bits, valid_rows):
+    rq, rs = oracle.swiglu_quant(y1_bits[valid_rows])
+    gq, gs = q[valid_rows], s
+    # scales within 4 float32 ulp
+    ulp = np.spacing(rs.astype(np.float32))
+    assert (np.abs(gs.astype(np.float64) - rs) <= 4 * ulp).all(), "scales beyond 4 ulp"
+    mism = np.nonzero(gq != rq)
+    frac = mism[0].size / max(rq.size, 1)
+    assert frac < 1e-4, f"code mismatch fraction {frac}"
+    if mism[0].size:
+        h = oracle.swiglu(y1_bits[valid_rows])
+        for r, c in zip(*mism):
+            a, b = int(gq[r, c]), int(rq[r, c])
+            assert (a & 0x80) == (b & 0x80) and abs((a & 0x7F) - (b & 0x7F)) == 1, (r, c, a, b)
+            v = float(h[r, c]) / float(rs[c // 128, r])
+            mid = (abs(oracle.e4m3_decode(np.uint8(a))) + abs(oracle.e4m3_decode(np.uint8(b)))) / 2
+            near = abs(abs(v) - mid) <= 2.0 ** -19 * mid
+            scale_moved = gs[c // 128, r] != rs[c // 128, r]
+            assert near or scale_moved, (r, c, a, b, v, mid)
+
+
+def test_swiglu_quant_masked_rows(lib):
+    E, max_m, I = 3, 64, 256
+    counts = np.array([64, 0, 17], np.int32)
+    y1 = _y1(E * max_m, I, 1)
+    q = torch.full((E * max_m, I), SENTINEL_U8, dtype=torch.uint8, device="cuda")
+    s = torch.full((E, I // 128, max_m), SENTINEL_F32, device="cuda")
+    lib.moe_swiglu_quant(from_bits(y1), q, s, counts=to_dev(counts), max_m=max_m)
+    torch.cuda.synchronize()
+    qh, sh = u8(q), s.cpu().numpy()
+    valid = np.concatenate([np.arange(max_m) < c for c in counts])
+    sflat = sh.transpose(1, 0, 2).reshape(I // 128, -1)
+    _check_swiglu(qh, sflat[:, valid], y1, valid)
+    assert (qh[~valid] == SENTINEL_U8).all() and (sflat[:, ~valid] == SENTINEL_F32).all()
+
+
+def test_swiglu_quant_contig_selection_and_full_width(lib):
+    rows, I = 512, 2048
+    mi = np.full(rows, -1, np.int32)
+    mi[:200] = 0
+    mi[256:300] = 1
+    y1 = _y1(rows, I, 2, scale=3.0)
+    q = torch.full((rows, I), SENTINEL_U8, dtype=torch.uint8, device="cuda")
+    s = torch.full((I // 128, rows), SENTINEL_F32, device="cuda")
+    lib.moe_swiglu_quant(from_bits(y1), q, s, m_indices=to_dev(mi), s_ld=rows)
+    torch.cuda.synchronize()
+    qh, sh = u8(q), s.cpu().numpy()
+    valid = mi >= 0
+    _check_swiglu(qh, sh[:, valid], y1, valid)
+    assert (qh[~valid] == SENTINEL_U8).all() and (sh[:, ~valid] == SENTINEL_F32).all()
+
+
+def _combine(lib, y2_bits, dst, w):
+    T, k = w.shape
+    out = torch.full((T, y2_bits.shape[1]), SENTINEL_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    err = lib.new_error_word()
+    lib.moe_combine(from_bits(y2_bits), to_dev(dst.astype(np.int32)), to_dev(w.astype(np.float32)), out, err=err)
+    st, _ = lib.moe_read_device_status(err)
+    return bits(out), st
+
+
+def test_combine_matches_oracle_decode_routing(lib):
+    cfg = synth.get_config("c4")
+    r = synth.make_routing(cfg)
+    p = oracle.permute(r["topk_ids"], r["expert_begin"], cfg.E, "masked", cfg.max_m)
+    H = 1024
+    y2 = _y1(cfg.E * cfg.max_m, H // 2, 3)
+    got, st = _combine(lib, y2, p["dst_row"], r["topk_w"])
+    assert st == 0
+    check_tol(got, oracle.combine(y2, p["dst_row"], r["topk_w"]), "combine c4 routing")
+
+
+def test_combine_gather_and_constant_rows_and_dropped(lib):
+    rng = np.random.default_rng(4)
+    H = 7168
+    y2 = _y1(40, H // 2, 4)
+    dst = rng.permutation(40)[:25]
+    got, st = _combine(lib, y2, dst, np.ones((25, 1), np.float32))
+    assert st == 0 and np.array_equal(got, y2[dst])
+    # constant rows, weights summing to one
+    c = oracle.bf16_encode(rng.standard_normal(H))
+    yc = np.tile(c, (32, 1))
+    w = rng.random((8, 4)).astype(np.float32)
+    w /= w.sum(1, keepdims=True)
+    got, st = _combine(lib, yc, rng.permutation(32), w)
+    assert np.array_equal(got, np.tile(c, (8, 1)))
+    # dropped entries; a token with none gets zeros
+    dst2 = np.array([0, -1, -1, -1, 5, 6], np.int64)
+    w2 = np.full((3, 2), 0.5, np.float32)
+    got, st = _combine(lib, y2, dst2, w2)
+    assert np.array_equal(got, oracle.combine(y2, dst2, w2))
+    assert (oracle.bf16_decode(got[1]) == 0).all()
+
+
+def test_combine_bad_row_index_is_reported(lib):
+    y2 = _y1(8, 64, 5)
+    dst = np.array([0, 9, 3, 2], np.int64)             # 9 >= 8 rows
+    got, st = _combine(lib, y2, dst, np.full((2, 2), 0.5, np.float32))
+    assert st == lib.MOE_ERR_BAD_INDEX
+    ok = dst.copy()
+    ok[1] = -1
+    assert np.array_equal(got, oracle.combine(y2, ok, np.full((2, 2), 0.5, np.float32)))
