@@ -335,6 +335,299 @@ int launch_tokens_m(const uint8_t* A, int64_t a_rows, int64_t lda, const uint8_t
   return launch_status();
 }
 
+// =============================================================================
+// Weights-as-M variant for the masked (decode) layout.
+//
+// Decode sends few tokens to each expert, so a 128-row token tile would be
+// mostly empty while the expert's weights stream from HBM.  Here the roles
+// swap: 128 weight rows (one 128x128 scale block row) are the UMMA M side and
+// the expert's tokens are the N side, sized per tile at run time in steps of
+// 16 (UMMA N from 16 to BNT).  D^T sits in TMEM as [weight row (lane), token
+// (column)]; the epilogue scales column c by sB[nb, kb] * sA[token c, kb].
+// Stages are small (16 KB of weights + the token rows), so the ring is deep
+// (4..8 stages) to keep enough bytes in flight per SM, and TMEM holds 2..8
+// accumulation buffers.
+// =============================================================================
+template <int BNT>
+struct WeightsM {
+  static constexpr uint32_t kWBytes = 128 * BK;                // weight tile
+  static constexpr uint32_t kTBytes = BNT * BK;                // token tile (max)
+  static constexpr uint32_t kStage = kWBytes + kTBytes;
+  static constexpr int kStages = (196608 / kStage) > 8 ? 8 : (196608 / kStage);
+  static constexpr int kBufs = (512 / BNT) > 8 ? 8 : (512 / BNT);
+  static constexpr int kHalf = BNT / 2;                        // columns per epilogue warpgroup
+  static constexpr size_t smem_bytes(int E) {
+    return 1024 + static_cast<size_t>(kStages) * kStage + (2 * kStages + 2 * kBufs) * 8 + 16 +
+           sizeof(int32_t) * (3 * E + 1);
+  }
+};
+
+// Warp 0: per expert kept rows, token tiles of BNT, tiles = token tiles x N/128.
+template <int BNT>
+__device__ void build_schedule_wm(const GemmArgs& p, const Sched& s, int nblk) {
+  const int lane = threadIdx.x & 31;
+  const int per = (p.E + 31) / 32;
+  const int e0 = min(lane * per, p.E), e1 = min(e0 + per, p.E);
+  int local = 0;
+  bool overflow = false, bad = false;
+  for (int e = e0; e < e1; ++e) {
+    int c = p.counts[e];
+    if (c > p.max_m) { overflow = true; c = p.max_m; }
+    if (c < 0) { bad = true; c = 0; }
+    s.rbase[e] = e * p.max_m;
+    s.rext[e] = c;
+    local += (c + BNT - 1) / BNT * nblk;
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int run = incl - local;
+  for (int e = e0; e < e1; ++e) {
+    s.tile0[e] = run;
+    run += (s.rext[e] + BNT - 1) / BNT * nblk;
+  }
+  if (lane == 31) s.tile0[p.E] = incl;
+  if (blockIdx.x == 0) {
+    if (overflow) set_err(p.err, MOE_DEV_OVERFLOW);
+    if (bad) set_err(p.err, MOE_DEV_BAD_INDEX);
+  }
+}
+
+template <int BNT>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_fp8_weights_m_kernel(const __grid_constant__ CUtensorMap tmT,   // tokens  [E*max_m, K]
+                              const __grid_constant__ CUtensorMap tmW,   // weights [E*N, K]
+                              const GemmArgs p) {
+  using C = WeightsM<BNT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 2 * C::kBufs);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int32_t* sched_mem = reinterpret_cast<int32_t*>(tmem_slot + 4);
+  const Sched sched{sched_mem, sched_mem + p.E + 1, sched_mem + 2 * p.E + 1};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * C::kStages;
+  const uint32_t tfull0 = empty0 + 8 * C::kStages;
+  const uint32_t tempty0 = tfull0 + 8 * C::kBufs;
+  const int nblk = p.N / 128;
+  const int KB = p.K / BK;
+  volatile int* abort = abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < C::kBufs; ++b) {
+      mbar_init(tfull0 + 8 * b, 1);
+      mbar_init(tempty0 + 8 * b, kEpiWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    build_schedule_wm<BNT>(p, sched, nblk);
+    if (lane == 0) {
+      tma_prefetch_desc(&tmT);
+      tma_prefetch_desc(&tmW);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = sched.tile0[p.E];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && !(p.flags & MOE_GEMM_DEBUG_STALL)) {
+      const uint64_t pol_w = l2_policy_evict_first();   // weights stream through once
+      uint32_t it = 0;
+      TileCursor cur;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        cur.seek(sched, t);
+        const int e = cur.e;
+        const int l = t - sched.tile0[e];
+        const int j = l / nblk, nb = l % nblk;
+        const int ntok = min(BNT, sched.rext[e] - j * BNT);
+        const int ncols = (ntok + 15) & ~15;
+        const int t_row = sched.rbase[e] + j * BNT;
+        const int w_row = e * p.N + nb * 128;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1;
+          if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, p.err, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st_base = smem_u32(smem + s * C::kStage);
+          mbar_arrive_expect_tx(full0 + 8 * s, C::kWBytes + ncols * BK);
+          tma_load_2d_hint(st_base, &tmW, full0 + 8 * s, kb * BK, w_row, pol_w);
+          for (int r = 0; r < ncols; r += 16)
+            tma_load_2d(st_base + C::kWBytes + r * BK, &tmT, full0 + 8 * s, kb * BK, t_row + r);
+        }
+      }
+      if (!ok) {
+        const uint32_t first = it > static_cast<uint32_t>(C::kStages) ? it - C::kStages : 0;
+        for (uint32_t jj = first; jj < it; ++jj) {
+          int dummy = 0;
+          mbar_wait_bounded(full0 + 8 * (jj % C::kStages), (jj / C::kStages) & 1, &dummy, nullptr,
+                            p.wait_limit_ns / 10);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, acc = 0;
+      TileCursor cur;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        cur.seek(sched, t);
+        const int e = cur.e;
+        const int j = (t - sched.tile0[e]) / nblk;
+        const int ntok = min(BNT, sched.rext[e] - j * BNT);
+        const int ncols = (ntok + 15) & ~15;
+        const uint32_t idesc = idesc_e4m3_f32(128, ncols);
+        for (int kb = 0; kb < KB; ++kb, ++it, ++acc) {
+          const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1;
+          const uint32_t b = acc % C::kBufs, tph = (acc / C::kBufs) & 1;
+          if (!mbar_wait_bounded(tempty0 + 8 * b, tph ^ 1, abort, p.err, p.wait_limit_ns) ||
+              !mbar_wait_bounded(full0 + 8 * s, ph, abort, p.err, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st_base = smem_u32(smem + s * C::kStage);
+          const uint64_t wd = sdesc_kmajor_sw128(st_base);
+          const uint64_t td = sdesc_kmajor_sw128(st_base + C::kWBytes);
+          const uint32_t d_tmem = tmem_base + b * BNT;
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)
+            umma_e4m3(d_tmem, wd + 2 * k, td + 2 * k, idesc, k > 0 ? 1u : 0u);
+          umma_commit(empty0 + 8 * s);
+          umma_commit(tfull0 + 8 * b);
+        }
+      }
+      if (!ok && acc > 0) {
+        int dummy = 0;
+        const uint32_t last = acc - 1;
+        mbar_wait_bounded(tfull0 + 8 * (last % C::kBufs), (last / C::kBufs) & 1, &dummy, nullptr,
+                          p.wait_limit_ns / 10);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;             // TMEM lanes = weight rows q*32 .. q*32+31
+    const int g = (warp - 2) >> 2;      // token columns [g*kHalf, (g+1)*kHalf)
+    uint32_t acc_it = 0;
+    TileCursor cur;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+      cur.seek(sched, t);
+      const int e = cur.e;
+      const int l = t - sched.tile0[e];
+      const int j = l / nblk, nb = l % nblk;
+      const int ntok = min(BNT, sched.rext[e] - j * BNT);
+      const int ncols = (ntok + 15) & ~15;
+      const int col0 = g * C::kHalf;
+      const int my_cols = max(0, min(C::kHalf, ncols - col0));
+      const int nchunk = my_cols / 16;
+      const float* sa_base = p.sA + static_cast<int64_t>(e) * KB * p.max_m + j * BNT + col0;
+      const float* sb_ptr = p.sB + (static_cast<int64_t>(e) * nblk + nb) * KB;
+      float acc[C::kHalf];
+#pragma unroll
+      for (int i = 0; i < C::kHalf; ++i) acc[i] = 0.f;
+      for (int kb = 0; kb < KB; ++kb, ++acc_it) {
+        const uint32_t b = acc_it % C::kBufs, tph = (acc_it / C::kBufs) & 1;
+        const float sb = __ldg(sb_ptr + kb);
+        const float* sa_k = sa_base + static_cast<int64_t>(kb) * p.max_m;
+        int got = 1;
+        if (lane == 0) got = mbar_wait_bounded(tfull0 + 8 * b, tph, abort, p.err, p.wait_limit_ns);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BNT + col0;
+#pragma unroll
+        for (int ch = 0; ch < C::kHalf / 16; ++ch) {
+          if (ch < nchunk) {
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(tbase + ch * 16, r);
+            float4 sa4[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) sa4[v] = __ldg(reinterpret_cast<const float4*>(sa_k + ch * 16) + v);
+            tmem_ld_wait();
+            const float sa[16] = {sa4[0].x, sa4[0].y, sa4[0].z, sa4[0].w, sa4[1].x, sa4[1].y,
+                                  sa4[1].z, sa4[1].w, sa4[2].x, sa4[2].y, sa4[2].z, sa4[2].w,
+                                  sa4[3].x, sa4[3].y, sa4[3].z, sa4[3].w};
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              acc[ch * 16 + i] = fmaf(sb * sa[i], __uint_as_float(r[i]), acc[ch * 16 + i]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty0 + 8 * b);
+      }
+      if (!ok) break;
+      // D[e][token][n]: a warp writes 32 consecutive n of one token per store
+      const int64_t n = static_cast<int64_t>(nb) * 128 + q * 32 + lane;
+      uint16_t* dcol = p.D + (static_cast<int64_t>(e) * p.max_m + j * BNT + col0) * p.N + n;
+      const int valid = max(0, min(my_cols, ntok - col0));
+#pragma unroll
+      for (int c = 0; c < C::kHalf; ++c) {
+        if (c < valid) {
+          const __nv_bfloat16 v = __float2bfloat16_rn(acc[c]);
+          dcol[static_cast<int64_t>(c) * p.N] = *reinterpret_cast<const uint16_t*>(&v);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int BNT>
+int launch_weights_m(const uint8_t* A, const uint8_t* B, GemmArgs& args, cudaStream_t stream) {
+  using C = WeightsM<BNT>;
+  CUtensorMap tmT, tmW;
+  if (int st = make_tmap_u8_sw128(&tmT, A, static_cast<uint64_t>(args.E) * args.max_m, args.K,
+                                  args.K, 16))
+    return st;
+  if (int st = make_tmap_u8_sw128(&tmW, B, static_cast<uint64_t>(args.E) * args.N, args.K, args.K, 128))
+    return st;
+  const size_t smem = C::smem_bytes(args.E);
+  MOE_CUDA_TRY(cudaFuncSetAttribute(gemm_fp8_weights_m_kernel<BNT>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem)));
+  if (args.wait_limit_ns == 0) args.wait_limit_ns = kWaitLimitNs;
+  const int64_t tiles_upper = static_cast<int64_t>(args.E) * ((args.max_m + BNT - 1) / BNT) * (args.N / 128);
+  int64_t grid = num_sms();
+  if (tiles_upper < grid) grid = tiles_upper;
+  if (grid < 1) grid = 1;
+  gemm_fp8_weights_m_kernel<BNT><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmT, tmW, args);
+  return launch_status();
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -397,6 +690,23 @@ extern "C" int moe_gemm_fp8_masked(const uint8_t* A, const float* sA, const uint
   a.err = err;
   a.flags = flags;
   if (flags & MOE_GEMM_DEBUG_STALL) a.wait_limit_ns = 200ull * 1000ull * 1000ull;
+  // Kernel choice: weights-as-M streams each expert's weights once per up to 256
+  // tokens and sizes the token side to the count, so it serves decode counts;
+  // tokens-as-M is kept for large counts.  Host-side only: the counts stay on
+  // the device.
+  const int hint = expected_m > 0 ? expected_m : max_m;
+  bool weights_m = (max_m % 16 == 0) && hint <= 256;
+  if (flags & MOE_GEMM_FORCE_TOKENS_M) weights_m = false;
+  if (flags & MOE_GEMM_FORCE_WEIGHTS_M) {
+    if (max_m % 16 != 0) return MOE_ERR_UNSUPPORTED;
+    weights_m = true;
+  }
+  cudaStream_t st = as_stream(stream);
+  if (weights_m) {
+    if (hint <= 48) return launch_weights_m<64>(A, B, a, st);
+    if (hint <= 112) return launch_weights_m<128>(A, B, a, st);
+    return launch_weights_m<256>(A, B, a, st);
+  }
   const int64_t tiles = static_cast<int64_t>(E) * ((max_m + BM - 1) / BM) * ((N + BN - 1) / BN);
-  return launch_tokens_m(A, static_cast<int64_t>(E) * max_m, K, B, tiles, a, as_stream(stream));
+  return launch_tokens_m(A, static_cast<int64_t>(E) * max_m, K, B, tiles, a, st);
 }

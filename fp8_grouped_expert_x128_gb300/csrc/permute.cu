@@ -23,6 +23,7 @@ namespace {
 constexpr int kIdxThreads = 1024;
 constexpr int kIdxWarps = kIdxThreads / 32;
 constexpr int kMaxExperts = 1024;
+constexpr size_t kIdxSmemLimit = 200 * 1024;
 
 struct IndexParams {
   const int32_t* topk_ids;
@@ -37,21 +38,32 @@ struct IndexParams {
   int32_t* err;
 };
 
-// dynamic smem: cnt[E] | base[E] | wc[kIdxWarps][E]
-__global__ void __launch_bounds__(kIdxThreads) permute_index_kernel(IndexParams p) {
+// dynamic smem: cnt[E] | base[E] | wc[kIdxWarps][E] | ids[n_assign] (when they fit)
+// The routing ids are read from global memory once, into shared memory, so the
+// ordered rank pass below runs at shared-memory latency.
+__global__ void __launch_bounds__(kIdxThreads) permute_index_kernel(IndexParams p, int ids_in_smem) {
   extern __shared__ int32_t sm[];
   const int E = p.E;
   int32_t* cnt = sm;
   int32_t* base = sm + E;
   int32_t* wc = sm + 2 * E;
+  int32_t* ids = sm + 2 * E + kIdxWarps * E;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  auto local_expert = [&](int64_t i) -> int {
+    const int e = (ids_in_smem ? ids[i] : p.topk_ids[i]) - p.expert_begin;
+    return (e >= 0 && e < E) ? e : -1;
+  };
 
-  // 1. histogram (order-free)
+  // 1. stage ids, histogram (order-free; one atomic per distinct expert per warp)
   for (int e = tid; e < E; e += kIdxThreads) cnt[e] = 0;
+  if (ids_in_smem)
+    for (int64_t i = tid; i < p.n_assign; i += kIdxThreads) ids[i] = p.topk_ids[i];
   __syncthreads();
-  for (int64_t i = tid; i < p.n_assign; i += kIdxThreads) {
-    const int e = p.topk_ids[i] - p.expert_begin;
-    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+  for (int64_t c0 = 0; c0 < p.n_assign; c0 += kIdxThreads) {
+    const int64_t i = c0 + tid;
+    const int e = i < p.n_assign ? local_expert(i) : -1;
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && (same & ((1u << lane) - 1u)) == 0) atomicAdd(&cnt[e], __popc(same));
   }
   __syncthreads();
 
@@ -89,11 +101,7 @@ __global__ void __launch_bounds__(kIdxThreads) permute_index_kernel(IndexParams 
   // 3. ranks in ascending assignment order, chunk by chunk
   for (int64_t c0 = 0; c0 < p.n_assign; c0 += kIdxThreads) {
     const int64_t i = c0 + tid;
-    int e = -1;
-    if (i < p.n_assign) {
-      e = p.topk_ids[i] - p.expert_begin;
-      if (e < 0 || e >= E) e = -1;
-    }
+    const int e = i < p.n_assign ? local_expert(i) : -1;
     for (int x = tid; x < kIdxWarps * E; x += kIdxThreads) wc[x] = 0;
     __syncthreads();
     const uint32_t same = __match_any_sync(0xffffffffu, e);
@@ -232,13 +240,16 @@ extern "C" int moe_permute(const uint8_t* q, const float* s, int64_t s_ld, const
   cudaStream_t st = as_stream(stream);
   IndexParams p{topk_ids, T * k, expert_begin, E, layout, max_m, rows_capacity,
                 counts, offsets, m_indices, row_src, dst_row, err};
-  const size_t smem = sizeof(int32_t) * (2 * E + kIdxWarps * E);
+  size_t smem = sizeof(int32_t) * (2 * E + kIdxWarps * E);
+  const size_t ids_bytes = sizeof(int32_t) * static_cast<size_t>(T * k);
+  const int ids_in_smem = smem + ids_bytes <= kIdxSmemLimit ? 1 : 0;
+  if (ids_in_smem) smem += ids_bytes;
   if (smem > 48 * 1024) {
     MOE_CUDA_TRY(cudaFuncSetAttribute(permute_index_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(smem)));
   }
-  permute_index_kernel<<<1, kIdxThreads, smem, st>>>(p);
+  permute_index_kernel<<<1, kIdxThreads, smem, st>>>(p, ids_in_smem);
   if (int rc = launch_status()) return rc;
   if (T == 0) return MOE_OK;
   const int64_t n = T * k;

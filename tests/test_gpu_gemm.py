@@ -50,7 +50,14 @@ def _check_masked(got, ref, valid, what):
     assert (got[~valid] == SENTINEL_BF16).all(), f"{what}: rows past the count were written"
 
 
-def test_gemm_integer_exact_masked(lib):
+# (flags, expected_m): the tokens-as-M kernel, and the weights-as-M kernel with
+# each token-tile width (64 / 128 / 256 columns)
+MASKED_KERNELS = [(0x1, 0), (0x2, 16), (0x2, 100), (0x2, 200)]
+MASKED_IDS = ["tokens_m", "weights_m64", "weights_m128", "weights_m256"]
+
+
+@pytest.mark.parametrize("flags,hint", MASKED_KERNELS, ids=MASKED_IDS)
+def test_gemm_integer_exact_masked(lib, flags, hint):
     rng = np.random.default_rng(11)
     E, max_m, N, K = 3, 256, 384, 512                 # N = 1.5 tiles of 256: half last tile
     counts = [256, 0, 77]
@@ -59,7 +66,7 @@ def test_gemm_integer_exact_masked(lib):
     A, B = oracle.e4m3_encode(a.astype(np.float64)), oracle.e4m3_encode(b.astype(np.float64))
     sA = np.ones((E, K // 128, max_m), np.float32)
     sB = np.ones((E, N // 128, K // 128), np.float32)
-    got, st = _masked(lib, A, sA, B, sB, counts)
+    got, st = _masked(lib, A, sA, B, sB, counts, flags=flags, expected_m=hint)
     assert st == 0
     for e in range(E):
         c = counts[e]
@@ -91,14 +98,15 @@ def test_gemm_integer_exact_contig(lib):
     assert (got[mi < 0] == SENTINEL_BF16).all()
 
 
-def test_gemm_masked_random_scales(lib):
+@pytest.mark.parametrize("flags,hint", MASKED_KERNELS, ids=MASKED_IDS)
+def test_gemm_masked_random_scales(lib, flags, hint):
     rng = np.random.default_rng(13)
     E, max_m, N, K = 4, 384, 640, 1024
     counts = [1, 383, 0, 129]
     A, B = rand_codes(rng, (E, max_m, K)), rand_codes(rng, (E, N, K))
     sA = np.exp(rng.uniform(-8, 2, (E, K // 128, max_m))).astype(np.float32)
     sB = np.exp(rng.uniform(-8, 2, (E, N // 128, K // 128))).astype(np.float32)
-    got, st = _masked(lib, A, sA, B, sB, counts)
+    got, st = _masked(lib, A, sA, B, sB, counts, flags=flags, expected_m=hint)
     assert st == 0
     ref, valid = oracle.gemm_masked(A, sA, B, sB, counts)
     _check_masked(got, ref, valid, "masked random")
@@ -125,13 +133,14 @@ def test_gemm_contig_random_scales(lib):
     assert (got[~valid] == SENTINEL_BF16).all()
 
 
-def test_gemm_masked_count_above_max_m_is_clamped(lib):
+@pytest.mark.parametrize("flags,hint", MASKED_KERNELS[:2], ids=MASKED_IDS[:2])
+def test_gemm_masked_count_above_max_m_is_clamped(lib, flags, hint):
     rng = np.random.default_rng(15)
     E, max_m, N, K = 2, 128, 256, 256
     A, B = rand_codes(rng, (E, max_m, K)), rand_codes(rng, (E, N, K))
     sA = np.ones((E, K // 128, max_m), np.float32)
     sB = np.ones((E, N // 128, K // 128), np.float32)
-    got, st = _masked(lib, A, sA, B, sB, [500, 3])
+    got, st = _masked(lib, A, sA, B, sB, [500, 3], flags=flags, expected_m=hint)
     assert st == lib.MOE_ERR_OVERFLOW
     ref, valid = oracle.gemm_masked(A, sA, B, sB, [128, 3])
     _check_masked(got, ref, valid, "clamped")
@@ -152,11 +161,13 @@ def _decode_gemm_inputs(cfg_name, which):
     return cfg, p["q"].reshape(cfg.E, cfg.max_m, K), p["s"], p["counts"]
 
 
+@pytest.mark.parametrize("flags", [0, 0x1], ids=["default", "tokens_m"])
 @pytest.mark.parametrize("which", ["w13", "w2"])
-def test_gemm_masked_decode_full_size(lib, which):
+def test_gemm_masked_decode_full_size(lib, which, flags):
     cfg, A, sA, counts = _decode_gemm_inputs("c2", which)
     Bq, Bs = oracle_weights("c2", which, tuple(range(cfg.E)))
-    got, st = _masked(lib, A, sA, Bq, Bs, counts)
+    got, st = _masked(lib, A, sA, Bq, Bs, counts, flags=flags,
+                      expected_m=int(np.ceil(counts.sum() / (counts > 0).sum())))
     assert st == 0
     ref, valid = oracle.gemm_masked(A, sA, Bq, Bs, counts)
     _check_masked(got, ref, valid, f"c2 {which}")
@@ -218,8 +229,10 @@ def test_gemm_stall_reports_timeout_and_recovers(lib):
     A, B = rand_codes(rng, (E, max_m, K)), rand_codes(rng, (E, N, K))
     sA = np.ones((E, K // 128, max_m), np.float32)
     sB = np.ones((E, N // 128, K // 128), np.float32)
-    got, st = _masked(lib, A, sA, B, sB, [5], flags=lib.MOE_GEMM_DEBUG_STALL)
-    assert st == lib.MOE_ERR_TIMEOUT
+    for kernel in (lib.MOE_GEMM_FORCE_TOKENS_M, lib.MOE_GEMM_FORCE_WEIGHTS_M):
+        got, st = _masked(lib, A, sA, B, sB, [5], flags=lib.MOE_GEMM_DEBUG_STALL | kernel)
+        assert st == lib.MOE_ERR_TIMEOUT
+        assert (got == SENTINEL_BF16).all()
     got, st = _masked(lib, A, sA, B, sB, [5])
     assert st == 0
     ref, valid = oracle.gemm_masked(A, sA, B, sB, [5])
