@@ -5,7 +5,7 @@ PyTorch supplies device memory and the current stream.  Each function has the
 name of the C entry point it calls (see include/moe_fp8.h for the definitions,
 layouts and error rules).  A non-zero status raises ``MoeError``.
 
-The library is built in-tree by ``fp8_grouped_expert_x128_gb300._build``
+The library is built in-tree by ``fp8_grouped_expert_x128_gb300/_build.py``
 (``__graft_entry__.build()`` does it).  Importing this package without the
 built library raises ImportError: there is no fallback path.
 """
@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe_fp8.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing: build it with `python -m fp8_grouped_expert_x128_gb300._build` "
+        f"{LIB_PATH} is missing: build it with `python fp8_grouped_expert_x128_gb300/_build.py` "
         "(the CUDA library is the only implementation; there is no CPU fallback)")
 
 _lib = ctypes.CDLL(LIB_PATH)

@@ -2,7 +2,7 @@
 extension machinery): every .cu under csrc/ is compiled in parallel, then
 linked into one shared library next to this file.
 
-    python -m fp8_grouped_expert_x128_gb300._build [--force] [--verbose]
+    python fp8_grouped_expert_x128_gb300/_build.py [--force] [--verbose] [--ptxas-info]
 """
 from __future__ import annotations
 

@@ -12,8 +12,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def so():
-    from fp8_grouped_expert_x128_gb300 import _build
-    path = _build.build()
+    import __graft_entry__
+    path = __graft_entry__._builder().build()
     return ctypes.CDLL(path), path
 
 
