@@ -190,7 +190,8 @@ extern "C" int moe_quant_weight_fp8(const uint16_t* w, int64_t E, int64_t N, int
                                     float* s, void* stream) {
   MOE_CHECK_ARG(E >= 0 && N > 0 && K > 0 && N % 128 == 0 && K % 128 == 0);
   if (E == 0) return MOE_OK;
-  MOE_CHECK_ARG(w && q && s && aligned16(w) && aligned16(q) && aligned16(s));
+  MOE_CHECK_ARG(w && q && s && aligned16(w) && aligned16(q));
+  MOE_CHECK_ARG((reinterpret_cast<uintptr_t>(s) & 3u) == 0);  // scalar scale stores
   if (int st = check_device()) return st;
   const int64_t tiles = E * (N / 128) * (K / 128);
   MOE_CHECK_ARG(tiles < (1ll << 31));

@@ -106,7 +106,8 @@ int moe_quant_fp8(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
  * a3 -- 128x128 block weight quantisation (set-up, not on the timed path).
  * The a1 rule with amax taken over each 128x128 tile.
  * w : device bf16 [E, N, K] (K-major: the GEMM's B operand, out x in).
- * q : device uint8 [E, N, K];  s : device fp32 [E, N/128, K/128].
+ * q : device uint8 [E, N, K];  s : device fp32 [E, N/128, K/128] (4-byte
+ * alignment suffices for s, so per-expert slices may be quantised one by one).
  */
 int moe_quant_weight_fp8(const uint16_t *w, int64_t E, int64_t N, int64_t K,
                          uint8_t *q, float *s, void *stream);
