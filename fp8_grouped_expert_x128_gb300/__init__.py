@@ -240,6 +240,11 @@ def make_ffn_desc(x, topk_ids, topk_w, w13, w13_s, w2, w2_s, out, expert_begin, 
                      w2_s=w2_s.data_ptr(), out=out.data_ptr(),
                      err=err.data_ptr() if err is not None else None, stage_events=None)
     if stage_events is not None:
+        if len(stage_events) != 7:
+            raise ValueError("stage_events needs 7 events")
+        for ev in stage_events:
+            if not ev.cuda_event:          # torch creates the CUDA event on first record
+                ev.record()
         arr = (ctypes.c_void_p * len(stage_events))(*[ev.cuda_event for ev in stage_events])
         d._events_keepalive = arr
         d.stage_events = ctypes.cast(arr, ctypes.c_void_p)

@@ -60,24 +60,63 @@ def check_tol(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = ""):
 
 # End to end, an FP8 requantisation sits between the two GEMMs: a one-ulp bf16
 # difference in Y1 (fp32 vs float64 accumulation) or a few-ulp float32
-# difference in h (expf) can flip one E4M3 code of h, which moves that output
-# row by up to one E4M3 step of one term.  Stage-fed checks hold every stage to
-# the strict bound; end to end, at most CHAIN_FRAC of the outputs may leave the
-# strict bound, and those must stay inside the one-step bound below.
+# difference in h (expf) can flip one E4M3 code of h, which moves that routed
+# row's output by one E4M3 step of one term.  Stage-fed checks hold every stage
+# to the strict bound.  End to end, at most CHAIN_FRAC of the outputs may leave
+# the strict bound, and every output must stay within the strict bound plus
+# the largest effect one such flip per routed row can have (computed by the
+# oracle alone, see flip_bound).
 CHAIN_FRAC = 1e-3
-CHAIN_REL, CHAIN_RMS = 2.0 ** -4, 1e-2
 
 
-def check_tol_chain(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = ""):
+def flip_bound(ref: dict, topk_w: np.ndarray, w2q: np.ndarray, w2s: np.ndarray) -> np.ndarray:
+    """Oracle-side bound [T, H] on how far one E4M3 flip of h per routed row can
+    move each output: sum_j w_j * max_i(step(q2[r_j, i]) * s2[r_j, i]) * max_i |W2[e_j][n, i]|,
+    with step the larger gap to a neighbouring code and W2 dequantised."""
+    rows_valid = ref["valid"]
+    q2 = ref["q2"]
+    I = q2.shape[1]
+    KB2 = I // 128
+    s2 = ref["s2"]
+    if s2.ndim == 3:                                     # masked [E, KB, max_m] -> [KB, rows]
+        s2 = s2.transpose(1, 0, 2).reshape(KB2, -1)
+    mag = (q2 & 0x7F).astype(np.int64)
+    up = np.abs(oracle.e4m3_decode(np.minimum(mag + 1, 0x7E).astype(np.uint8)) - oracle.e4m3_decode(mag.astype(np.uint8)))
+    dn = np.abs(oracle.e4m3_decode(mag.astype(np.uint8)) - oracle.e4m3_decode(np.maximum(mag - 1, 0).astype(np.uint8)))
+    step = np.maximum(up, dn) * np.repeat(s2.T, 128, axis=1)          # [rows, I]
+    rowflip = np.where(rows_valid, step.max(axis=1), 0.0)             # [rows]
+    E = w2q.shape[0]
+    colmax = np.stack([np.abs(oracle.e4m3_decode(w2q[e]) * np.repeat(np.repeat(w2s[e], 128, 0), 128, 1)).max(axis=1)
+                       for e in range(E)])                            # [E, H]
+    dst = ref["perm"]["dst_row"].reshape(topk_w.shape)
+    T, k = topk_w.shape
+    rows_per_e = rows_valid.size // E if ref["perm"].get("offsets") is None else None
+    out = np.zeros((T, colmax.shape[1]))
+    for j in range(k):
+        d = dst[:, j]
+        ok = d >= 0
+        if rows_per_e is not None:
+            e_of = d // rows_per_e
+        else:
+            e_of = ref["perm"]["m_indices"][np.maximum(d, 0)]
+        out[ok] += (topk_w[ok, j] * rowflip[d[ok]])[:, None] * colmax[e_of[ok]]
+    return out
+
+
+def check_tol_chain(got_bits: np.ndarray, ref_bits: np.ndarray, extra: np.ndarray, what: str = ""):
     got = oracle.bf16_decode(got_bits)
     ref = oracle.bf16_decode(ref_bits)
     assert np.isfinite(got).all(), f"{what}: non-finite GPU output"
     rms = np.sqrt(np.mean(ref ** 2))
     err = np.abs(got - ref)
-    strict = err > REL_TOL * np.abs(ref) + RMS_TOL * rms
-    loose = err > CHAIN_REL * np.abs(ref) + CHAIN_RMS * rms
+    strict_b = REL_TOL * np.abs(ref) + RMS_TOL * rms
+    strict = err > strict_b
+    beyond = err > strict_b + extra
     frac = strict.mean()
-    assert not loose.any(), f"{what}: {loose.sum()} outputs beyond one FP8 step"
+    if beyond.any():
+        i = np.unravel_index(np.argmax(err - strict_b - extra), err.shape)
+        raise AssertionError(f"{what}: {beyond.sum()} outputs beyond the one-flip bound; worst at {i}: "
+                             f"gpu {got[i]!r} ref {ref[i]!r} strict {strict_b[i]!r} flip {extra[i]!r}")
     assert frac <= CHAIN_FRAC, f"{what}: {frac:.2e} of outputs outside the strict bound"
     return frac
 

@@ -13,8 +13,8 @@ import torch
 import oracle
 import synth
 from bench import build_workload, make_desc
-from tests.gpu_common import (bits, check_swiglu, check_tol, check_tol_chain, from_bits,
-                              oracle_weights, to_dev, u8)
+from tests.gpu_common import (bits, check_swiglu, check_tol, check_tol_chain, flip_bound,
+                              from_bits, oracle_weights, to_dev, u8)
 
 pytestmark = pytest.mark.gpu
 
@@ -120,9 +120,9 @@ def test_ffn_decode_configs_end_to_end(lib, name):
     wl = build_workload(name)
     got, st = _gpu_ffn(lib, wl)
     assert st in (0, lib.MOE_ERR_OVERFLOW)
-    ref, _ = _oracle_full(name, wl)
+    ref, (_, _, w2q, w2s) = _oracle_full(name, wl)
     assert (st == lib.MOE_ERR_OVERFLOW) == bool(ref["perm"]["overflow"])
-    check_tol_chain(got, ref["out"], f"{name} ffn")
+    check_tol_chain(got, ref["out"], flip_bound(ref, wl["routing"]["topk_w"], w2q, w2s), f"{name} ffn")
 
 
 def test_ffn_all_experts_layer_sampled_tokens(lib):
