@@ -462,7 +462,12 @@ def main():
         achieved = alg["flops_g1"] / g1_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": achieved / fp8_peak}
-    roof.update({"traffic": None, "kernel": "gemm_fp8_tokens_m_kernel (GEMM1, W13)",
+    if wl["layout"] == moe.MOE_LAYOUT_MASKED:
+        v = moe.moe_gemm_fp8_masked_variant(cfg.max_m, wl["expected_m"], 0)
+        kname = "gemm_fp8_tokens_m_kernel" if v == 0 else f"gemm_fp8_weights_m_kernel<{v}>"
+    else:
+        kname = "gemm_fp8_tokens_m_kernel"
+    roof.update({"traffic": None, "kernel": f"{kname} (GEMM1, W13)",
                  "launch_ms": 1e3 * g1_s, "peak_source": f"{peak_src}" +
                  ("" if roof["bound"] == "hbm" else " bf16 burst x2 (nominal FP8:BF16)"),
                  "algorithmic": {"bytes": alg["g1_bytes"], "flops": alg["flops_g1"]}})

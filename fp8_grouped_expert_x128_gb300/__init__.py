@@ -44,7 +44,7 @@ MOE_GEMM_DEBUG_STALL = 0x100
 EXPORTED = [
     "moe_status_string", "moe_version", "moe_read_device_status", "moe_quant_fp8",
     "moe_quant_weight_fp8", "moe_contig_rows_bound", "moe_permute", "moe_gemm_fp8_contig",
-    "moe_gemm_fp8_masked", "moe_swiglu_quant", "moe_combine", "moe_ffn_workspace_size", "moe_ffn",
+    "moe_gemm_fp8_masked", "moe_gemm_fp8_masked_variant", "moe_swiglu_quant", "moe_combine", "moe_ffn_workspace_size", "moe_ffn",
 ]
 
 _P = ctypes.c_void_p
@@ -82,6 +82,7 @@ _sig("moe_gemm_fp8_contig", ctypes.c_int,
      [_P, _I64, _P, _I64, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _P, _I64, _I32, _P, _P])
 _sig("moe_gemm_fp8_masked", ctypes.c_int,
      [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I32, _P, _P])
+_sig("moe_gemm_fp8_masked_variant", ctypes.c_int, [_I32, _I32, _I32])
 _sig("moe_swiglu_quant", ctypes.c_int, [_P, _I64, _I32, _P, _I32, _P, _P, _P, _I64, _P, _P])
 _sig("moe_combine", ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I32, _I32, _P, _I64, _P, _P])
 _sig("moe_ffn_workspace_size", ctypes.c_size_t, [ctypes.POINTER(moe_ffn_desc)])
@@ -206,6 +207,11 @@ def moe_gemm_fp8_masked(A, sA, B, sB, counts, D, expected_m=0, flags=0, err=None
                                     E, max_m, N, K, expected_m, _ptr(D), flags, _ptr(err),
                                     _stream(stream)), "moe_gemm_fp8_masked")
     return D
+
+
+def moe_gemm_fp8_masked_variant(max_m: int, expected_m: int = 0, flags: int = 0) -> int:
+    """0 = tokens-as-M kernel; 64/128/256 = weights-as-M token-tile width."""
+    return int(_lib.moe_gemm_fp8_masked_variant(max_m, expected_m, flags))
 
 
 def moe_swiglu_quant(Y1, q, s, counts=None, max_m=0, m_indices=None, s_ld=0, err=None,

@@ -258,11 +258,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       float acc[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) acc[i] = 0.f;
+      // scales of k-block kb+1 are loaded while kb is waited for and processed
+      float sa_next = row_ok ? __ldg(sa_ptr) : 0.f;
+      float sb_next = __ldg(sb_ptr);
       for (int kb = 0; kb < KB; ++kb, ++acc_it) {
         const uint32_t b = acc_it & 1, tph = (acc_it >> 1) & 1;
-        const float sa = row_ok ? __ldg(sa_ptr + static_cast<int64_t>(kb) * p.sA_G) : 0.f;
-        const float sb = __ldg(sb_ptr + kb);
-        const float sc = sa * sb;
+        const float sc = sa_next * sb_next;
+        if (kb + 1 < KB) {
+          sa_next = row_ok ? __ldg(sa_ptr + static_cast<int64_t>(kb + 1) * p.sA_G) : 0.f;
+          sb_next = __ldg(sb_ptr + kb + 1);
+        }
         // one lane waits, the warp follows it: tcgen05.ld is warp-collective
         int got = 1;
         if (lane == 0) got = mbar_wait_bounded(tfull0 + 8 * b, tph, abort, p.err, p.wait_limit_ns);
@@ -356,9 +361,11 @@ struct WeightsM {
   static constexpr int kStages = (196608 / kStage) > 8 ? 8 : (196608 / kStage);
   static constexpr int kBufs = (512 / BNT) > 8 ? 8 : (512 / BNT);
   static constexpr int kHalf = BNT / 2;                        // columns per epilogue warpgroup
+  static constexpr int kPair = BNT <= 128 ? 2 : 1;             // TMEM loads in flight (registers)
+  static constexpr size_t kScaleBufBytes = sizeof(float) * kEpiWarps * 2 * kHalf;
   static constexpr size_t smem_bytes(int E) {
     return 1024 + static_cast<size_t>(kStages) * kStage + (2 * kStages + 2 * kBufs) * 8 + 16 +
-           sizeof(int32_t) * (3 * E + 1);
+           sizeof(int32_t) * (3 * E + 1) + 16 + kScaleBufBytes;
   }
 };
 
@@ -410,6 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int32_t* sched_mem = reinterpret_cast<int32_t*>(tmem_slot + 4);
   const Sched sched{sched_mem, sched_mem + p.E + 1, sched_mem + 2 * p.E + 1};
+  float* sa_stage = reinterpret_cast<float*>(
+      (reinterpret_cast<uintptr_t>(sched_mem + 3 * p.E + 1) + 15) & ~static_cast<uintptr_t>(15));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars);
@@ -531,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;             // TMEM lanes = weight rows q*32 .. q*32+31
     const int g = (warp - 2) >> 2;      // token columns [g*kHalf, (g+1)*kHalf)
+    float* my_sa = sa_stage + (warp - 2) * 2 * C::kHalf;
     uint32_t acc_it = 0;
     TileCursor cur;
     bool ok = true;
@@ -546,13 +556,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nchunk = my_cols / 16;
       const float* sa_base = p.sA + static_cast<int64_t>(e) * KB * p.max_m + j * BNT + col0;
       const float* sb_ptr = p.sB + (static_cast<int64_t>(e) * nblk + nb) * KB;
+      // The token scales of k-block kb+1 are fetched while kb is processed and
+      // parked in this warp's shared double buffer (one float4 per lane), so
+      // the epilogue never waits on a global load after its TMEM wait.
+      const bool ld_lane = lane * 4 < my_cols;
+      float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ld_lane) pre = __ldg(reinterpret_cast<const float4*>(sa_base) + lane);
+      float sb_next = __ldg(sb_ptr);
+      __syncwarp();
+      if (ld_lane) reinterpret_cast<float4*>(my_sa)[lane] = pre;
+      __syncwarp();
       float acc[C::kHalf];
 #pragma unroll
       for (int i = 0; i < C::kHalf; ++i) acc[i] = 0.f;
       for (int kb = 0; kb < KB; ++kb, ++acc_it) {
         const uint32_t b = acc_it % C::kBufs, tph = (acc_it / C::kBufs) & 1;
-        const float sb = __ldg(sb_ptr + kb);
-        const float* sa_k = sa_base + static_cast<int64_t>(kb) * p.max_m;
+        const float sb = sb_next;
+        if (kb + 1 < KB) {
+          if (ld_lane)
+            pre = __ldg(reinterpret_cast<const float4*>(sa_base + static_cast<int64_t>(kb + 1) * p.max_m) + lane);
+          sb_next = __ldg(sb_ptr + kb + 1);
+        }
         int got = 1;
         if (lane == 0) got = mbar_wait_bounded(tfull0 + 8 * b, tph, abort, p.err, p.wait_limit_ns);
         got = __shfl_sync(0xffffffffu, got, 0);
@@ -562,26 +586,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BNT + col0;
+        const float* sa_cur = my_sa + (kb & 1) * C::kHalf;
 #pragma unroll
-        for (int ch = 0; ch < C::kHalf / 16; ++ch) {
+        for (int ch = 0; ch < C::kHalf / 16; ch += C::kPair) {
           if (ch < nchunk) {
-            uint32_t r[16];
-            tmem_ld_32x32b_x16(tbase + ch * 16, r);
-            float4 sa4[4];
-#pragma unroll
-            for (int v = 0; v < 4; ++v) sa4[v] = __ldg(reinterpret_cast<const float4*>(sa_k + ch * 16) + v);
+            uint32_t r[C::kPair][16];
+            tmem_ld_32x32b_x16(tbase + ch * 16, r[0]);
+            if (C::kPair == 2 && ch + 1 < nchunk) tmem_ld_32x32b_x16(tbase + (ch + 1) * 16, r[C::kPair - 1]);
             tmem_ld_wait();
-            const float sa[16] = {sa4[0].x, sa4[0].y, sa4[0].z, sa4[0].w, sa4[1].x, sa4[1].y,
-                                  sa4[1].z, sa4[1].w, sa4[2].x, sa4[2].y, sa4[2].z, sa4[2].w,
-                                  sa4[3].x, sa4[3].y, sa4[3].z, sa4[3].w};
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              acc[ch * 16 + i] = fmaf(sb * sa[i], __uint_as_float(r[i]), acc[ch * 16 + i]);
+            for (int h = 0; h < C::kPair; ++h) {
+              if (ch + h < nchunk) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  const int c = (ch + h) * 16 + i;
+                  acc[c] = fmaf(sb * sa_cur[c], __uint_as_float(r[h][i]), acc[c]);
+                }
+              }
+            }
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty0 + 8 * b);
+        if (kb + 1 < KB) {
+          if (ld_lane) reinterpret_cast<float4*>(my_sa + ((kb + 1) & 1) * C::kHalf)[lane] = pre;
+          __syncwarp();
+        }
       }
       if (!ok) break;
       // D[e][token][n]: a warp writes 32 consecutive n of one token per store
@@ -664,6 +695,18 @@ extern "C" int moe_gemm_fp8_contig(const uint8_t* A, int64_t lda, const float* s
   return launch_tokens_m(A, M_capacity, lda, B, tiles, a, as_stream(stream));
 }
 
+extern "C" int moe_gemm_fp8_masked_variant(int32_t max_m, int32_t expected_m, int32_t flags) {
+  const int hint = expected_m > 0 ? expected_m : max_m;
+  bool weights_m = (max_m % 16 == 0) && hint <= 256;
+  if (flags & MOE_GEMM_FORCE_TOKENS_M) weights_m = false;
+  if (flags & MOE_GEMM_FORCE_WEIGHTS_M) {
+    if (max_m % 16 != 0) return MOE_ERR_UNSUPPORTED;
+    weights_m = true;
+  }
+  if (!weights_m) return 0;
+  return hint <= 48 ? 64 : hint <= 112 ? 128 : 256;
+}
+
 extern "C" int moe_gemm_fp8_masked(const uint8_t* A, const float* sA, const uint8_t* B,
                                    const float* sB, const int32_t* counts, int32_t E,
                                    int32_t max_m, int32_t N, int32_t K, int32_t expected_m,
@@ -694,19 +737,12 @@ extern "C" int moe_gemm_fp8_masked(const uint8_t* A, const float* sA, const uint
   // tokens and sizes the token side to the count, so it serves decode counts;
   // tokens-as-M is kept for large counts.  Host-side only: the counts stay on
   // the device.
-  const int hint = expected_m > 0 ? expected_m : max_m;
-  bool weights_m = (max_m % 16 == 0) && hint <= 256;
-  if (flags & MOE_GEMM_FORCE_TOKENS_M) weights_m = false;
-  if (flags & MOE_GEMM_FORCE_WEIGHTS_M) {
-    if (max_m % 16 != 0) return MOE_ERR_UNSUPPORTED;
-    weights_m = true;
-  }
+  const int variant = moe_gemm_fp8_masked_variant(max_m, expected_m, flags);
+  if (variant < 0) return MOE_ERR_UNSUPPORTED;
   cudaStream_t st = as_stream(stream);
-  if (weights_m) {
-    if (hint <= 48) return launch_weights_m<64>(A, B, a, st);
-    if (hint <= 112) return launch_weights_m<128>(A, B, a, st);
-    return launch_weights_m<256>(A, B, a, st);
-  }
+  if (variant == 64) return launch_weights_m<64>(A, B, a, st);
+  if (variant == 128) return launch_weights_m<128>(A, B, a, st);
+  if (variant == 256) return launch_weights_m<256>(A, B, a, st);
   const int64_t tiles = static_cast<int64_t>(E) * ((max_m + BM - 1) / BM) * ((N + BN - 1) / BN);
   return launch_tokens_m(A, static_cast<int64_t>(E) * max_m, K, B, tiles, a, st);
 }

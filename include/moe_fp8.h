@@ -188,6 +188,16 @@ int moe_gemm_fp8_masked(const uint8_t *A, const float *sA, const uint8_t *B, con
                         void *stream);
 
 /*
+ * Which masked-GEMM kernel moe_gemm_fp8_masked runs for these arguments
+ * (host-side, nothing launched): 0 = tokens-as-M (128 token rows x 256 weight
+ * rows per tile); 64 / 128 / 256 = weights-as-M with token tiles of that many
+ * columns; MOE_ERR_UNSUPPORTED if the flags ask for weights-as-M and max_m is
+ * not a multiple of 16.  The choice follows expected_m (0 = use max_m):
+ * weights-as-M up to 256 expected rows per expert, tokens-as-M above.
+ */
+int moe_gemm_fp8_masked_variant(int32_t max_m, int32_t expected_m, int32_t flags);
+
+/*
  * a5 -- fused SwiGLU + 1x128 requantisation (moe_swiglu_quant).
  *   h[r, i] = silu(g) * u,  g = Y1[r, i], u = Y1[r, I + i]   (gate first, then up)
  * computed in fp32 (silu(g) = g / (1 + exp(-g))), never rounded to bf16, then
