@@ -45,6 +45,7 @@ EXPORTED = [
     "moe_status_string", "moe_version", "moe_read_device_status", "moe_quant_fp8",
     "moe_quant_weight_fp8", "moe_contig_rows_bound", "moe_permute", "moe_gemm_fp8_contig",
     "moe_gemm_fp8_masked", "moe_gemm_fp8_masked_variant", "moe_swiglu_quant", "moe_combine", "moe_ffn_workspace_size", "moe_ffn",
+    "moe_ffn_noalloc", "moe_ffn_noalloc_capacity",
 ]
 
 _P = ctypes.c_void_p
@@ -87,6 +88,8 @@ _sig("moe_swiglu_quant", ctypes.c_int, [_P, _I64, _I32, _P, _I32, _P, _P, _P, _I
 _sig("moe_combine", ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I32, _I32, _P, _I64, _P, _P])
 _sig("moe_ffn_workspace_size", ctypes.c_size_t, [ctypes.POINTER(moe_ffn_desc)])
 _sig("moe_ffn", ctypes.c_int, [ctypes.POINTER(moe_ffn_desc), _P, ctypes.c_size_t, _P])
+_sig("moe_ffn_noalloc", ctypes.c_int, [ctypes.POINTER(moe_ffn_desc), _P])
+_sig("moe_ffn_noalloc_capacity", ctypes.c_size_t, [])
 
 
 class MoeError(RuntimeError):
@@ -266,6 +269,17 @@ def moe_ffn(desc: moe_ffn_desc, workspace: torch.Tensor, stream=None):
     least moe_ffn_workspace_size(desc) bytes, 256-byte aligned."""
     _check(_lib.moe_ffn(ctypes.byref(desc), _ptr(workspace), workspace.numel(), _stream(stream)),
            "moe_ffn")
+
+
+def moe_ffn_noalloc(desc: moe_ffn_desc, stream=None):
+    """a8 without a workspace argument: the intermediates live in the library's
+    fixed device scratch (moe_ffn_noalloc_capacity() bytes, shared by all calls;
+    calls that overlap on the GPU race).  For callers that cannot allocate."""
+    _check(_lib.moe_ffn_noalloc(ctypes.byref(desc), _stream(stream)), "moe_ffn_noalloc")
+
+
+def moe_ffn_noalloc_capacity() -> int:
+    return int(_lib.moe_ffn_noalloc_capacity())
 
 
 def alloc_workspace(desc: moe_ffn_desc, device=None) -> torch.Tensor:

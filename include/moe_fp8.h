@@ -260,6 +260,38 @@ typedef struct moe_ffn_desc {
 size_t moe_ffn_workspace_size(const moe_ffn_desc *desc);
 int moe_ffn(const moe_ffn_desc *desc, void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * moe_ffn without a caller-supplied workspace (no counterpart in the pages:
+ * this is a convenience of this library, not part of the method).
+ *
+ * Some callers cannot allocate device memory at the point where they run the
+ * FFN: a plug-in inside an inference runtime that owns all device memory and
+ * hands out only the tensors it plans, code that runs while a CUDA graph is
+ * being captured (where cudaMalloc is not allowed), or a latency-critical loop
+ * that must not stall on the allocator.  For them this call runs exactly the
+ * moe_ffn path, but keeps every intermediate in a scratch array that is part of
+ * the library's own device image, so neither the caller nor the library
+ * allocates anything.  The caller still passes the inputs and the output
+ * through `desc` (desc->err may be NULL, as in moe_ffn).
+ *
+ * Limits and rules:
+ *  - The scratch holds moe_ffn_noalloc_capacity() bytes (64 MiB); every GPU
+ *    that loads the library holds it until the process exits.  A descriptor
+ *    whose moe_ffn_workspace_size exceeds it is rejected with
+ *    MOE_ERR_UNSUPPORTED before anything is launched (the masked decode layout
+ *    needs about 40 KB per row of E*max_m at hidden 7168 / intermediate 2048).
+ *  - The first call on a device looks up the scratch's device address (with
+ *    that device current) and caches it; make that first call before any stream
+ *    capture on the device.
+ *  - All calls share the one array, which keeps the last call's contents.
+ *    Calls whose work overlaps on the GPU (other streams, or other host threads
+ *    on the same device) race on it: serialise them.  Nothing in the scratch
+ *    needs to start at zero.
+ *  - Return codes as moe_ffn.
+ */
+size_t moe_ffn_noalloc_capacity(void);
+int moe_ffn_noalloc(const moe_ffn_desc *desc, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
