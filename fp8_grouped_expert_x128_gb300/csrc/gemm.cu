@@ -12,10 +12,11 @@
 //  * persistent: one CTA per SM walks a linear tile list built on the device
 //    from the per-expert row extents (masked counts or contiguous offsets), so
 //    no host synchronisation is needed and skewed experts share the SMs evenly;
-//  * warp-specialised, 10 warps: warp 0 = TMA producer (4-stage ring of
+//  * warp-specialised, 12 warps: warp 0 = TMA producer (4-stage ring of
 //    128x128 A and 256x128 B byte tiles, 128-byte swizzle), warp 1 = a single
 //    thread issuing tcgen05.mma (M=128, N=256, K=32 x4 per 128-deep block),
-//    warps 2..9 = epilogue;
+//    warps 4..11 = epilogue (warps 2-3 only complete warpgroup 0, which hands
+//    its registers to the epilogue warpgroups with setmaxnreg);
 //  * scale promotion: the fp32 scales differ per row (sA) and per 128x128
 //    weight block (sB), so each 128-deep block is accumulated alone into one of
 //    two TMEM buffers (2 x 256 columns), and the epilogue warps read it with
@@ -33,7 +34,35 @@ constexpr int BN = 256;
 constexpr int BK = 128;
 constexpr int kStages = 4;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kEpiWarp0 = 4;                         // epilogue = warps 4..11 (warpgroups 1, 2)
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);  // warps 2-3 only hold warpgroup 0 together
+// Register split between warpgroups (setmaxnreg): warpgroup 0 (TMA + MMA
+// issue) needs few registers, the epilogue holds 128 fp32 accumulators per
+// thread.  The launch allocates kLaunchRegs to all 384 threads; warpgroup 0
+// gives back down to kRegsLow and the two epilogue warpgroups take kRegsHigh:
+// 128 * 40 + 256 * 232 = 64512 = 384 * 168, exactly the launch allocation, so
+// the increase never waits on registers that do not exist.  The host refuses to
+// launch a split kernel whose compiled register count differs from kLaunchRegs.
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsLow = 40;
+constexpr int kRegsHigh = 232;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kLaunchRegs, "register split");
+static_assert(kThreads * kLaunchRegs <= 65536, "register file");
+
+__device__ __forceinline__ void regs_release_low() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+}
+__device__ __forceinline__ void regs_acquire_high() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+}
+
+// The launch register count must equal kLaunchRegs for kernels that split.
+template <typename F>
+int check_split_regs(F kernel) {
+  cudaFuncAttributes attr;
+  if (cudaFuncGetAttributes(&attr, kernel) != cudaSuccess) return MOE_ERR_CUDA;
+  return attr.numRegs == kLaunchRegs ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
 constexpr uint32_t kATileBytes = BM * BK;
 constexpr uint32_t kBTileBytes = BN * BK;
 constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
@@ -162,7 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = sched.tile0[p.E];
-
+  if (warp < kEpiWarp0) {
+    regs_release_low();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && !(p.flags & MOE_GEMM_DEBUG_STALL)) {
@@ -233,10 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                           p.wait_limit_ns / 10);
       }
     }
+  }
   } else {
+    regs_acquire_high();
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                // TMEM lane quadrant of this warp
-    const int g = (warp - 2) >> 2;         // column half of the 256-wide tile
+    const int g = (warp - kEpiWarp0) >> 2;  // column half of the 256-wide tile
     uint32_t acc_it = 0;
     TileCursor cur;
     bool ok = true;
@@ -280,12 +312,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (active) {
           const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + g * 128;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tbase + c * 32, r);
+          for (int c = 0; c < 4; c += 2) {   // two 32-column loads in flight
+            uint32_t r0[32], r1[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, r0);
+            tmem_ld_32x32b_x32(tbase + (c + 1) * 32, r1);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(sc, __uint_as_float(r[i]), acc[c * 32 + i]);
+            for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(sc, __uint_as_float(r0[i]), acc[c * 32 + i]);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              acc[(c + 1) * 32 + i] = fmaf(sc, __uint_as_float(r1[i]), acc[(c + 1) * 32 + i]);
           }
         }
         tc_fence_before();
@@ -329,6 +365,7 @@ int launch_tokens_m(const uint8_t* A, int64_t a_rows, int64_t lda, const uint8_t
   if (int st = make_tmap_u8_sw128(&tmB, B, static_cast<uint64_t>(args.E) * args.N, args.K, args.K, BN))
     return st;
   const size_t smem = tokens_m_smem_bytes(args.E);
+  if (int st = check_split_regs(gemm_fp8_tokens_m_kernel)) return st;
   MOE_CUDA_TRY(cudaFuncSetAttribute(gemm_fp8_tokens_m_kernel,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem)));
@@ -361,7 +398,8 @@ struct WeightsM {
   static constexpr int kStages = (196608 / kStage) > 8 ? 8 : (196608 / kStage);
   static constexpr int kBufs = (512 / BNT) > 8 ? 8 : (512 / BNT);
   static constexpr int kHalf = BNT / 2;                        // columns per epilogue warpgroup
-  static constexpr int kPair = BNT <= 128 ? 2 : 1;             // TMEM loads in flight (registers)
+  static constexpr bool kSplitRegs = BNT > 128;                // 128 accumulators/thread need the split
+  static constexpr int kPair = 2;                              // TMEM loads in flight
   static constexpr size_t kScaleBufBytes = sizeof(float) * kEpiWarps * 2 * kHalf;
   static constexpr size_t smem_bytes(int E) {
     return 1024 + static_cast<size_t>(kStages) * kStage + (2 * kStages + 2 * kBufs) * 8 + 16 +
@@ -457,7 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = sched.tile0[p.E];
-
+  if (warp < kEpiWarp0) {
+    if constexpr (C::kSplitRegs) regs_release_low();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && !(p.flags & MOE_GEMM_DEBUG_STALL)) {
@@ -536,11 +575,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                           p.wait_limit_ns / 10);
       }
     }
+  }
   } else {
+    if constexpr (C::kSplitRegs) regs_acquire_high();
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;             // TMEM lanes = weight rows q*32 .. q*32+31
-    const int g = (warp - 2) >> 2;      // token columns [g*kHalf, (g+1)*kHalf)
-    float* my_sa = sa_stage + (warp - 2) * 2 * C::kHalf;
+    const int g = (warp - kEpiWarp0) >> 2;  // token columns [g*kHalf, (g+1)*kHalf)
+    float* my_sa = sa_stage + (warp - kEpiWarp0) * 2 * C::kHalf;
     uint32_t acc_it = 0;
     TileCursor cur;
     bool ok = true;
@@ -647,6 +688,9 @@ int launch_weights_m(const uint8_t* A, const uint8_t* B, GemmArgs& args, cudaStr
   if (int st = make_tmap_u8_sw128(&tmW, B, static_cast<uint64_t>(args.E) * args.N, args.K, args.K, 128))
     return st;
   const size_t smem = C::smem_bytes(args.E);
+  if (C::kSplitRegs) {
+    if (int st = check_split_regs(gemm_fp8_weights_m_kernel<BNT>)) return st;
+  }
   MOE_CUDA_TRY(cudaFuncSetAttribute(gemm_fp8_weights_m_kernel<BNT>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem)));

@@ -91,3 +91,34 @@ def test_contig_bound_and_workspace_plan(so):
     assert ws % 256 == 0
     d.H = 200
     assert moe.moe_ffn_workspace_size(d) == 0         # invalid descriptor
+
+
+def test_register_split_kernels_compile_to_the_launch_budget(tmp_path):
+    """The GEMM kernels that hand registers between warpgroups (setmaxnreg
+    40 / 232 over 384 threads) are only safe when they launch with exactly 168
+    registers per thread: 128*40 + 256*232 = 384*168.  Compile gemm.cu and
+    read ptxas's register report (the library also re-checks at launch)."""
+    import shutil
+    import subprocess
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    src = os.path.join(ROOT, "fp8_grouped_expert_x128_gb300", "csrc", "gemm.cu")
+    r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
+                        "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include"), "-Xptxas", "-v",
+                        "-c", src, "-o", str(tmp_path / "g.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-2000:]
+    report = {}
+    current = None
+    for line in r.stderr.splitlines():
+        m = re.search(r"Compiling entry function '(\S+)'", line)
+        if m:
+            current = m.group(1)
+        m = re.search(r"Used (\d+) registers", line)
+        if m and current:
+            report[current] = int(m.group(1))
+        m = re.search(r"(\d+) bytes spill stores", line)
+        if m and current and "gemm" in current:
+            assert int(m.group(1)) == 0, f"{current} spills"
+    split = [k for k in report if "tokens_m" in k or "weights_m_kernelILi256" in k]
+    assert len(split) == 2
+    for k in split:
+        assert report[k] == 168, (k, report[k])
