@@ -201,8 +201,16 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
   uint16_t* y2 = static_cast<uint16_t*>(at(p.off_y2));
   const bool masked = d->layout == MOE_LAYOUT_MASKED;
   cudaEvent_t* ev = reinterpret_cast<cudaEvent_t*>(d->stage_events);
+  // Under stream capture the stage events become external event-record nodes,
+  // which keep their timestamps when the graph is replayed.
+  unsigned ev_flags = cudaEventRecordDefault;
+  if (ev) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    MOE_CUDA_TRY(cudaStreamIsCapturing(st, &cap));
+    if (cap == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
+  }
   auto mark = [&](int i) -> int {
-    if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[i], st));
+    if (ev) MOE_CUDA_TRY(cudaEventRecordWithFlags(ev[i], st, ev_flags));
     return MOE_OK;
   };
   int rc;

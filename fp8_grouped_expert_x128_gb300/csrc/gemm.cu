@@ -24,6 +24,10 @@
 //    registers while the tensor cores fill the other buffer;
 //  * every wait is bounded (see common.cuh): a stalled pipeline flags
 //    MOE_DEV_TIMEOUT and the CTA unwinds, frees its TMEM and returns.
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "common.cuh"
 
 namespace moe {
@@ -56,12 +60,33 @@ __device__ __forceinline__ void regs_acquire_high() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
 }
 
-// The launch register count must equal kLaunchRegs for kernels that split.
+// Per-device, per-kernel launch set-up done once: the dynamic shared-memory
+// opt-in and, for kernels that split registers, the check that the launch
+// register count equals kLaunchRegs.  Keyed by (device, kernel address).
 template <typename F>
-int check_split_regs(F kernel) {
-  cudaFuncAttributes attr;
-  if (cudaFuncGetAttributes(&attr, kernel) != cudaSuccess) return MOE_ERR_CUDA;
-  return attr.numRegs == kLaunchRegs ? MOE_OK : MOE_ERR_UNSUPPORTED;
+int prepare_kernel(F kernel, size_t smem, bool split_regs) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> prepared;  // -> smem opted in
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  const auto key = std::make_pair(dev, reinterpret_cast<const void*>(kernel));
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = prepared.find(key);
+  if (it == prepared.end()) {
+    if (split_regs) {
+      cudaFuncAttributes attr;
+      if (cudaFuncGetAttributes(&attr, kernel) != cudaSuccess) return MOE_ERR_CUDA;
+      if (attr.numRegs != kLaunchRegs) return MOE_ERR_UNSUPPORTED;
+    }
+    it = prepared.emplace(key, 0).first;
+  }
+  if (smem > it->second) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    it->second = smem;
+  }
+  return MOE_OK;
 }
 constexpr uint32_t kATileBytes = BM * BK;
 constexpr uint32_t kBTileBytes = BN * BK;
@@ -365,10 +390,7 @@ int launch_tokens_m(const uint8_t* A, int64_t a_rows, int64_t lda, const uint8_t
   if (int st = make_tmap_u8_sw128(&tmB, B, static_cast<uint64_t>(args.E) * args.N, args.K, args.K, BN))
     return st;
   const size_t smem = tokens_m_smem_bytes(args.E);
-  if (int st = check_split_regs(gemm_fp8_tokens_m_kernel)) return st;
-  MOE_CUDA_TRY(cudaFuncSetAttribute(gemm_fp8_tokens_m_kernel,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(smem)));
+  if (int st = prepare_kernel(gemm_fp8_tokens_m_kernel, smem, true)) return st;
   if (args.wait_limit_ns == 0) args.wait_limit_ns = kWaitLimitNs;
   int64_t grid = num_sms();
   if (tiles_upper < grid) grid = tiles_upper;
@@ -688,12 +710,7 @@ int launch_weights_m(const uint8_t* A, const uint8_t* B, GemmArgs& args, cudaStr
   if (int st = make_tmap_u8_sw128(&tmW, B, static_cast<uint64_t>(args.E) * args.N, args.K, args.K, 128))
     return st;
   const size_t smem = C::smem_bytes(args.E);
-  if (C::kSplitRegs) {
-    if (int st = check_split_regs(gemm_fp8_weights_m_kernel<BNT>)) return st;
-  }
-  MOE_CUDA_TRY(cudaFuncSetAttribute(gemm_fp8_weights_m_kernel<BNT>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(smem)));
+  if (int st = prepare_kernel(gemm_fp8_weights_m_kernel<BNT>, smem, C::kSplitRegs)) return st;
   if (args.wait_limit_ns == 0) args.wait_limit_ns = kWaitLimitNs;
   const int64_t tiles_upper = static_cast<int64_t>(args.E) * ((args.max_m + BNT - 1) / BNT) * (args.N / 128);
   int64_t grid = num_sms();
