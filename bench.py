@@ -80,8 +80,8 @@ def make_desc(wl, out, err=None, stage_events=None, x=None, ids=None, w=None):
     return moe.make_ffn_desc(x if x is not None else wl["x"], ids if ids is not None else wl["topk_ids"],
                              w if w is not None else wl["topk_w"], wl["w13"], wl["w13_s"], wl["w2"],
                              wl["w2_s"], out, wl["routing"]["expert_begin"], cfg.E, wl["layout"],
-                             max_m=cfg.max_m, expected_m=wl["expected_m"], err=err,
-                             stage_events=stage_events)
+                             max_m=cfg.max_m, expected_m=wl["expected_m"],
+                             gemm_flags=wl.get("gemm_flags", 0), err=err, stage_events=stage_events)
 
 
 def algorithmic_counts(wl):
@@ -351,6 +351,9 @@ def main():
     ap.add_argument("--ref-step-s", type=float, default=4.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager moe_ffn calls instead of a CUDA graph")
+    ap.add_argument("--expected-m", type=int, default=None,
+                    help="override the per-expert count hint given to the masked GEMMs (tuning)")
+    ap.add_argument("--gemm-flags", type=int, default=0, help="MOE_GEMM_* flags for both GEMMs (tuning)")
     args = ap.parse_args()
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
@@ -364,6 +367,9 @@ def main():
 
     dev = torch.device("cuda", local if world > 1 else 0)
     wl = build_workload(args.workload, dev)
+    if args.expected_m is not None:
+        wl["expected_m"] = args.expected_m
+    wl["gemm_flags"] = args.gemm_flags
     cfg = wl["cfg"]
     T, H = wl["T"], cfg.H
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
@@ -490,7 +496,7 @@ def main():
         roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": achieved / fp8_peak}
     if wl["layout"] == moe.MOE_LAYOUT_MASKED:
-        v = moe.moe_gemm_fp8_masked_variant(cfg.max_m, wl["expected_m"], 0)
+        v = moe.moe_gemm_fp8_masked_variant(cfg.max_m, wl["expected_m"], args.gemm_flags)
         kname = "gemm_fp8_tokens_m_kernel" if v == 0 else f"gemm_fp8_weights_m_kernel<{v}>"
     else:
         kname = "gemm_fp8_tokens_m_kernel"
@@ -519,6 +525,7 @@ def main():
                        "tokens": "routed (token, local expert) rows", "rows_per_step": wl["rows"],
                        "local_tokens": T, "counts": [int(c) for c in wl["counts"]],
                        "max_m": cfg.max_m, "active_experts": wl["active_experts"],
+                       "expected_m_hint": wl["expected_m"], "gemm_flags": args.gemm_flags,
                        "l2": "flushed (256 MiB write) before every timed step",
                        "launch": "eager moe_ffn" if graph is None else "moe_ffn captured once in a CUDA graph, replayed per step",
                        "parallelism": f"replicas x{world}"},
