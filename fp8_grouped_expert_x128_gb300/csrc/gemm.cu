@@ -47,6 +47,7 @@ constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);  // warps 2-3 only hold w
 // 128 * 40 + 256 * 232 = 64512 = 384 * 168, exactly the launch allocation, so
 // the increase never waits on registers that do not exist.  The host refuses to
 // launch a split kernel whose compiled register count differs from kLaunchRegs.
+constexpr int kScaleAhead = 4;                       // scale prefetch distance (k-blocks)
 constexpr int kLaunchRegs = 168;
 constexpr int kRegsLow = 40;
 constexpr int kRegsHigh = 232;
@@ -315,16 +316,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       float acc[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) acc[i] = 0.f;
-      // scales of k-block kb+1 are loaded while kb is waited for and processed
-      float sa_next = row_ok ? __ldg(sa_ptr) : 0.f;
-      float sb_next = __ldg(sb_ptr);
+      // The scales run kScaleAhead k-blocks ahead of their use in a register
+      // ring (rotated, so every index is static): a global load has several
+      // k-blocks of work to hide behind, not one.
+      auto load_sa = [&](int k) { return (row_ok && k < KB) ? __ldg(sa_ptr + static_cast<int64_t>(k) * p.sA_G) : 0.f; };
+      auto load_sb = [&](int k) { return k < KB ? __ldg(sb_ptr + k) : 0.f; };
+      float sa0 = load_sa(0), sa1 = load_sa(1), sa2 = load_sa(2), sa3 = load_sa(3);
+      float sb0 = load_sb(0), sb1 = load_sb(1), sb2 = load_sb(2), sb3 = load_sb(3);
       for (int kb = 0; kb < KB; ++kb, ++acc_it) {
         const uint32_t b = acc_it & 1, tph = (acc_it >> 1) & 1;
-        const float sc = sa_next * sb_next;
-        if (kb + 1 < KB) {
-          sa_next = row_ok ? __ldg(sa_ptr + static_cast<int64_t>(kb + 1) * p.sA_G) : 0.f;
-          sb_next = __ldg(sb_ptr + kb + 1);
-        }
+        const float sc = sa0 * sb0;
+        sa0 = sa1; sa1 = sa2; sa2 = sa3; sa3 = load_sa(kb + kScaleAhead);
+        sb0 = sb1; sb1 = sb2; sb2 = sb3; sb3 = load_sb(kb + kScaleAhead);
         // one lane waits, the warp follows it: tcgen05.ld is warp-collective
         int got = 1;
         if (lane == 0) got = mbar_wait_bounded(tfull0 + 8 * b, tph, abort, p.err, p.wait_limit_ns);
@@ -619,27 +622,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nchunk = my_cols / 16;
       const float* sa_base = p.sA + static_cast<int64_t>(e) * KB * p.max_m + j * BNT + col0;
       const float* sb_ptr = p.sB + (static_cast<int64_t>(e) * nblk + nb) * KB;
-      // The token scales of k-block kb+1 are fetched while kb is processed and
-      // parked in this warp's shared double buffer (one float4 per lane), so
-      // the epilogue never waits on a global load after its TMEM wait.
+      // Token scales run kScaleAhead k-blocks ahead of their use: one float4
+      // per lane in a register ring (rotated, static indices), parked in this
+      // warp's shared double buffer one k-block before use, so no global load
+      // latency sits on the per-k-block path.
       const bool ld_lane = lane * 4 < my_cols;
-      float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (ld_lane) pre = __ldg(reinterpret_cast<const float4*>(sa_base) + lane);
-      float sb_next = __ldg(sb_ptr);
-      __syncwarp();
-      if (ld_lane) reinterpret_cast<float4*>(my_sa)[lane] = pre;
-      __syncwarp();
+      auto load_sa4 = [&](int k) {
+        return (ld_lane && k < KB)
+                   ? __ldg(reinterpret_cast<const float4*>(sa_base + static_cast<int64_t>(k) * p.max_m) + lane)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      };
+      auto load_sb = [&](int k) { return k < KB ? __ldg(sb_ptr + k) : 0.f; };
+      float4 pa1 = load_sa4(1), pa2 = load_sa4(2), pa3 = load_sa4(3);
+      float sb0 = load_sb(0), sb1 = load_sb(1), sb2 = load_sb(2), sb3 = load_sb(3);
+      {
+        const float4 pa0 = load_sa4(0);
+        __syncwarp();
+        if (ld_lane) reinterpret_cast<float4*>(my_sa)[lane] = pa0;
+        __syncwarp();
+      }
       float acc[C::kHalf];
 #pragma unroll
       for (int i = 0; i < C::kHalf; ++i) acc[i] = 0.f;
       for (int kb = 0; kb < KB; ++kb, ++acc_it) {
         const uint32_t b = acc_it % C::kBufs, tph = (acc_it / C::kBufs) & 1;
-        const float sb = sb_next;
-        if (kb + 1 < KB) {
-          if (ld_lane)
-            pre = __ldg(reinterpret_cast<const float4*>(sa_base + static_cast<int64_t>(kb + 1) * p.max_m) + lane);
-          sb_next = __ldg(sb_ptr + kb + 1);
-        }
+        const float sb = sb0;
+        const float4 pa4 = load_sa4(kb + kScaleAhead);
+        sb0 = sb1; sb1 = sb2; sb2 = sb3; sb3 = load_sb(kb + kScaleAhead);
         int got = 1;
         if (lane == 0) got = mbar_wait_bounded(tfull0 + 8 * b, tph, abort, p.err, p.wait_limit_ns);
         got = __shfl_sync(0xffffffffu, got, 0);
@@ -673,9 +682,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty0 + 8 * b);
         if (kb + 1 < KB) {
-          if (ld_lane) reinterpret_cast<float4*>(my_sa + ((kb + 1) & 1) * C::kHalf)[lane] = pre;
+          if (ld_lane) reinterpret_cast<float4*>(my_sa + ((kb + 1) & 1) * C::kHalf)[lane] = pa1;
           __syncwarp();
         }
+        pa1 = pa2; pa2 = pa3; pa3 = pa4;
       }
       if (!ok) break;
       // D[e][token][n]: a warp writes 32 consecutive n of one token per store
