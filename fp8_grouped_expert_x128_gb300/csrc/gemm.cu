@@ -313,9 +313,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t grp = gr / p.sA_G, pos = gr - grp * p.sA_G;
       const float* sa_ptr = p.sA + grp * KB * p.sA_G + pos;
       const float* sb_ptr = p.sB + (static_cast<int64_t>(e) * NB + (active ? n0 / 128 : 0)) * KB;
-      float acc[128];
+      // fp32 accumulators as pairs: the promotion runs as packed FMAs
+      // (two round-to-nearest fp32 FMAs per instruction, same bits as fmaf)
+      float2 acc[64];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) acc[i] = 0.f;
+      for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.f, 0.f);
       // The scales run kScaleAhead k-blocks ahead of their use in a register
       // ring (rotated, so every index is static): a global load has several
       // k-blocks of work to hide behind, not one.
@@ -339,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (active) {
           const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + g * 128;
+          const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
           for (int c = 0; c < 4; c += 2) {   // two 32-column loads in flight
             uint32_t r0[32], r1[32];
@@ -346,10 +349,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_32x32b_x32(tbase + (c + 1) * 32, r1);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(sc, __uint_as_float(r0[i]), acc[c * 32 + i]);
+            for (int i = 0; i < 16; ++i)
+              acc[c * 16 + i] = __ffma2_rn(sc2, make_float2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1])),
+                                           acc[c * 16 + i]);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              acc[(c + 1) * 32 + i] = fmaf(sc, __uint_as_float(r1[i]), acc[(c + 1) * 32 + i]);
+            for (int i = 0; i < 16; ++i)
+              acc[(c + 1) * 16 + i] = __ffma2_rn(
+                  sc2, make_float2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])), acc[(c + 1) * 16 + i]);
           }
         }
         tc_fence_before();
@@ -364,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t o[4];
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
-            const __nv_bfloat162 bb = __floats2bfloat162_rn(acc[v * 8 + 2 * h], acc[v * 8 + 2 * h + 1]);
+            const __nv_bfloat162 bb = __floats2bfloat162_rn(acc[v * 4 + h].x, acc[v * 4 + h].y);
             o[h] = *reinterpret_cast<const uint32_t*>(&bb);
           }
           dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -641,9 +647,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ld_lane) reinterpret_cast<float4*>(my_sa)[lane] = pa0;
         __syncwarp();
       }
-      float acc[C::kHalf];
+      float2 acc[C::kHalf / 2];
 #pragma unroll
-      for (int i = 0; i < C::kHalf; ++i) acc[i] = 0.f;
+      for (int i = 0; i < C::kHalf / 2; ++i) acc[i] = make_float2(0.f, 0.f);
       for (int kb = 0; kb < KB; ++kb, ++acc_it) {
         const uint32_t b = acc_it % C::kBufs, tph = (acc_it / C::kBufs) & 1;
         const float sb = sb0;
@@ -670,9 +676,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int h = 0; h < C::kPair; ++h) {
               if (ch + h < nchunk) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                  const int c = (ch + h) * 16 + i;
-                  acc[c] = fmaf(sb * sa_cur[c], __uint_as_float(r[h][i]), acc[c]);
+                for (int i = 0; i < 8; ++i) {
+                  const int c = (ch + h) * 16 + 2 * i;
+                  const float2 s2 = __fmul2_rn(make_float2(sb, sb), make_float2(sa_cur[c], sa_cur[c + 1]));
+                  acc[c / 2] = __ffma2_rn(
+                      s2, make_float2(__uint_as_float(r[h][2 * i]), __uint_as_float(r[h][2 * i + 1])), acc[c / 2]);
                 }
               }
             }
@@ -695,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < C::kHalf; ++c) {
         if (c < valid) {
-          const __nv_bfloat16 v = __float2bfloat16_rn(acc[c]);
+          const __nv_bfloat16 v = __float2bfloat16_rn((c & 1) ? acc[c / 2].y : acc[c / 2].x);
           dcol[static_cast<int64_t>(c) * p.N] = *reinterpret_cast<const uint16_t*>(&v);
         }
       }
@@ -767,8 +775,11 @@ extern "C" int moe_gemm_fp8_contig(const uint8_t* A, int64_t lda, const float* s
 }
 
 extern "C" int moe_gemm_fp8_masked_variant(int32_t max_m, int32_t expected_m, int32_t flags) {
+  // Measured on GB300: weights-as-M wins only for a few tokens per expert
+  // (all-experts decode, 1-8 rows each); from ~100 rows per expert the
+  // tokens-as-M tile moves fewer bytes per k-block and is about 2x faster.
   const int hint = expected_m > 0 ? expected_m : max_m;
-  bool weights_m = (max_m % 16 == 0) && hint <= 256;
+  bool weights_m = (max_m % 16 == 0) && hint <= 32;
   if (flags & MOE_GEMM_FORCE_TOKENS_M) weights_m = false;
   if (flags & MOE_GEMM_FORCE_WEIGHTS_M) {
     if (max_m % 16 != 0) return MOE_ERR_UNSUPPORTED;

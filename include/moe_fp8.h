@@ -193,7 +193,9 @@ int moe_gemm_fp8_masked(const uint8_t *A, const float *sA, const uint8_t *B, con
  * rows per tile); 64 / 128 / 256 = weights-as-M with token tiles of that many
  * columns; MOE_ERR_UNSUPPORTED if the flags ask for weights-as-M and max_m is
  * not a multiple of 16.  The choice follows expected_m (0 = use max_m):
- * weights-as-M up to 256 expected rows per expert, tokens-as-M above.
+ * weights-as-M (64-column token tiles) up to 32 expected rows per expert,
+ * tokens-as-M above.  MOE_GEMM_FORCE_WEIGHTS_M with expected_m in (48, 112]
+ * or above 112 selects the 128- or 256-column token tiles.
  */
 int moe_gemm_fp8_masked_variant(int32_t max_m, int32_t expected_m, int32_t flags);
 
