@@ -530,13 +530,13 @@ def main():
                        "launch": "eager moe_ffn" if graph is None else "moe_ffn captured once in a CUDA graph, replayed per step",
                        "parallelism": f"replicas x{world}"},
             "stage_ms": {n: round(v, 4) for n, v in zip(
-                ["quant", "permute", "gemm1", "swiglu_quant", "gemm2", "combine"], stage_ms)},
+                ["quant (fused into permute)", "quant+permute", "gemm1", "swiglu_quant", "gemm2", "combine"], stage_ms)},
             "tflops": alg["flops"] / (ms_per_step / 1e3) / 1e12,
             "weight_gbs": alg["weight_bytes"] / (ms_per_step / 1e3) / 1e9,
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 7 * args.steps,
+            "gpu_launches": 6 * args.steps,
             "clocks": clk.summary(),
             "device_status": moe.moe_status_string(status),
             "wall_s_timed": t_wall,

@@ -84,7 +84,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 
 struct FfnPlan {
   int64_t T_pad, rows, s_ld1, s_ld2;
-  size_t off_qx, off_sx, off_counts, off_offsets, off_mind, off_rowsrc, off_dst, off_a1, off_sa1,
+  size_t off_counts, off_offsets, off_mind, off_rowsrc, off_dst, off_a1, off_sa1,
       off_y1, off_a2, off_sa2, off_y2, total;
 };
 
@@ -112,8 +112,6 @@ int plan_ffn(const moe_ffn_desc* d, FfnPlan* p) {
     o = align256(o + bytes);
     return at;
   };
-  p->off_qx = take(static_cast<size_t>(d->T) * H);
-  p->off_sx = take(sizeof(float) * (H / 128) * p->T_pad);
   p->off_counts = take(sizeof(int32_t) * E);
   p->off_offsets = take(sizeof(int32_t) * (E + 1));
   p->off_mind = take(sizeof(int32_t) * p->rows);
@@ -186,8 +184,6 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
   cudaStream_t st = as_stream(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   auto at = [&](size_t off) { return static_cast<void*>(ws + off); };
-  uint8_t* qx = static_cast<uint8_t*>(at(p.off_qx));
-  float* sx = static_cast<float*>(at(p.off_sx));
   int32_t* counts = static_cast<int32_t*>(at(p.off_counts));
   int32_t* offsets = static_cast<int32_t*>(at(p.off_offsets));
   int32_t* mind = static_cast<int32_t*>(at(p.off_mind));
@@ -214,12 +210,13 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
     return MOE_OK;
   };
   int rc;
+  // stages 1+2: routing index pass, then each routed token row is quantised
+  // straight into its expert slot (no token-order FP8 copy in between)
   if ((rc = mark(0))) return rc;
-  if ((rc = moe_quant_fp8(d->x, d->T, d->H, d->H, qx, d->H, sx, p.T_pad, d->err, stream))) return rc;
   if ((rc = mark(1))) return rc;
-  if ((rc = moe_permute(qx, sx, p.T_pad, d->topk_ids, d->T, d->H, d->k, d->expert_begin, d->E,
-                        d->layout, d->max_m, a1, sa1, p.s_ld1, counts, offsets, mind, rowsrc, dst,
-                        p.rows, d->err, stream)))
+  if ((rc = permute_launch(nullptr, nullptr, 0, d->x, d->H, d->topk_ids, d->T, d->H, d->k,
+                           d->expert_begin, d->E, d->layout, d->max_m, a1, sa1, p.s_ld1, counts,
+                           offsets, mind, rowsrc, dst, p.rows, d->err, st)))
     return rc;
   if ((rc = mark(2))) return rc;
   if (masked)

@@ -35,6 +35,15 @@ inline int launch_status() {
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// Permute (index pass + row gather), shared by moe_permute and moe_ffn.  With
+// x != nullptr the rows are quantised from bf16 on the way (1x128 rule).
+int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_t* x, int64_t ldx,
+                   const int32_t* topk_ids, int64_t T, int32_t H, int32_t k,
+                   int32_t expert_begin, int32_t E, int32_t layout, int32_t max_m,
+                   uint8_t* q_out, float* s_out, int64_t s_out_ld, int32_t* counts,
+                   int32_t* offsets, int32_t* m_indices, int32_t* row_src, int32_t* dst_row,
+                   int64_t rows_capacity, int32_t* err, cudaStream_t st);
+
 // Encode a 2-D K-major uint8 tensor map with 128-byte swizzle:
 // global [rows, cols] (row stride ld bytes), box [box_rows, 128 bytes].
 int make_tmap_u8_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
@@ -233,5 +242,47 @@ __device__ __forceinline__ uint16_t e4m3x2_rn_satfinite(float a, float b) {
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);
 }
+
+
+// ---- 1x128 block quantisation helpers (one half-warp per 128-element block,
+// 8 bf16 per lane): s = fp32(max(amax, 1e-4) / 448), q = e4m3(fp32(x / s)),
+// both IEEE float32 divisions.  Every kernel that quantises uses these, so the
+// bytes are the same whichever kernel wrote them.
+constexpr float kQuantFloor = 1e-4f;
+constexpr float kQuantMax = 448.0f;
+
+__device__ __forceinline__ float half_warp_max(float v) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// Quantise 8 values with scale s into 8 E4M3 bytes (element 0 in the low byte).
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t a = e4m3x2_rn_satfinite(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
+    const uint32_t b =
+        e4m3x2_rn_satfinite(__fdiv_rn(f[4 + 2 * i], s), __fdiv_rn(f[4 + 2 * i + 1], s));
+    lo |= a << (16 * i);
+    hi |= b << (16 * i);
+  }
+  return make_uint2(lo, hi);
+}
+
+__device__ __forceinline__ float block_scale(float amax) {
+  return __fdiv_rn(fmaxf(amax, kQuantFloor), kQuantMax);
+}
+
 
 }  // namespace moe

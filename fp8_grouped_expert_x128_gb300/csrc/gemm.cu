@@ -343,19 +343,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + g * 128;
           const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
-          for (int c = 0; c < 4; c += 2) {   // two 32-column loads in flight
-            uint32_t r0[32], r1[32];
-            tmem_ld_32x32b_x32(tbase + c * 32, r0);
-            tmem_ld_32x32b_x32(tbase + (c + 1) * 32, r1);
+          for (int c = 0; c < 8; c += 2) {   // two 16-column loads in flight
+            uint32_t r0[16], r1[16];
+            tmem_ld_32x32b_x16(tbase + c * 16, r0);
+            tmem_ld_32x32b_x16(tbase + (c + 1) * 16, r1);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              acc[c * 16 + i] = __ffma2_rn(sc2, make_float2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1])),
-                                           acc[c * 16 + i]);
+            for (int i = 0; i < 8; ++i)
+              acc[c * 8 + i] = __ffma2_rn(sc2, make_float2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1])),
+                                          acc[c * 8 + i]);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              acc[(c + 1) * 16 + i] = __ffma2_rn(
-                  sc2, make_float2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])), acc[(c + 1) * 16 + i]);
+            for (int i = 0; i < 8; ++i)
+              acc[(c + 1) * 8 + i] = __ffma2_rn(
+                  sc2, make_float2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])), acc[(c + 1) * 8 + i]);
           }
         }
         tc_fence_before();

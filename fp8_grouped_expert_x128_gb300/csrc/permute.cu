@@ -13,7 +13,8 @@
 // permute: one CTA of 1024 threads assigns every routed row a destination in
 // ascending assignment order (deterministic), counting with warp match masks
 // and a per-warp table in shared memory; a second kernel copies the 1-byte
-// rows (16-byte vectors, one warp per row) and gathers their fp32 scales.
+// rows (16-byte vectors, one warp per row) and gathers their fp32 scales, or --
+// inside moe_ffn -- quantises the bf16 token rows straight into their slots.
 // combine: one CTA per token, fp32 accumulation over the k choices in order.
 #include "common.cuh"
 
@@ -157,47 +158,116 @@ __global__ void __launch_bounds__(128) permute_scatter_kernel(
   for (int64_t kb = lane; kb < KB; kb += 32) s_out[(grp * KB + kb) * G + pos] = __ldg(s + kb * s_ld + t);
 }
 
-// One CTA per token; each thread owns 8 consecutive columns per step.
-__global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict__ y2, int64_t ldy,
-                                                      int64_t y_rows,
-                                                      const int32_t* __restrict__ dst_row,
-                                                      const float* __restrict__ topk_w, int32_t k,
-                                                      int64_t H, uint16_t* __restrict__ out,
-                                                      int64_t ldo, int32_t* err) {
+// Fused 1x128 quantisation + scatter for moe_ffn: one warp per routed row
+// quantises the token's bf16 row straight into its expert slot (the bytes equal
+// moe_quant_fp8 followed by moe_permute: same helpers, same arithmetic).
+__global__ void __launch_bounds__(128) quant_scatter_kernel(
+    const uint16_t* __restrict__ x, int64_t ldx, const int32_t* __restrict__ dst_row,
+    int64_t n_assign, int32_t k, int64_t H, uint8_t* __restrict__ q_out, float* __restrict__ s_out,
+    int64_t G) {
+  const int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (i >= n_assign) return;
+  const int32_t dst = __ldg(dst_row + i);
+  if (dst < 0) return;
+  const int64_t t = i / k;
+  const int64_t KB = H / 128;
+  const int64_t grp = dst / G, pos = dst - grp * G;
+  const uint16_t* xr = x + t * ldx;
+  uint8_t* qr = q_out + static_cast<int64_t>(dst) * H;
+  for (int64_t kb0 = 0; kb0 < KB; kb0 += 2) {
+    const int64_t kb = kb0 + (lane >> 4);
+    const bool active = kb < KB;
+    const int64_t col = kb * 128 + (lane & 15) * 8;
+    float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (active) unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(xr + col)), f);
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    amax = half_warp_max(amax);
+    if (active) {
+      const float sc = block_scale(amax);
+      *reinterpret_cast<uint2*>(qr + col) = quant8(f, sc);
+      if ((lane & 15) == 0) s_out[(grp * KB + kb) * G + pos] = sc;
+    }
+  }
+}
+
+// One CTA per token.  The token's valid routing slots are compacted first
+// (order kept); then for each slot a thread issues all of its 16-byte row loads
+// (kCombVec chunks of 8 columns, strided by the block) before accumulating, so
+// the loads of one token overlap instead of running one after another.
+// Accumulation per element is fp32 fmaf in slot order.
+constexpr int kCombThreads = 128;
+constexpr int kCombVec = 8;
+
+__global__ void __launch_bounds__(kCombThreads) combine_kernel(
+    const uint16_t* __restrict__ y2, int64_t ldy, int64_t y_rows, const int32_t* __restrict__ dst_row,
+    const float* __restrict__ topk_w, int32_t k, int64_t H, uint16_t* __restrict__ out, int64_t ldo,
+    int32_t* err) {
   __shared__ int32_t s_dst[32];
   __shared__ float s_w[32];
+  __shared__ int s_n;
   const int64_t t = blockIdx.x;
-  if (threadIdx.x < k) {
-    int32_t d = dst_row[t * k + threadIdx.x];
-    if (d >= y_rows) {
-      set_err(err, MOE_DEV_BAD_INDEX);
-      d = -1;
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    int32_t d = -1;
+    float w = 0.f;
+    if (tid < k) {
+      d = dst_row[t * k + tid];
+      if (d >= y_rows) {
+        set_err(err, MOE_DEV_BAD_INDEX);
+        d = -1;
+      }
+      w = topk_w[t * k + tid];
     }
-    s_dst[threadIdx.x] = d;
-    s_w[threadIdx.x] = topk_w[t * k + threadIdx.x];
+    const uint32_t valid = __ballot_sync(0xffffffffu, d >= 0);
+    if (d >= 0) {
+      const int slot = __popc(valid & ((1u << tid) - 1u));
+      s_dst[slot] = d;
+      s_w[slot] = w;
+    }
+    if (tid == 0) s_n = __popc(valid);
   }
   __syncthreads();
-  for (int64_t c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int j = 0; j < k; ++j) {
-      const int32_t d = s_dst[j];
-      if (d < 0) continue;
-      const float w = s_w[j];
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(y2 + static_cast<int64_t>(d) * ldy + c));
-      const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+  const int n = s_n;
+  for (int64_t base = 0; base < H; base += static_cast<int64_t>(kCombThreads) * 8 * kCombVec) {
+    float acc[kCombVec][8];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        acc[2 * h] = fmaf(w, __uint_as_float(v[h] << 16), acc[2 * h]);
-        acc[2 * h + 1] = fmaf(w, __uint_as_float(v[h] & 0xFFFF0000u), acc[2 * h + 1]);
+    for (int v = 0; v < kCombVec; ++v)
+#pragma unroll
+      for (int h = 0; h < 8; ++h) acc[v][h] = 0.f;
+    for (int jj = 0; jj < n; ++jj) {
+      const uint16_t* row = y2 + static_cast<int64_t>(s_dst[jj]) * ldy;
+      const float w = s_w[jj];
+      uint4 u[kCombVec];
+#pragma unroll
+      for (int v = 0; v < kCombVec; ++v) {
+        const int64_t c = base + (static_cast<int64_t>(v) * kCombThreads + tid) * 8;
+        u[v] = c < H ? __ldg(reinterpret_cast<const uint4*>(row + c)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int v = 0; v < kCombVec; ++v) {
+        const uint32_t x[4] = {u[v].x, u[v].y, u[v].z, u[v].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          acc[v][2 * h] = fmaf(w, __uint_as_float(x[h] << 16), acc[v][2 * h]);
+          acc[v][2 * h + 1] = fmaf(w, __uint_as_float(x[h] & 0xFFFF0000u), acc[v][2 * h + 1]);
+        }
       }
     }
-    uint32_t o[4];
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * h], acc[2 * h + 1]);
-      o[h] = *reinterpret_cast<const uint32_t*>(&b);
+    for (int v = 0; v < kCombVec; ++v) {
+      const int64_t c = base + (static_cast<int64_t>(v) * kCombThreads + tid) * 8;
+      if (c >= H) continue;
+      uint32_t o[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[v][2 * h], acc[v][2 * h + 1]);
+        o[h] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      *reinterpret_cast<uint4*>(out + t * ldo + c) = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    *reinterpret_cast<uint4*>(out + t * ldo + c) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -211,12 +281,17 @@ extern "C" int64_t moe_contig_rows_bound(int64_t assignments, int32_t E) {
   return (assignments + 127ll * E) / 128 * 128;
 }
 
-extern "C" int moe_permute(const uint8_t* q, const float* s, int64_t s_ld, const int32_t* topk_ids,
-                           int64_t T, int32_t H, int32_t k, int32_t expert_begin, int32_t E,
-                           int32_t layout, int32_t max_m, uint8_t* q_out, float* s_out,
-                           int64_t s_out_ld, int32_t* counts, int32_t* offsets,
-                           int32_t* m_indices, int32_t* row_src, int32_t* dst_row,
-                           int64_t rows_capacity, int32_t* err, void* stream) {
+namespace moe {
+
+// Shared by moe_permute and moe_ffn: validate, run the index pass, then either
+// gather already-quantised rows (q, s) or, when x is given, quantise the bf16
+// token rows straight into the grouped layout.
+int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_t* x, int64_t ldx,
+                   const int32_t* topk_ids, int64_t T, int32_t H, int32_t k,
+                   int32_t expert_begin, int32_t E, int32_t layout, int32_t max_m,
+                   uint8_t* q_out, float* s_out, int64_t s_out_ld, int32_t* counts,
+                   int32_t* offsets, int32_t* m_indices, int32_t* row_src, int32_t* dst_row,
+                   int64_t rows_capacity, int32_t* err, cudaStream_t st) {
   MOE_CHECK_ARG(T >= 0 && H > 0 && H % 128 == 0 && k >= 1 && k <= 32);
   MOE_CHECK_ARG(E >= 1 && E <= kMaxExperts);
   MOE_CHECK_ARG(layout == MOE_LAYOUT_MASKED || layout == MOE_LAYOUT_CONTIG);
@@ -233,11 +308,14 @@ extern "C" int moe_permute(const uint8_t* q, const float* s, int64_t s_ld, const
     G = s_out_ld;
   }
   if (T > 0) {
-    MOE_CHECK_ARG(q && s && topk_ids && dst_row && aligned16(q) && s_ld >= T);
+    MOE_CHECK_ARG(topk_ids && dst_row);
+    if (x != nullptr)
+      MOE_CHECK_ARG(aligned16(x) && ldx >= H && ldx % 8 == 0);
+    else
+      MOE_CHECK_ARG(q && s && aligned16(q) && s_ld >= T);
   }
   MOE_CHECK_ARG(T * k < (1ll << 31));
-  if (int st = check_device()) return st;
-  cudaStream_t st = as_stream(stream);
+  if (int rc = check_device()) return rc;
   IndexParams p{topk_ids, T * k, expert_begin, E, layout, max_m, rows_capacity,
                 counts, offsets, m_indices, row_src, dst_row, err};
   size_t smem = sizeof(int32_t) * (2 * E + kIdxWarps * E);
@@ -253,9 +331,25 @@ extern "C" int moe_permute(const uint8_t* q, const float* s, int64_t s_ld, const
   if (int rc = launch_status()) return rc;
   if (T == 0) return MOE_OK;
   const int64_t n = T * k;
-  permute_scatter_kernel<<<static_cast<unsigned>((n + 3) / 4), 128, 0, st>>>(
-      q, s, s_ld, dst_row, n, k, H, q_out, s_out, G);
+  const unsigned grid = static_cast<unsigned>((n + 3) / 4);
+  if (x != nullptr)
+    quant_scatter_kernel<<<grid, 128, 0, st>>>(x, ldx, dst_row, n, k, H, q_out, s_out, G);
+  else
+    permute_scatter_kernel<<<grid, 128, 0, st>>>(q, s, s_ld, dst_row, n, k, H, q_out, s_out, G);
   return launch_status();
+}
+
+}  // namespace moe
+
+extern "C" int moe_permute(const uint8_t* q, const float* s, int64_t s_ld, const int32_t* topk_ids,
+                           int64_t T, int32_t H, int32_t k, int32_t expert_begin, int32_t E,
+                           int32_t layout, int32_t max_m, uint8_t* q_out, float* s_out,
+                           int64_t s_out_ld, int32_t* counts, int32_t* offsets,
+                           int32_t* m_indices, int32_t* row_src, int32_t* dst_row,
+                           int64_t rows_capacity, int32_t* err, void* stream) {
+  return permute_launch(q, s, s_ld, nullptr, 0, topk_ids, T, H, k, expert_begin, E, layout, max_m,
+                        q_out, s_out, s_out_ld, counts, offsets, m_indices, row_src, dst_row,
+                        rows_capacity, err, as_stream(stream));
 }
 
 extern "C" int moe_combine(const uint16_t* Y2, int64_t ldy, int64_t y_rows, const int32_t* dst_row,
@@ -267,7 +361,7 @@ extern "C" int moe_combine(const uint16_t* Y2, int64_t ldy, int64_t y_rows, cons
   MOE_CHECK_ARG(ldy >= H && ldy % 8 == 0 && ldo >= H && ldo % 8 == 0 && y_rows >= 0);
   MOE_CHECK_ARG(T < (1ll << 31));
   if (int st = check_device()) return st;
-  combine_kernel<<<static_cast<unsigned>(T), 128, 0, as_stream(stream)>>>(
+  combine_kernel<<<static_cast<unsigned>(T), kCombThreads, 0, as_stream(stream)>>>(
       Y2, ldy, y_rows, dst_row, topk_w, k, H, out, ldo, err);
   return launch_status();
 }

@@ -15,42 +15,6 @@
 namespace moe {
 namespace {
 
-constexpr float kFloor = 1e-4f;
-constexpr float kE4M3Max = 448.0f;
-
-__device__ __forceinline__ float half_warp_max(float v) {
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
-__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float (&f)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
-// Quantise 8 values with scale s into 8 E4M3 bytes (element 0 in the low byte).
-__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
-  uint32_t lo = 0, hi = 0;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint32_t a = e4m3x2_rn_satfinite(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
-    const uint32_t b =
-        e4m3x2_rn_satfinite(__fdiv_rn(f[4 + 2 * i], s), __fdiv_rn(f[4 + 2 * i + 1], s));
-    lo |= a << (16 * i);
-    hi |= b << (16 * i);
-  }
-  return make_uint2(lo, hi);
-}
-
-__device__ __forceinline__ float block_scale(float amax) {
-  return __fdiv_rn(fmaxf(amax, kFloor), kE4M3Max);
-}
-
 // ---------------------------------------------------------------- a1
 // One warp covers 256 columns of one row: lanes 0-15 block 2w, 16-31 block 2w+1.
 __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __restrict__ x,

@@ -236,7 +236,9 @@ int moe_combine(const uint16_t *Y2, int64_t ldy, int64_t y_rows,
  * workspace: device, at least moe_ffn_workspace_size(desc) bytes, 256-byte
  * aligned; holds every intermediate.  stage_events (optional, may be NULL):
  * 7 cudaEvent_t handles recorded on `stream` before stage 1 and after each of
- * the six stages, for per-stage timing.
+ * the six stages, for per-stage timing.  moe_ffn quantises each routed token
+ * row straight into its expert slot (stages 1 and 2 fused, same bytes as the
+ * separate calls), so events 0 and 1 are recorded back to back.
  */
 typedef struct moe_ffn_desc {
   int64_t T;              /* tokens (rows of x and out)                 */

@@ -145,3 +145,49 @@ def test_ffn_prefill_contiguous_sampled_tokens(lib):
         tokens += list(rng.choice(np.nonzero(r["topk_ids"][:, 0] == e)[0], 3, replace=False))
     tokens = sorted(tokens)
     check_tol(got[tokens], _oracle_tokens("c3", wl, tokens), "c3 ffn tokens")
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3"])
+def test_ffn_equals_the_stage_entry_points(lib, name):
+    """moe_ffn fuses quantisation into the permute; its output must be bit-identical
+    to the public stage calls made one by one (quant, permute, GEMM1, SwiGLU+quant,
+    GEMM2, combine)."""
+    wl = build_workload(name)
+    cfg = wl["cfg"]
+    got, st = _gpu_ffn(lib, wl)
+    T, H, I, E, k = wl["T"], cfg.H, cfg.I, cfg.E, wl["k"]
+    dev = "cuda"
+    q = torch.empty((T, H), dtype=torch.uint8, device=dev)
+    Tp = (T + 3) // 4 * 4
+    s = torch.empty((H // 128, Tp), dtype=torch.float32, device=dev)
+    lib.moe_quant_fp8(wl["x"], q, s, Tp)
+    masked = wl["layout"] == lib.MOE_LAYOUT_MASKED
+    rows = E * cfg.max_m if masked else lib.moe_contig_rows_bound(T * k, E)
+    A1 = torch.empty((rows, H), dtype=torch.uint8, device=dev)
+    sA1 = torch.empty((E, H // 128, cfg.max_m) if masked else (H // 128, rows), dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    mi = torch.empty(rows, dtype=torch.int32, device=dev)
+    row_src = torch.empty(rows, dtype=torch.int32, device=dev)
+    dst = torch.empty(T * k, dtype=torch.int32, device=dev)
+    lib.moe_permute(q, s, wl["topk_ids"], wl["routing"]["expert_begin"], E, wl["layout"], cfg.max_m,
+                    A1, sA1, counts, offsets, mi, row_src, dst, rows_capacity=0 if masked else rows, s_ld=Tp)
+    Y1 = torch.empty((rows, 2 * I), dtype=torch.bfloat16, device=dev)
+    A2 = torch.empty((rows, I), dtype=torch.uint8, device=dev)
+    sA2 = torch.empty((E, I // 128, cfg.max_m) if masked else (I // 128, rows), dtype=torch.float32, device=dev)
+    Y2 = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+    if masked:
+        M = cfg.max_m
+        lib.moe_gemm_fp8_masked(A1.view(E, M, H), sA1, wl["w13"], wl["w13_s"], counts, Y1.view(E, M, 2 * I),
+                                expected_m=wl["expected_m"])
+        lib.moe_swiglu_quant(Y1, A2, sA2, counts=counts, max_m=M)
+        lib.moe_gemm_fp8_masked(A2.view(E, M, I), sA2, wl["w2"], wl["w2_s"], counts, Y2.view(E, M, H),
+                                expected_m=wl["expected_m"])
+    else:
+        lib.moe_gemm_fp8_contig(A1, sA1, wl["w13"], wl["w13_s"], offsets, mi, Y1)
+        lib.moe_swiglu_quant(Y1, A2, sA2, m_indices=mi, s_ld=rows)
+        lib.moe_gemm_fp8_contig(A2, sA2, wl["w2"], wl["w2_s"], offsets, mi, Y2)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    lib.moe_combine(Y2, dst, wl["topk_w"], out)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(out), got)
