@@ -84,16 +84,32 @@ def make_desc(wl, out, err=None, stage_events=None, x=None, ids=None, w=None):
                              gemm_flags=wl.get("gemm_flags", 0), err=err, stage_events=stage_events)
 
 
+def gemm1_variant(wl):
+    """The GEMM1 kernel moe_ffn runs for this workload."""
+    import fp8_grouped_expert_x128_gb300 as moe
+    if wl["layout"] == moe.MOE_LAYOUT_MASKED:
+        v = moe.moe_gemm_fp8_masked_variant(wl["cfg"].max_m, wl["expected_m"], wl.get("gemm_flags", 0))
+        if v != 0:
+            return f"gemm_fp8_weights_m_kernel<{v}>"
+    return "gemm_fp8_tokens_m_kernel<swiglu>"
+
+
+def gemm1_fused(wl):
+    return gemm1_variant(wl).endswith("<swiglu>")
+
+
 def algorithmic_counts(wl):
     """Algorithmic FLOPs and bytes per step and per GEMM1 launch."""
     cfg = wl["cfg"]
     H, I = cfg.H, cfg.I
     rows, act = wl["rows"], wl["active_experts"]
+    fused = gemm1_fused(wl)
     flops_g1 = 2.0 * rows * H * 2 * I
     flops_g2 = 2.0 * rows * I * H
     w13_bytes = act * (2 * I * H + 4 * (2 * I // 128) * (H // 128))
     w2_bytes = act * (H * I + 4 * (H // 128) * (I // 128))
-    g1_bytes = w13_bytes + rows * (H + 4 * H / 128) + rows * 2 * I * 2
+    g1_out = rows * (I + 4 * I / 128) if fused else rows * 2 * I * 2   # FP8 h + scales, or bf16 Y1
+    g1_bytes = w13_bytes + rows * (H + 4 * H / 128) + g1_out
     return dict(flops=flops_g1 + flops_g2, flops_g1=flops_g1, g1_bytes=g1_bytes,
                 weight_bytes=w13_bytes + w2_bytes)
 
@@ -285,6 +301,25 @@ def _sum_over_ranks(world, v):
     t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.SUM)
     return float(t.item())
+
+
+def recorded_traffic(kernel_label: str, workload: str):
+    """DRAM bytes (read + write) per launch of this kernel on this workload from
+    the ncu capture recorded in profiles/traffic.json, or None when there is no
+    capture or gemm.cu has changed since it was taken."""
+    import hashlib
+    path = os.path.join(HERE, "profiles", "traffic.json")
+    src = os.path.join(HERE, "fp8_grouped_expert_x128_gb300", "csrc", "gemm.cu")
+    if not os.path.exists(path):
+        return None
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    with open(path) as f:
+        rec = json.load(f)
+    r = rec.get(f"{kernel_label}@{workload}")
+    if not r or r.get("gemm_cu_sha256") != sha:
+        return None
+    return r["dram_read_bytes"] + r["dram_write_bytes"]
 
 
 def load_peaks():
@@ -495,12 +530,9 @@ def main():
         achieved = alg["flops_g1"] / g1_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": achieved / fp8_peak}
-    if wl["layout"] == moe.MOE_LAYOUT_MASKED:
-        v = moe.moe_gemm_fp8_masked_variant(cfg.max_m, wl["expected_m"], args.gemm_flags)
-        kname = "gemm_fp8_tokens_m_kernel" if v == 0 else f"gemm_fp8_weights_m_kernel<{v}>"
-    else:
-        kname = "gemm_fp8_tokens_m_kernel"
-    roof.update({"traffic": None, "kernel": f"{kname} (GEMM1, W13)",
+    kname = gemm1_variant(wl)
+    what = "GEMM1 (W13) + SwiGLU + FP8 requant" if gemm1_fused(wl) else "GEMM1 (W13)"
+    roof.update({"traffic": recorded_traffic(kname, args.workload), "kernel": f"{kname} ({what})",
                  "launch_ms": 1e3 * g1_s, "peak_source": f"{peak_src}" +
                  ("" if roof["bound"] == "hbm" else " bf16 burst x2 (nominal FP8:BF16)"),
                  "algorithmic": {"bytes": alg["g1_bytes"], "flops": alg["flops_g1"]}})
@@ -530,13 +562,13 @@ def main():
                        "launch": "eager moe_ffn" if graph is None else "moe_ffn captured once in a CUDA graph, replayed per step",
                        "parallelism": f"replicas x{world}"},
             "stage_ms": {n: round(v, 4) for n, v in zip(
-                ["quant (fused into permute)", "quant+permute", "gemm1", "swiglu_quant", "gemm2", "combine"], stage_ms)},
+                ["quant (fused into permute)", "quant+permute", "gemm1", "swiglu_quant (fused into gemm1 when 0)", "gemm2", "combine"], stage_ms)},
             "tflops": alg["flops"] / (ms_per_step / 1e3) / 1e12,
             "weight_gbs": alg["weight_bytes"] / (ms_per_step / 1e3) / 1e9,
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 6 * args.steps,
+            "gpu_launches": (5 if gemm1_fused(wl) else 6) * args.steps,
             "clocks": clk.summary(),
             "device_status": moe.moe_status_string(status),
             "wall_s_timed": t_wall,

@@ -44,6 +44,17 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
                    int32_t* offsets, int32_t* m_indices, int32_t* row_src, int32_t* dst_row,
                    int64_t rows_capacity, int32_t* err, cudaStream_t st);
 
+// GEMM1 with SwiGLU + 1x128 requantisation fused into the tokens-as-M
+// epilogue (bytes equal GEMM1 -> moe_swiglu_quant); used inside moe_ffn.
+int gemm_masked_swiglu(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                       const int32_t* counts, int32_t E, int32_t max_m, int32_t N, int32_t K,
+                       uint8_t* Q2, float* S2, int32_t flags, int32_t* err, cudaStream_t st);
+int gemm_contig_swiglu(const uint8_t* A, int64_t lda, const float* sA, int64_t sA_ld,
+                       const uint8_t* B, const float* sB, const int32_t* offsets,
+                       const int32_t* m_indices, int64_t M_capacity, int32_t E, int32_t N, int32_t K,
+                       uint8_t* Q2, float* S2, int64_t s2_ld, int32_t flags, int32_t* err,
+                       cudaStream_t st);
+
 // Encode a 2-D K-major uint8 tensor map with 128-byte swizzle:
 // global [rows, cols] (row stride ld bytes), box [box_rows, 128 bytes].
 int make_tmap_u8_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,

@@ -108,6 +108,10 @@ struct GemmArgs {
   int32_t* err;
   uint64_t wait_limit_ns;
   int32_t flags;
+  // fused SwiGLU + 1x128 requantisation (tokens-as-M kernel, kSwiGLU mode)
+  uint8_t* Q2;       // [rows, N/2] FP8
+  float* S2;         // grouped scales, group size S2_G
+  int64_t S2_G;
 };
 
 struct Sched {
@@ -165,6 +169,11 @@ __device__ void build_schedule(const GemmArgs& p, const Sched& s, int n_tiles) {
   }
 }
 
+// kSwiGLU: the 256-wide B tile is 128 gate rows + the matching 128 up rows
+// (two 128-row TMA boxes), and the epilogue turns the tile into h = silu(g)*u
+// quantised 1x128 (bytes equal GEMM1 -> bf16 -> moe_swiglu_quant), writing
+// FP8 + scales instead of bf16 D.
+template <bool kSwiGLU>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_tokens_m_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
@@ -174,17 +183,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* a_tiles = smem;
   uint8_t* b_tiles = smem + kStages * kATileBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 8);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int32_t* sched_mem = reinterpret_cast<int32_t*>(tmem_slot + 4);
   const Sched sched{sched_mem, sched_mem + p.E + 1, sched_mem + 2 * p.E + 1};
+  // SwiGLU mode: per-row amax of each warpgroup's 64 columns, [tile parity][g][row]
+  float* xch = reinterpret_cast<float*>(sched_mem + ((3 * p.E + 1 + 3) & ~3));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * kStages;
   const uint32_t tfull0 = empty0 + 8 * kStages;
   const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t xfull0 = tempty0 + 16;   // amax written (per tile parity)
+  const uint32_t xempty0 = xfull0 + 16;   // amax read
   const int n_tiles = (p.N + BN - 1) / BN;
+  const int I2 = p.N / 2;                 // SwiGLU mode: intermediate size
   const int KB = p.K / BK;
   const int NB = p.N / 128;
   volatile int* abort = abort_flag;
@@ -197,6 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8 * b, 1);
       mbar_init(tempty0 + 8 * b, kEpiWarps);
+      mbar_init(xfull0 + 8 * b, kEpiWarps);
+      mbar_init(xempty0 + 8 * b, kEpiWarps);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -229,7 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         cur.seek(sched, t);
         const int l = t - sched.tile0[cur.e];
         const int a_row = sched.rbase[cur.e] + (l / n_tiles) * BM;
-        const int b_row = cur.e * p.N + (l % n_tiles) * BN;
+        // plain: 256 consecutive weight rows; SwiGLU: gate rows then the up rows
+        // of the same 128 intermediate columns
+        const int b_row = kSwiGLU ? cur.e * p.N + (l % n_tiles) * 128 : cur.e * p.N + (l % n_tiles) * BN;
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const uint32_t s = it % kStages, ph = (it / kStages) & 1;
           if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, p.err, p.wait_limit_ns)) {
@@ -238,7 +256,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(full0 + 8 * s, kStageBytes);
           tma_load_2d(smem_u32(a_tiles + s * kATileBytes), &tmA, full0 + 8 * s, kb * BK, a_row);
-          tma_load_2d(smem_u32(b_tiles + s * kBTileBytes), &tmB, full0 + 8 * s, kb * BK, b_row);
+          if (kSwiGLU) {
+            tma_load_2d(smem_u32(b_tiles + s * kBTileBytes), &tmB, full0 + 8 * s, kb * BK, b_row);
+            tma_load_2d(smem_u32(b_tiles + s * kBTileBytes + 128 * BK), &tmB, full0 + 8 * s, kb * BK,
+                        b_row + I2);
+          } else {
+            tma_load_2d(smem_u32(b_tiles + s * kBTileBytes), &tmB, full0 + 8 * s, kb * BK, b_row);
+          }
         }
       }
       if (!ok) {
@@ -293,17 +317,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     regs_acquire_high();
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;                // TMEM lane quadrant of this warp
-    const int g = (warp - kEpiWarp0) >> 2;  // column half of the 256-wide tile
+    const int q = warp & 3;                 // TMEM lane quadrant of this warp
+    const int g = (warp - kEpiWarp0) >> 2;  // plain: column half; SwiGLU: intermediate half
     uint32_t acc_it = 0;
+    uint32_t tile_no = 0;
     TileCursor cur;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++tile_no) {
       cur.seek(sched, t);
       const int e = cur.e;
       const int l = t - sched.tile0[e];
       const int mt = l / n_tiles, nt = l % n_tiles;
-      const bool half = (nt == n_tiles - 1) && (p.N % BN) != 0;
+      const bool half = !kSwiGLU && (nt == n_tiles - 1) && (p.N % BN) != 0;
       const bool active = !(half && g == 1);
       const int r_local = mt * BM + q * 32 + lane;
       const int64_t gr = static_cast<int64_t>(sched.rbase[e]) + r_local;
@@ -312,9 +337,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n0 = nt * BN + g * 128;
       const int64_t grp = gr / p.sA_G, pos = gr - grp * p.sA_G;
       const float* sa_ptr = p.sA + grp * KB * p.sA_G + pos;
-      const float* sb_ptr = p.sB + (static_cast<int64_t>(e) * NB + (active ? n0 / 128 : 0)) * KB;
+      // plain: the weight block of this warp's 128 columns; SwiGLU: the gate
+      // block (sb_ptr) and the up block (sb2_ptr) of the tile's 128 columns
+      const float* sb_ptr = kSwiGLU ? p.sB + (static_cast<int64_t>(e) * NB + nt) * KB
+                                    : p.sB + (static_cast<int64_t>(e) * NB + (active ? n0 / 128 : 0)) * KB;
+      const float* sb2_ptr = p.sB + (static_cast<int64_t>(e) * NB + (kSwiGLU ? I2 / 128 + nt : 0)) * KB;
       // fp32 accumulators as pairs: the promotion runs as packed FMAs
-      // (two round-to-nearest fp32 FMAs per instruction, same bits as fmaf)
+      // (two round-to-nearest fp32 FMAs per instruction, same bits as fmaf).
+      // SwiGLU mode: acc[0..31] gate columns, acc[32..63] up columns.
       float2 acc[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.f, 0.f);
@@ -323,13 +353,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // k-blocks of work to hide behind, not one.
       auto load_sa = [&](int k) { return (row_ok && k < KB) ? __ldg(sa_ptr + static_cast<int64_t>(k) * p.sA_G) : 0.f; };
       auto load_sb = [&](int k) { return k < KB ? __ldg(sb_ptr + k) : 0.f; };
+      auto load_sb2 = [&](int k) { return (kSwiGLU && k < KB) ? __ldg(sb2_ptr + k) : 0.f; };
       float sa0 = load_sa(0), sa1 = load_sa(1), sa2 = load_sa(2), sa3 = load_sa(3);
       float sb0 = load_sb(0), sb1 = load_sb(1), sb2 = load_sb(2), sb3 = load_sb(3);
+      float su0 = load_sb2(0), su1 = load_sb2(1), su2 = load_sb2(2), su3 = load_sb2(3);
       for (int kb = 0; kb < KB; ++kb, ++acc_it) {
         const uint32_t b = acc_it & 1, tph = (acc_it >> 1) & 1;
         const float sc = sa0 * sb0;
+        const float scu = sa0 * su0;
         sa0 = sa1; sa1 = sa2; sa2 = sa3; sa3 = load_sa(kb + kScaleAhead);
         sb0 = sb1; sb1 = sb2; sb2 = sb3; sb3 = load_sb(kb + kScaleAhead);
+        if (kSwiGLU) { su0 = su1; su1 = su2; su2 = su3; su3 = load_sb2(kb + kScaleAhead); }
         // one lane waits, the warp follows it: tcgen05.ld is warp-collective
         int got = 1;
         if (lane == 0) got = mbar_wait_bounded(tfull0 + 8 * b, tph, abort, p.err, p.wait_limit_ns);
@@ -340,22 +374,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         if (active) {
-          const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + g * 128;
+          const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
           const float2 sc2 = make_float2(sc, sc);
+          if (kSwiGLU) {
+            const float2 scu2 = make_float2(scu, scu);
+            const uint32_t tg = tmem_base + lanes + b * BN + g * 64;        // gate columns
+            const uint32_t tu = tmem_base + lanes + b * BN + 128 + g * 64;  // up columns
 #pragma unroll
-          for (int c = 0; c < 8; c += 2) {   // two 16-column loads in flight
-            uint32_t r0[16], r1[16];
-            tmem_ld_32x32b_x16(tbase + c * 16, r0);
-            tmem_ld_32x32b_x16(tbase + (c + 1) * 16, r1);
-            tmem_ld_wait();
+            for (int c = 0; c < 4; ++c) {
+              uint32_t r0[16], r1[16];
+              tmem_ld_32x32b_x16(tg + c * 16, r0);
+              tmem_ld_32x32b_x16(tu + c * 16, r1);
+              tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              acc[c * 8 + i] = __ffma2_rn(sc2, make_float2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1])),
-                                          acc[c * 8 + i]);
+              for (int i = 0; i < 8; ++i)
+                acc[c * 8 + i] = __ffma2_rn(sc2, make_float2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1])),
+                                            acc[c * 8 + i]);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              acc[(c + 1) * 8 + i] = __ffma2_rn(
-                  sc2, make_float2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])), acc[(c + 1) * 8 + i]);
+              for (int i = 0; i < 8; ++i)
+                acc[32 + c * 8 + i] = __ffma2_rn(
+                    scu2, make_float2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])), acc[32 + c * 8 + i]);
+            }
+          } else {
+            const uint32_t tbase = tmem_base + lanes + b * BN + g * 128;
+#pragma unroll
+            for (int c = 0; c < 8; c += 2) {   // two 16-column loads in flight
+              uint32_t r0[16], r1[16];
+              tmem_ld_32x32b_x16(tbase + c * 16, r0);
+              tmem_ld_32x32b_x16(tbase + (c + 1) * 16, r1);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                acc[c * 8 + i] = __ffma2_rn(sc2, make_float2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1])),
+                                            acc[c * 8 + i]);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                acc[(c + 1) * 8 + i] = __ffma2_rn(
+                    sc2, make_float2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])), acc[(c + 1) * 8 + i]);
+            }
           }
         }
         tc_fence_before();
@@ -363,17 +419,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(tempty0 + 8 * b);
       }
       if (!ok) break;
-      if (active && row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(p.D + gr * p.ldd + n0);
+      if (!kSwiGLU) {
+        if (active && row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(p.D + gr * p.ldd + n0);
 #pragma unroll
-        for (int v = 0; v < 16; ++v) {
-          uint32_t o[4];
+          for (int v = 0; v < 16; ++v) {
+            uint32_t o[4];
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const __nv_bfloat162 bb = __floats2bfloat162_rn(acc[v * 4 + h].x, acc[v * 4 + h].y);
-            o[h] = *reinterpret_cast<const uint32_t*>(&bb);
+            for (int h = 0; h < 4; ++h) {
+              const __nv_bfloat162 bb = __floats2bfloat162_rn(acc[v * 4 + h].x, acc[v * 4 + h].y);
+              o[h] = *reinterpret_cast<const uint32_t*>(&bb);
+            }
+            dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
           }
-          dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      } else {
+        // h = silu(g) * u from the bf16-rounded GEMM1 values (what the bf16 Y1
+        // would hold), same formula as moe_swiglu_quant; h overwrites acc[0..31].
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float g0 = __bfloat162float(__float2bfloat16_rn(acc[i].x));
+          const float g1 = __bfloat162float(__float2bfloat16_rn(acc[i].y));
+          const float u0 = __bfloat162float(__float2bfloat16_rn(acc[32 + i].x));
+          const float u1 = __bfloat162float(__float2bfloat16_rn(acc[32 + i].y));
+          acc[i].x = __fdiv_rn(g0, 1.0f + expf(-g0)) * u0;
+          acc[i].y = __fdiv_rn(g1, 1.0f + expf(-g1)) * u1;
+          amax = fmaxf(amax, fmaxf(fabsf(acc[i].x), fabsf(acc[i].y)));
+        }
+        // the 1x128 block spans both warpgroups: swap the half-row amax with the
+        // partner warp (same rows, other 64 columns) through shared memory,
+        // ordered by a written/read mbarrier pair per tile parity (bounded waits)
+        const uint32_t par = tile_no & 1, xph = (tile_no >> 1) & 1;
+        int okx = 1;
+        if (lane == 0) okx = mbar_wait_bounded(xempty0 + 8 * par, xph ^ 1, abort, p.err, p.wait_limit_ns);
+        okx = __shfl_sync(0xffffffffu, okx, 0);
+        if (!okx) {
+          ok = false;
+          break;
+        }
+        float* x = xch + par * 256;
+        x[g * 128 + q * 32 + lane] = amax;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xfull0 + 8 * par);
+        if (lane == 0) okx = mbar_wait_bounded(xfull0 + 8 * par, xph, abort, p.err, p.wait_limit_ns);
+        okx = __shfl_sync(0xffffffffu, okx, 0);
+        if (!okx) {
+          ok = false;
+          break;
+        }
+        amax = fmaxf(amax, x[(1 - g) * 128 + q * 32 + lane]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xempty0 + 8 * par);
+        if (row_ok) {
+          const float sc = block_scale(amax);
+          uint2 qv[8];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const float f[8] = {acc[4 * v].x, acc[4 * v].y, acc[4 * v + 1].x, acc[4 * v + 1].y,
+                                acc[4 * v + 2].x, acc[4 * v + 2].y, acc[4 * v + 3].x, acc[4 * v + 3].y};
+            qv[v] = quant8(f, sc);
+          }
+          uint4* dq = reinterpret_cast<uint4*>(p.Q2 + gr * I2 + nt * 128 + g * 64);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dq[v] = make_uint4(qv[2 * v].x, qv[2 * v].y, qv[2 * v + 1].x, qv[2 * v + 1].y);
+          if (g == 0) {
+            const int64_t grp2 = gr / p.S2_G, pos2 = gr - grp2 * p.S2_G;
+            p.S2[(grp2 * (I2 / 128) + nt) * p.S2_G + pos2] = sc;
+          }
         }
       }
     }
@@ -388,23 +501,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 size_t tokens_m_smem_bytes(int E) {
-  return 1024 + static_cast<size_t>(kStages) * kStageBytes + (2 * kStages + 4) * 8 + 16 +
-         sizeof(int32_t) * (3 * E + 1);
+  return 1024 + static_cast<size_t>(kStages) * kStageBytes + (2 * kStages + 8) * 8 + 16 +
+         sizeof(int32_t) * (3 * E + 1 + 3) + sizeof(float) * 2 * 256;
 }
 
 int launch_tokens_m(const uint8_t* A, int64_t a_rows, int64_t lda, const uint8_t* B,
-                    int64_t tiles_upper, GemmArgs& args, cudaStream_t stream) {
+                    int64_t tiles_upper, GemmArgs& args, cudaStream_t stream, bool swiglu = false) {
   CUtensorMap tmA, tmB;
   if (int st = make_tmap_u8_sw128(&tmA, A, a_rows, args.K, lda, BM)) return st;
-  if (int st = make_tmap_u8_sw128(&tmB, B, static_cast<uint64_t>(args.E) * args.N, args.K, args.K, BN))
+  if (int st = make_tmap_u8_sw128(&tmB, B, static_cast<uint64_t>(args.E) * args.N, args.K, args.K,
+                                  swiglu ? 128 : BN))
     return st;
   const size_t smem = tokens_m_smem_bytes(args.E);
-  if (int st = prepare_kernel(gemm_fp8_tokens_m_kernel, smem, true)) return st;
   if (args.wait_limit_ns == 0) args.wait_limit_ns = kWaitLimitNs;
   int64_t grid = num_sms();
   if (tiles_upper < grid) grid = tiles_upper;
   if (grid < 1) grid = 1;
-  gemm_fp8_tokens_m_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, args);
+  if (swiglu) {
+    if (int st = prepare_kernel(gemm_fp8_tokens_m_kernel<true>, smem, true)) return st;
+    gemm_fp8_tokens_m_kernel<true><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, args);
+  } else {
+    if (int st = prepare_kernel(gemm_fp8_tokens_m_kernel<false>, smem, true)) return st;
+    gemm_fp8_tokens_m_kernel<false><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, args);
+  }
   return launch_status();
 }
 
@@ -739,6 +858,66 @@ int launch_weights_m(const uint8_t* A, const uint8_t* B, GemmArgs& args, cudaStr
 }
 
 }  // namespace
+
+// GEMM1 with SwiGLU + 1x128 requantisation fused into the epilogue (used by
+// moe_ffn when the tokens-as-M kernel serves the layout).  Outputs: FP8
+// Q2 [rows, N/2] (row stride N/2) and fp32 scales S2 in groups of S2_G rows.
+int gemm_masked_swiglu(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                       const int32_t* counts, int32_t E, int32_t max_m, int32_t N, int32_t K,
+                       uint8_t* Q2, float* S2, int32_t flags, int32_t* err, cudaStream_t st) {
+  MOE_CHECK_ARG(E >= 1 && E <= kMaxExperts && N > 0 && N % 256 == 0 && K > 0 && K % 128 == 0);
+  MOE_CHECK_ARG(max_m > 0 && static_cast<int64_t>(E) * max_m < (1ll << 31));
+  MOE_CHECK_ARG(A && sA && B && sB && counts && Q2 && S2 && aligned16(A) && aligned16(B) && aligned16(Q2));
+  if (int rc = check_device()) return rc;
+  GemmArgs a{};
+  a.sA = sA;
+  a.sA_G = max_m;
+  a.sB = sB;
+  a.counts = counts;
+  a.E = E;
+  a.N = N;
+  a.K = K;
+  a.max_m = max_m;
+  a.layout = MOE_LAYOUT_MASKED;
+  a.err = err;
+  a.flags = flags & ~MOE_GEMM_DEBUG_STALL;
+  a.Q2 = Q2;
+  a.S2 = S2;
+  a.S2_G = max_m;
+  const int64_t tiles = static_cast<int64_t>(E) * ((max_m + BM - 1) / BM) * (N / BN);
+  return launch_tokens_m(A, static_cast<int64_t>(E) * max_m, K, B, tiles, a, st, true);
+}
+
+int gemm_contig_swiglu(const uint8_t* A, int64_t lda, const float* sA, int64_t sA_ld,
+                       const uint8_t* B, const float* sB, const int32_t* offsets,
+                       const int32_t* m_indices, int64_t M_capacity, int32_t E, int32_t N, int32_t K,
+                       uint8_t* Q2, float* S2, int64_t s2_ld, int32_t flags, int32_t* err,
+                       cudaStream_t st) {
+  MOE_CHECK_ARG(E >= 1 && E <= kMaxExperts && N > 0 && N % 256 == 0 && K > 0 && K % 128 == 0);
+  MOE_CHECK_ARG(M_capacity > 0 && M_capacity % BM == 0 && M_capacity < (1ll << 31));
+  MOE_CHECK_ARG(A && sA && B && sB && offsets && m_indices && Q2 && S2);
+  MOE_CHECK_ARG(aligned16(A) && aligned16(B) && aligned16(Q2) && lda % 16 == 0 && sA_ld >= M_capacity &&
+                s2_ld >= M_capacity);
+  if (int rc = check_device()) return rc;
+  GemmArgs a{};
+  a.sA = sA;
+  a.sA_G = sA_ld;
+  a.sB = sB;
+  a.offsets = offsets;
+  a.m_indices = m_indices;
+  a.E = E;
+  a.N = N;
+  a.K = K;
+  a.layout = MOE_LAYOUT_CONTIG;
+  a.err = err;
+  a.flags = flags & ~MOE_GEMM_DEBUG_STALL;
+  a.Q2 = Q2;
+  a.S2 = S2;
+  a.S2_G = s2_ld;
+  const int64_t tiles = (M_capacity / BM) * (N / BN);
+  return launch_tokens_m(A, M_capacity, lda, B, tiles, a, st, true);
+}
+
 }  // namespace moe
 
 using namespace moe;
