@@ -158,37 +158,50 @@ __global__ void __launch_bounds__(128) permute_scatter_kernel(
   for (int64_t kb = lane; kb < KB; kb += 32) s_out[(grp * KB + kb) * G + pos] = __ldg(s + kb * s_ld + t);
 }
 
-// Fused 1x128 quantisation + scatter for moe_ffn: one warp per routed row
-// quantises the token's bf16 row straight into its expert slot (the bytes equal
-// moe_quant_fp8 followed by moe_permute: same helpers, same arithmetic).
-__global__ void __launch_bounds__(128) quant_scatter_kernel(
+// Fused 1x128 quantisation + scatter for moe_ffn: one CTA per routed row; its
+// kQsWarps warps share the row's 128-column block pairs (a half-warp per
+// block), loads issued before use, and quantise the token's bf16 row straight
+// into its expert slot (the bytes equal moe_quant_fp8 followed by moe_permute:
+// same helpers, same arithmetic).  Non-local assignments leave at once.
+constexpr int kQsWarps = 8;
+constexpr int kQsPairs = 4;  // block pairs per warp per pass (H up to 8192 in one pass)
+
+__global__ void __launch_bounds__(32 * kQsWarps) quant_scatter_kernel(
     const uint16_t* __restrict__ x, int64_t ldx, const int32_t* __restrict__ dst_row,
     int64_t n_assign, int32_t k, int64_t H, uint8_t* __restrict__ q_out, float* __restrict__ s_out,
     int64_t G) {
-  const int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+  const int64_t i = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (i >= n_assign) return;
   const int32_t dst = __ldg(dst_row + i);
   if (dst < 0) return;
   const int64_t t = i / k;
-  const int64_t KB = H / 128;
+  const int64_t KB = H / 128, NP = (KB + 1) / 2;
   const int64_t grp = dst / G, pos = dst - grp * G;
   const uint16_t* xr = x + t * ldx;
   uint8_t* qr = q_out + static_cast<int64_t>(dst) * H;
-  for (int64_t kb0 = 0; kb0 < KB; kb0 += 2) {
-    const int64_t kb = kb0 + (lane >> 4);
-    const bool active = kb < KB;
-    const int64_t col = kb * 128 + (lane & 15) * 8;
-    float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (active) unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(xr + col)), f);
-    float amax = 0.f;
+  for (int64_t p0 = warp; p0 < NP; p0 += static_cast<int64_t>(kQsWarps) * kQsPairs) {
+    uint4 u[kQsPairs];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
-    amax = half_warp_max(amax);
-    if (active) {
-      const float sc = block_scale(amax);
-      *reinterpret_cast<uint2*>(qr + col) = quant8(f, sc);
-      if ((lane & 15) == 0) s_out[(grp * KB + kb) * G + pos] = sc;
+    for (int j = 0; j < kQsPairs; ++j) {
+      const int64_t kb = (p0 + j * kQsWarps) * 2 + (lane >> 4);
+      u[j] = kb < KB ? __ldg(reinterpret_cast<const uint4*>(xr + kb * 128 + (lane & 15) * 8))
+                     : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < kQsPairs; ++j) {
+      const int64_t kb = (p0 + j * kQsWarps) * 2 + (lane >> 4);
+      float f[8];
+      unpack_bf16x8(u[j], f);
+      float amax = 0.f;
+#pragma unroll
+      for (int v = 0; v < 8; ++v) amax = fmaxf(amax, fabsf(f[v]));
+      amax = half_warp_max(amax);
+      if (kb < KB) {
+        const float sc = block_scale(amax);
+        *reinterpret_cast<uint2*>(qr + kb * 128 + (lane & 15) * 8) = quant8(f, sc);
+        if ((lane & 15) == 0) s_out[(grp * KB + kb) * G + pos] = sc;
+      }
     }
   }
 }
@@ -333,7 +346,8 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
   const int64_t n = T * k;
   const unsigned grid = static_cast<unsigned>((n + 3) / 4);
   if (x != nullptr)
-    quant_scatter_kernel<<<grid, 128, 0, st>>>(x, ldx, dst_row, n, k, H, q_out, s_out, G);
+    quant_scatter_kernel<<<static_cast<unsigned>(n), 32 * kQsWarps, 0, st>>>(x, ldx, dst_row, n, k, H,
+                                                                          q_out, s_out, G);
   else
     permute_scatter_kernel<<<grid, 128, 0, st>>>(q, s, s_ld, dst_row, n, k, H, q_out, s_out, G);
   return launch_status();
