@@ -91,7 +91,9 @@ def gemm1_variant(wl):
         v = moe.moe_gemm_fp8_masked_variant(wl["cfg"].max_m, wl["expected_m"], wl.get("gemm_flags", 0))
         if v != 0:
             return f"gemm_fp8_weights_m_kernel<{v}>"
-    return "gemm_fp8_tokens_m_kernel<swiglu>"
+    if wl.get("gemm_flags", 0) & moe.MOE_FFN_FUSE_SWIGLU:
+        return "gemm_fp8_tokens_m_kernel<swiglu>"
+    return "gemm_fp8_tokens_m_kernel"
 
 
 def gemm1_fused(wl):

@@ -219,37 +219,44 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
                            offsets, mind, rowsrc, dst, p.rows, d->err, st)))
     return rc;
   if ((rc = mark(2))) return rc;
-  // stages 3+4: where the tokens-as-M kernel serves GEMM1, SwiGLU and the FP8
-  // requantisation run in its epilogue (no bf16 Y1 round trip); the
-  // weights-as-M decode kernel keeps the separate SwiGLU kernel.
+  // stages 3+4: on request (MOE_FFN_FUSE_SWIGLU) and where the tokens-as-M
+  // kernel serves GEMM1, SwiGLU and the FP8 requantisation run in its
+  // epilogue (no bf16 Y1 round trip); otherwise GEMM1 writes Y1 and the
+  // SwiGLU kernel requantises it.
+  const int32_t gflags = d->gemm_flags & ~MOE_FFN_FUSE_SWIGLU;
   const bool fuse_swiglu =
-      !masked || moe_gemm_fp8_masked_variant(d->max_m, d->expected_m, d->gemm_flags) == 0;
+      (d->gemm_flags & MOE_FFN_FUSE_SWIGLU) &&
+      (!masked || moe_gemm_fp8_masked_variant(d->max_m, d->expected_m, d->gemm_flags) == 0);
   if (fuse_swiglu) {
     if (masked)
       rc = gemm_masked_swiglu(a1, sa1, d->w13, d->w13_s, counts, d->E, d->max_m, 2 * d->I, d->H,
-                              a2, sa2, d->gemm_flags, d->err, st);
+                              a2, sa2, gflags, d->err, st);
     else
       rc = gemm_contig_swiglu(a1, d->H, sa1, p.s_ld1, d->w13, d->w13_s, offsets, mind, p.rows, d->E,
-                              2 * d->I, d->H, a2, sa2, p.s_ld2, d->gemm_flags, d->err, st);
+                              2 * d->I, d->H, a2, sa2, p.s_ld2, gflags, d->err, st);
     if (rc) return rc;
     if ((rc = mark(3))) return rc;
     if ((rc = mark(4))) return rc;
   } else {
-    rc = moe_gemm_fp8_masked(a1, sa1, d->w13, d->w13_s, counts, d->E, d->max_m, 2 * d->I, d->H,
-                             d->expected_m, y1, d->gemm_flags, d->err, stream);
+    if (masked)
+      rc = moe_gemm_fp8_masked(a1, sa1, d->w13, d->w13_s, counts, d->E, d->max_m, 2 * d->I, d->H,
+                               d->expected_m, y1, gflags, d->err, stream);
+    else
+      rc = moe_gemm_fp8_contig(a1, d->H, sa1, p.s_ld1, d->w13, d->w13_s, offsets, mind, p.rows, d->E,
+                               2 * d->I, d->H, y1, 2 * d->I, gflags, d->err, stream);
     if (rc) return rc;
     if ((rc = mark(3))) return rc;
-    if ((rc = moe_swiglu_quant(y1, p.rows, d->I, counts, d->max_m, nullptr, a2, sa2, p.s_ld2,
-                               d->err, stream)))
+    if ((rc = moe_swiglu_quant(y1, p.rows, d->I, masked ? counts : nullptr, masked ? d->max_m : 0,
+                               masked ? nullptr : mind, a2, sa2, p.s_ld2, d->err, stream)))
       return rc;
     if ((rc = mark(4))) return rc;
   }
   if (masked)
     rc = moe_gemm_fp8_masked(a2, sa2, d->w2, d->w2_s, counts, d->E, d->max_m, d->H, d->I,
-                             d->expected_m, y2, d->gemm_flags, d->err, stream);
+                             d->expected_m, y2, gflags, d->err, stream);
   else
     rc = moe_gemm_fp8_contig(a2, d->I, sa2, p.s_ld2, d->w2, d->w2_s, offsets, mind, p.rows, d->E,
-                             d->H, d->I, y2, d->H, d->gemm_flags, d->err, stream);
+                             d->H, d->I, y2, d->H, gflags, d->err, stream);
   if (rc) return rc;
   if ((rc = mark(5))) return rc;
   if ((rc = moe_combine(y2, d->H, p.rows, dst, d->topk_w, d->T, d->k, d->H, d->out, d->H, d->err,

@@ -54,33 +54,18 @@ constexpr int kRegsHigh = 232;
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kLaunchRegs, "register split");
 static_assert(kThreads * kLaunchRegs <= 65536, "register file");
 
-template <int N = kRegsLow>
 __device__ __forceinline__ void regs_release_low() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
 }
-template <int N = kRegsHigh>
 __device__ __forceinline__ void regs_acquire_high() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
 }
-
-// The tokens-as-M kernel drains each 256-column TMEM buffer with 16 epilogue
-// warps (4 per TMEM lane quadrant, 64 columns each), halving the per-k-block
-// drain latency that gates its MMA; 640 threads launch with 96 registers,
-// warpgroup 0 keeps 32 and the four epilogue warpgroups take 112:
-// 128 * 32 + 512 * 112 = 61440 = 640 * 96.
-constexpr int kTokEpiWarps = 16;
-constexpr int kTokThreads = 32 * (kEpiWarp0 + kTokEpiWarps);
-constexpr int kTokLaunchRegs = 96;
-constexpr int kTokRegsLow = 32;
-constexpr int kTokRegsHigh = 112;
-static_assert(128 * kTokRegsLow + 512 * kTokRegsHigh <= kTokThreads * kTokLaunchRegs, "register split");
-static_assert(kTokThreads * kTokLaunchRegs <= 65536, "register file");
 
 // Per-device, per-kernel launch set-up done once: the dynamic shared-memory
 // opt-in and, for kernels that split registers, the check that the launch
 // register count equals kLaunchRegs.  Keyed by (device, kernel address).
 template <typename F>
-int prepare_kernel(F kernel, size_t smem, bool split_regs, int launch_regs = kLaunchRegs) {
+int prepare_kernel(F kernel, size_t smem, bool split_regs) {
   static std::mutex mu;
   static std::map<std::pair<int, const void*>, size_t> prepared;  // -> smem opted in
   int dev = 0;
@@ -92,7 +77,7 @@ int prepare_kernel(F kernel, size_t smem, bool split_regs, int launch_regs = kLa
     if (split_regs) {
       cudaFuncAttributes attr;
       if (cudaFuncGetAttributes(&attr, kernel) != cudaSuccess) return MOE_ERR_CUDA;
-      if (attr.numRegs != launch_regs) return MOE_ERR_UNSUPPORTED;
+      if (attr.numRegs != kLaunchRegs) return MOE_ERR_UNSUPPORTED;
     }
     it = prepared.emplace(key, 0).first;
   }
@@ -189,7 +174,7 @@ __device__ void build_schedule(const GemmArgs& p, const Sched& s, int n_tiles) {
 // quantised 1x128 (bytes equal GEMM1 -> bf16 -> moe_swiglu_quant), writing
 // FP8 + scales instead of bf16 D.
 template <bool kSwiGLU>
-__global__ void __launch_bounds__(kTokThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_tokens_m_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
@@ -203,7 +188,7 @@ __global__ void __launch_bounds__(kTokThreads, 1)
   int32_t* sched_mem = reinterpret_cast<int32_t*>(tmem_slot + 4);
   const Sched sched{sched_mem, sched_mem + p.E + 1, sched_mem + 2 * p.E + 1};
   // SwiGLU mode: per-row amax of each warpgroup's 64 columns, [tile parity][g][row]
-  float* xch = reinterpret_cast<float*>(sched_mem + ((3 * p.E + 1 + 3) & ~3));  // [2][4][128]
+  float* xch = reinterpret_cast<float*>(sched_mem + ((3 * p.E + 1 + 3) & ~3));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars);
@@ -225,9 +210,9 @@ __global__ void __launch_bounds__(kTokThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8 * b, 1);
-      mbar_init(tempty0 + 8 * b, kTokEpiWarps);
-      mbar_init(xfull0 + 8 * b, kTokEpiWarps);
-      mbar_init(xempty0 + 8 * b, kTokEpiWarps);
+      mbar_init(tempty0 + 8 * b, kEpiWarps);
+      mbar_init(xfull0 + 8 * b, kEpiWarps);
+      mbar_init(xempty0 + 8 * b, kEpiWarps);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -249,7 +234,7 @@ __global__ void __launch_bounds__(kTokThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int total = sched.tile0[p.E];
   if (warp < kEpiWarp0) {
-    regs_release_low<kTokRegsLow>();
+    regs_release_low();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && !(p.flags & MOE_GEMM_DEBUG_STALL)) {
@@ -330,12 +315,10 @@ __global__ void __launch_bounds__(kTokThreads, 1)
     }
   }
   } else {
-    regs_acquire_high<kTokRegsHigh>();
+    regs_acquire_high();
     // ------------------------------------------------------------ epilogue
-    // 16 warps: q = TMEM lane quadrant, cg = 64-column group of the 256-wide
-    // tile (SwiGLU mode: 32 gate + the same 32 up columns)
-    const int q = warp & 3;
-    const int cg = (warp - kEpiWarp0) >> 2;
+    const int q = warp & 3;                 // TMEM lane quadrant of this warp
+    const int g = (warp - kEpiWarp0) >> 2;  // plain: column half; SwiGLU: intermediate half
     uint32_t acc_it = 0;
     uint32_t tile_no = 0;
     TileCursor cur;
@@ -346,25 +329,25 @@ __global__ void __launch_bounds__(kTokThreads, 1)
       const int l = t - sched.tile0[e];
       const int mt = l / n_tiles, nt = l % n_tiles;
       const bool half = !kSwiGLU && (nt == n_tiles - 1) && (p.N % BN) != 0;
-      const bool active = !(half && cg >= 2);
+      const bool active = !(half && g == 1);
       const int r_local = mt * BM + q * 32 + lane;
       const int64_t gr = static_cast<int64_t>(sched.rbase[e]) + r_local;
       bool row_ok = r_local < sched.rext[e];
       if (row_ok && p.layout == MOE_LAYOUT_CONTIG) row_ok = __ldg(p.m_indices + gr) >= 0;
-      const int n0 = nt * BN + cg * 64;
+      const int n0 = nt * BN + g * 128;
       const int64_t grp = gr / p.sA_G, pos = gr - grp * p.sA_G;
       const float* sa_ptr = p.sA + grp * KB * p.sA_G + pos;
-      // plain: the weight block of this warp's 64 columns; SwiGLU: the gate
+      // plain: the weight block of this warp's 128 columns; SwiGLU: the gate
       // block (sb_ptr) and the up block (sb2_ptr) of the tile's 128 columns
       const float* sb_ptr = kSwiGLU ? p.sB + (static_cast<int64_t>(e) * NB + nt) * KB
                                     : p.sB + (static_cast<int64_t>(e) * NB + (active ? n0 / 128 : 0)) * KB;
       const float* sb2_ptr = p.sB + (static_cast<int64_t>(e) * NB + (kSwiGLU ? I2 / 128 + nt : 0)) * KB;
       // fp32 accumulators as pairs: the promotion runs as packed FMAs
       // (two round-to-nearest fp32 FMAs per instruction, same bits as fmaf).
-      // SwiGLU mode: acc[0..15] gate columns, acc[16..31] up columns.
-      float2 acc[32];
+      // SwiGLU mode: acc[0..31] gate columns, acc[32..63] up columns.
+      float2 acc[64];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.f, 0.f);
+      for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.f, 0.f);
       // The scales run kScaleAhead k-blocks ahead of their use in a register
       // ring (rotated, so every index is static): a global load has several
       // k-blocks of work to hide behind, not one.
@@ -392,20 +375,43 @@ __global__ void __launch_bounds__(kTokThreads, 1)
         tc_fence_after();
         if (active) {
           const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
+          const float2 sc2 = make_float2(sc, sc);
+          if (kSwiGLU) {
+            const float2 scu2 = make_float2(scu, scu);
+            const uint32_t tg = tmem_base + lanes + b * BN + g * 64;        // gate columns
+            const uint32_t tu = tmem_base + lanes + b * BN + 128 + g * 64;  // up columns
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            // plain: columns cg*64 + 16c; SwiGLU: gate cg*32 + 16c (c < 2), up 128 + cg*32 + 16(c-2)
-            const uint32_t col = kSwiGLU ? (c < 2 ? cg * 32 + c * 16 : 128 + cg * 32 + (c - 2) * 16)
-                                         : cg * 64 + c * 16;
-            const float s_c = (kSwiGLU && c >= 2) ? scu : sc;
-            const float2 s2 = make_float2(s_c, s_c);
-            uint32_t r[16];
-            tmem_ld_32x32b_x16(tmem_base + lanes + b * BN + col, r);
-            tmem_ld_wait();
+            for (int c = 0; c < 4; ++c) {
+              uint32_t r0[16], r1[16];
+              tmem_ld_32x32b_x16(tg + c * 16, r0);
+              tmem_ld_32x32b_x16(tu + c * 16, r1);
+              tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              acc[c * 8 + i] = __ffma2_rn(s2, make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
-                                          acc[c * 8 + i]);
+              for (int i = 0; i < 8; ++i)
+                acc[c * 8 + i] = __ffma2_rn(sc2, make_float2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1])),
+                                            acc[c * 8 + i]);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                acc[32 + c * 8 + i] = __ffma2_rn(
+                    scu2, make_float2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])), acc[32 + c * 8 + i]);
+            }
+          } else {
+            const uint32_t tbase = tmem_base + lanes + b * BN + g * 128;
+#pragma unroll
+            for (int c = 0; c < 8; c += 2) {   // two 16-column loads in flight
+              uint32_t r0[16], r1[16];
+              tmem_ld_32x32b_x16(tbase + c * 16, r0);
+              tmem_ld_32x32b_x16(tbase + (c + 1) * 16, r1);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                acc[c * 8 + i] = __ffma2_rn(sc2, make_float2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1])),
+                                            acc[c * 8 + i]);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                acc[(c + 1) * 8 + i] = __ffma2_rn(
+                    sc2, make_float2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])), acc[(c + 1) * 8 + i]);
+            }
           }
         }
         tc_fence_before();
@@ -417,7 +423,7 @@ __global__ void __launch_bounds__(kTokThreads, 1)
         if (active && row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(p.D + gr * p.ldd + n0);
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
+          for (int v = 0; v < 16; ++v) {
             uint32_t o[4];
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
@@ -429,21 +435,21 @@ __global__ void __launch_bounds__(kTokThreads, 1)
         }
       } else {
         // h = silu(g) * u from the bf16-rounded GEMM1 values (what the bf16 Y1
-        // would hold), same formula as moe_swiglu_quant; h overwrites acc[0..15].
+        // would hold), same formula as moe_swiglu_quant; h overwrites acc[0..31].
         float amax = 0.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 32; ++i) {
           const float g0 = __bfloat162float(__float2bfloat16_rn(acc[i].x));
           const float g1 = __bfloat162float(__float2bfloat16_rn(acc[i].y));
-          const float u0 = __bfloat162float(__float2bfloat16_rn(acc[16 + i].x));
-          const float u1 = __bfloat162float(__float2bfloat16_rn(acc[16 + i].y));
+          const float u0 = __bfloat162float(__float2bfloat16_rn(acc[32 + i].x));
+          const float u1 = __bfloat162float(__float2bfloat16_rn(acc[32 + i].y));
           acc[i].x = __fdiv_rn(g0, 1.0f + expf(-g0)) * u0;
           acc[i].y = __fdiv_rn(g1, 1.0f + expf(-g1)) * u1;
           amax = fmaxf(amax, fmaxf(fabsf(acc[i].x), fabsf(acc[i].y)));
         }
-        // the 1x128 block spans the four column groups: swap the partial amax of
-        // each row through shared memory, ordered by a written/read mbarrier
-        // pair per tile parity (bounded waits, like every pipeline wait)
+        // the 1x128 block spans both warpgroups: swap the half-row amax with the
+        // partner warp (same rows, other 64 columns) through shared memory,
+        // ordered by a written/read mbarrier pair per tile parity (bounded waits)
         const uint32_t par = tile_no & 1, xph = (tile_no >> 1) & 1;
         int okx = 1;
         if (lane == 0) okx = mbar_wait_bounded(xempty0 + 8 * par, xph ^ 1, abort, p.err, p.wait_limit_ns);
@@ -452,8 +458,8 @@ __global__ void __launch_bounds__(kTokThreads, 1)
           ok = false;
           break;
         }
-        float* x = xch + par * 512;
-        x[cg * 128 + q * 32 + lane] = amax;
+        float* x = xch + par * 256;
+        x[g * 128 + q * 32 + lane] = amax;
         __syncwarp();
         if (lane == 0) mbar_arrive(xfull0 + 8 * par);
         if (lane == 0) okx = mbar_wait_bounded(xfull0 + 8 * par, xph, abort, p.err, p.wait_limit_ns);
@@ -462,23 +468,22 @@ __global__ void __launch_bounds__(kTokThreads, 1)
           ok = false;
           break;
         }
-#pragma unroll
-        for (int o = 0; o < 4; ++o) amax = fmaxf(amax, x[o * 128 + q * 32 + lane]);
+        amax = fmaxf(amax, x[(1 - g) * 128 + q * 32 + lane]);
         __syncwarp();
         if (lane == 0) mbar_arrive(xempty0 + 8 * par);
         if (row_ok) {
           const float sc = block_scale(amax);
-          uint2 qv[4];
+          uint2 qv[8];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
+          for (int v = 0; v < 8; ++v) {
             const float f[8] = {acc[4 * v].x, acc[4 * v].y, acc[4 * v + 1].x, acc[4 * v + 1].y,
                                 acc[4 * v + 2].x, acc[4 * v + 2].y, acc[4 * v + 3].x, acc[4 * v + 3].y};
             qv[v] = quant8(f, sc);
           }
-          uint4* dq = reinterpret_cast<uint4*>(p.Q2 + gr * I2 + nt * 128 + cg * 32);
-          dq[0] = make_uint4(qv[0].x, qv[0].y, qv[1].x, qv[1].y);
-          dq[1] = make_uint4(qv[2].x, qv[2].y, qv[3].x, qv[3].y);
-          if (cg == 0) {
+          uint4* dq = reinterpret_cast<uint4*>(p.Q2 + gr * I2 + nt * 128 + g * 64);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dq[v] = make_uint4(qv[2 * v].x, qv[2 * v].y, qv[2 * v + 1].x, qv[2 * v + 1].y);
+          if (g == 0) {
             const int64_t grp2 = gr / p.S2_G, pos2 = gr - grp2 * p.S2_G;
             p.S2[(grp2 * (I2 / 128) + nt) * p.S2_G + pos2] = sc;
           }
@@ -497,7 +502,7 @@ __global__ void __launch_bounds__(kTokThreads, 1)
 
 size_t tokens_m_smem_bytes(int E) {
   return 1024 + static_cast<size_t>(kStages) * kStageBytes + (2 * kStages + 8) * 8 + 16 +
-         sizeof(int32_t) * (3 * E + 1 + 3) + sizeof(float) * 2 * 512;
+         sizeof(int32_t) * (3 * E + 1 + 3) + sizeof(float) * 2 * 256;
 }
 
 int launch_tokens_m(const uint8_t* A, int64_t a_rows, int64_t lda, const uint8_t* B,
@@ -513,11 +518,11 @@ int launch_tokens_m(const uint8_t* A, int64_t a_rows, int64_t lda, const uint8_t
   if (tiles_upper < grid) grid = tiles_upper;
   if (grid < 1) grid = 1;
   if (swiglu) {
-    if (int st = prepare_kernel(gemm_fp8_tokens_m_kernel<true>, smem, true, kTokLaunchRegs)) return st;
-    gemm_fp8_tokens_m_kernel<true><<<static_cast<unsigned>(grid), kTokThreads, smem, stream>>>(tmA, tmB, args);
+    if (int st = prepare_kernel(gemm_fp8_tokens_m_kernel<true>, smem, true)) return st;
+    gemm_fp8_tokens_m_kernel<true><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, args);
   } else {
-    if (int st = prepare_kernel(gemm_fp8_tokens_m_kernel<false>, smem, true, kTokLaunchRegs)) return st;
-    gemm_fp8_tokens_m_kernel<false><<<static_cast<unsigned>(grid), kTokThreads, smem, stream>>>(tmA, tmB, args);
+    if (int st = prepare_kernel(gemm_fp8_tokens_m_kernel<false>, smem, true)) return st;
+    gemm_fp8_tokens_m_kernel<false><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, args);
   }
   return launch_status();
 }
@@ -743,9 +748,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* sa_base = p.sA + static_cast<int64_t>(e) * KB * p.max_m + j * BNT + col0;
       const float* sb_ptr = p.sB + (static_cast<int64_t>(e) * nblk + nb) * KB;
       // Token scales run kScaleAhead k-blocks ahead of their use: one float4
-      // per lane in a register ring (rotated, static indices), parked in this
-      // warp's shared double buffer one k-block before use, so no global load
-      // latency sits on the per-k-block path.
+      // per lane in a register ring, parked in this warp's shared double buffer
+      // one k-block before use, so no global load latency sits on the
+      // per-k-block path.  The k-block loop is unrolled by the ring depth, so
+      // each ring entry is loaded once and read kScaleAhead k-blocks later with
+      // no register moves in between (a move would wait for its load).
       const bool ld_lane = lane * 4 < my_cols;
       auto load_sa4 = [&](int k) {
         return (ld_lane && k < KB)
@@ -753,8 +760,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                    : make_float4(0.f, 0.f, 0.f, 0.f);
       };
       auto load_sb = [&](int k) { return k < KB ? __ldg(sb_ptr + k) : 0.f; };
-      float4 pa1 = load_sa4(1), pa2 = load_sa4(2), pa3 = load_sa4(3);
-      float sb0 = load_sb(0), sb1 = load_sb(1), sb2 = load_sb(2), sb3 = load_sb(3);
+      // pa[m] holds the token scales of the next k-block = m (mod 4) still to be
+      // parked; rs[m] the weight scale of the next k-block = m (mod 4) to use
+      float4 pa[kScaleAhead];
+      float rs[kScaleAhead];
+      static_assert(kScaleAhead == 4, "ring indexing below assumes 4");
+      pa[1] = load_sa4(1); pa[2] = load_sa4(2); pa[3] = load_sa4(3); pa[0] = load_sa4(4);
+#pragma unroll
+      for (int m = 0; m < kScaleAhead; ++m) rs[m] = load_sb(m);
       {
         const float4 pa0 = load_sa4(0);
         __syncwarp();
@@ -764,50 +777,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       float2 acc[C::kHalf / 2];
 #pragma unroll
       for (int i = 0; i < C::kHalf / 2; ++i) acc[i] = make_float2(0.f, 0.f);
-      for (int kb = 0; kb < KB; ++kb, ++acc_it) {
-        const uint32_t b = acc_it % C::kBufs, tph = (acc_it / C::kBufs) & 1;
-        const float sb = sb0;
-        const float4 pa4 = load_sa4(kb + kScaleAhead);
-        sb0 = sb1; sb1 = sb2; sb2 = sb3; sb3 = load_sb(kb + kScaleAhead);
-        int got = 1;
-        if (lane == 0) got = mbar_wait_bounded(tfull0 + 8 * b, tph, abort, p.err, p.wait_limit_ns);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BNT + col0;
-        const float* sa_cur = my_sa + (kb & 1) * C::kHalf;
+#pragma unroll 1
+      for (int kb0 = 0; ok && kb0 < KB; kb0 += kScaleAhead) {
 #pragma unroll
-        for (int ch = 0; ch < C::kHalf / 16; ch += C::kPair) {
-          if (ch < nchunk) {
-            uint32_t r[C::kPair][16];
-            tmem_ld_32x32b_x16(tbase + ch * 16, r[0]);
-            if (C::kPair == 2 && ch + 1 < nchunk) tmem_ld_32x32b_x16(tbase + (ch + 1) * 16, r[C::kPair - 1]);
-            tmem_ld_wait();
+        for (int m = 0; m < kScaleAhead; ++m) {
+          const int kb = kb0 + m;
+          if (kb >= KB) break;
+          const uint32_t b = acc_it % C::kBufs, tph = (acc_it / C::kBufs) & 1;
+          ++acc_it;
+          const float sb = rs[m];
+          rs[m] = load_sb(kb + kScaleAhead);
+          int got = 1;
+          if (lane == 0) got = mbar_wait_bounded(tfull0 + 8 * b, tph, abort, p.err, p.wait_limit_ns);
+          got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BNT + col0;
+          const float* sa_cur = my_sa + (kb & 1) * C::kHalf;
 #pragma unroll
-            for (int h = 0; h < C::kPair; ++h) {
-              if (ch + h < nchunk) {
+          for (int ch = 0; ch < C::kHalf / 16; ch += C::kPair) {
+            if (ch < nchunk) {
+              uint32_t r[C::kPair][16];
+              tmem_ld_32x32b_x16(tbase + ch * 16, r[0]);
+              if (C::kPair == 2 && ch + 1 < nchunk) tmem_ld_32x32b_x16(tbase + (ch + 1) * 16, r[C::kPair - 1]);
+              tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const int c = (ch + h) * 16 + 2 * i;
-                  const float2 s2 = __fmul2_rn(make_float2(sb, sb), make_float2(sa_cur[c], sa_cur[c + 1]));
-                  acc[c / 2] = __ffma2_rn(
-                      s2, make_float2(__uint_as_float(r[h][2 * i]), __uint_as_float(r[h][2 * i + 1])), acc[c / 2]);
+              for (int h = 0; h < C::kPair; ++h) {
+                if (ch + h < nchunk) {
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) {
+                    const int c = (ch + h) * 16 + 2 * i;
+                    const float2 s2 = __fmul2_rn(make_float2(sb, sb), make_float2(sa_cur[c], sa_cur[c + 1]));
+                    acc[c / 2] = __ffma2_rn(
+                        s2, make_float2(__uint_as_float(r[h][2 * i]), __uint_as_float(r[h][2 * i + 1])), acc[c / 2]);
+                  }
                 }
               }
             }
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty0 + 8 * b);
-        if (kb + 1 < KB) {
-          if (ld_lane) reinterpret_cast<float4*>(my_sa + ((kb + 1) & 1) * C::kHalf)[lane] = pa1;
+          tc_fence_before();
           __syncwarp();
+          if (lane == 0) mbar_arrive(tempty0 + 8 * b);
+          // park the next k-block's token scales, then refill that ring entry
+          const int mn = (m + 1) % kScaleAhead;
+          if (kb + 1 < KB) {
+            if (ld_lane) reinterpret_cast<float4*>(my_sa + ((kb + 1) & 1) * C::kHalf)[lane] = pa[mn];
+            __syncwarp();
+          }
+          pa[mn] = load_sa4(kb + 1 + kScaleAhead);
         }
-        pa1 = pa2; pa2 = pa3; pa3 = pa4;
       }
       if (!ok) break;
       // D[e][token][n]: a warp writes 32 consecutive n of one token per store

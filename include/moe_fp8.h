@@ -69,6 +69,10 @@ extern "C" {
 #define MOE_GEMM_DEFAULT 0
 #define MOE_GEMM_FORCE_TOKENS_M 0x1   /* masked: force the tokens-as-M tile kernel      */
 #define MOE_GEMM_FORCE_WEIGHTS_M 0x2  /* masked: force the weights-as-M (swap AB) kernel */
+#define MOE_FFN_FUSE_SWIGLU 0x4       /* moe_ffn only: where the tokens-as-M kernel serves
+                                         GEMM1, run SwiGLU + 1x128 requantisation in its
+                                         epilogue instead of writing bf16 Y1 and calling
+                                         moe_swiglu_quant (same bytes either way)         */
 #define MOE_GEMM_DEBUG_STALL 0x100    /* test only: the TMA producer never issues, so the
                                          consumer's bounded wait expires and the call
                                          reports MOE_DEV_TIMEOUT (no hang, no trap)      */
@@ -238,7 +242,9 @@ int moe_combine(const uint16_t *Y2, int64_t ldy, int64_t y_rows,
  * 7 cudaEvent_t handles recorded on `stream` before stage 1 and after each of
  * the six stages, for per-stage timing.  moe_ffn quantises each routed token
  * row straight into its expert slot (stages 1 and 2 fused, same bytes as the
- * separate calls), so events 0 and 1 are recorded back to back.
+ * separate calls), so events 0 and 1 are recorded back to back; with
+ * MOE_FFN_FUSE_SWIGLU in gemm_flags and the tokens-as-M kernel serving GEMM1,
+ * stages 3 and 4 are fused the same way (events 3 and 4 back to back).
  */
 typedef struct moe_ffn_desc {
   int64_t T;              /* tokens (rows of x and out)                 */

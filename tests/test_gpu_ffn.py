@@ -147,13 +147,16 @@ def test_ffn_prefill_contiguous_sampled_tokens(lib):
     check_tol(got[tokens], _oracle_tokens("c3", wl, tokens), "c3 ffn tokens")
 
 
-@pytest.mark.parametrize("name", ["c1", "c2", "c3"])
-def test_ffn_equals_the_stage_entry_points(lib, name):
-    """moe_ffn fuses quantisation into the permute; its output must be bit-identical
-    to the public stage calls made one by one (quant, permute, GEMM1, SwiGLU+quant,
-    GEMM2, combine)."""
+@pytest.mark.parametrize("name,fuse", [("c1", False), ("c2", False), ("c3", False), ("c2", True), ("c3", True)])
+def test_ffn_equals_the_stage_entry_points(lib, name, fuse):
+    """moe_ffn fuses quantisation into the permute (and, with MOE_FFN_FUSE_SWIGLU,
+    SwiGLU + requantisation into the tokens-as-M GEMM1 epilogue); its output must
+    be bit-identical to the public stage calls made one by one (quant, permute,
+    GEMM1, SwiGLU+quant, GEMM2, combine)."""
     wl = build_workload(name)
     cfg = wl["cfg"]
+    if fuse:
+        wl["gemm_flags"] = lib.MOE_FFN_FUSE_SWIGLU
     got, st = _gpu_ffn(lib, wl)
     T, H, I, E, k = wl["T"], cfg.H, cfg.I, cfg.E, wl["k"]
     dev = "cuda"
