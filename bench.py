@@ -412,7 +412,8 @@ def main():
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     err = moe.new_error_word(dev)
     events = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
-    desc = make_desc(wl, out, err=err, stage_events=events)
+    desc = make_desc(wl, out, err=err)                           # the timed step
+    desc_ev = make_desc(wl, out, err=err, stage_events=events)   # the per-stage split
     ws = moe.alloc_workspace(desc, dev)
     l2_flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -425,9 +426,13 @@ def main():
         raise SystemExit(f"device status {moe.moe_status_string(status)} during warm-up")
 
     # One step = one moe_ffn.  By default it is captured once in a CUDA graph
-    # (as the decode path runs in serving) and replayed; the stage events are
-    # event-record nodes of the graph, so they time the device work.
+    # (as the decode path runs in serving) and replayed.  The timed step is
+    # bracketed by two events on the stream around the replay; the per-stage
+    # split comes from a second graph of the same call with the stage events
+    # as event-record nodes (they sit between the kernels, so that graph is
+    # used for the split only).
     step = lambda: moe.moe_ffn(desc, ws)
+    step_ev = lambda: moe.moe_ffn(desc_ev, ws)
     graph = None
     if not args.eager:
         side = torch.cuda.Stream(dev)
@@ -438,27 +443,33 @@ def main():
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             moe.moe_ffn(desc, ws)
+        graph_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_ev):
+            moe.moe_ffn(desc_ev, ws)
         for _ in range(args.warmup):
             graph.replay()
+            graph_ev.replay()
         torch.cuda.synchronize(dev)
         try:                                       # the graph's stage events must be timeable
             events[0].elapsed_time(events[6])
-            step = graph.replay
+            step, step_ev = graph.replay, graph_ev.replay
         except RuntimeError as exc:
             print(f"graph stage events not timeable ({exc}); timing eager calls", file=sys.stderr)
             graph = None
 
-    step_ms, g1_ms = [], []
+    step_ms = []
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     _barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
         t_wall = time.perf_counter()
         for _ in range(args.steps):
             l2_flush.fill_(1)                       # evict the previous step from L2
+            t0.record(stream)
             step()
+            t1.record(stream)
             torch.cuda.synchronize(dev)
-            step_ms.append(events[0].elapsed_time(events[6]))
-            g1_ms.append(events[2].elapsed_time(events[3]))
+            step_ms.append(t0.elapsed_time(t1))
         t_wall = time.perf_counter() - t_wall
     _barrier(world)
     torch.cuda.synchronize(dev)
@@ -466,13 +477,17 @@ def main():
     if status not in (moe.MOE_OK, moe.MOE_ERR_OVERFLOW):
         raise SystemExit(f"device status {moe.moe_status_string(status)} in the timed region")
     stage_ms = [0.0] * 6
-    # one more instrumented pass for the per-stage split (not part of the value)
-    for _ in range(3):
+    g1_ms = []
+    # instrumented passes for the per-stage split and the GEMM1 launch time
+    # (not part of the value)
+    n_split = max(3, min(args.steps, 10))
+    for _ in range(n_split):
         l2_flush.fill_(1)
-        step()
+        step_ev()
         torch.cuda.synchronize(dev)
         for i in range(6):
-            stage_ms[i] += events[i].elapsed_time(events[i + 1]) / 3
+            stage_ms[i] += events[i].elapsed_time(events[i + 1]) / n_split
+        g1_ms.append(events[2].elapsed_time(events[3]))
 
     total_s = sum(step_ms) / 1e3
     total_s = _max_over_ranks(world, total_s)
@@ -562,6 +577,7 @@ def main():
                        "expected_m_hint": wl["expected_m"], "gemm_flags": args.gemm_flags,
                        "l2": "flushed (256 MiB write) before every timed step",
                        "launch": "eager moe_ffn" if graph is None else "moe_ffn captured once in a CUDA graph, replayed per step",
+                       "timing": "CUDA events on the launching stream around each step; stage split from a separate instrumented replay",
                        "parallelism": f"replicas x{world}"},
             "stage_ms": {n: round(v, 4) for n, v in zip(
                 ["quant (fused into permute)", "quant+permute", "gemm1", "swiglu_quant (fused into gemm1 when 0)", "gemm2", "combine"], stage_ms)},

@@ -127,7 +127,9 @@ struct TileCursor {
   }
 };
 
-// Warp 0 builds the tile schedule: each lane owns a contiguous chunk of experts.
+// Warp 0 builds the tile schedule: each lane owns a contiguous chunk of experts;
+// an expert's rows are cut into blocks of kRows (128, or 256 for a CTA pair).
+template <int kRows = BM>
 __device__ void build_schedule(const GemmArgs& p, const Sched& s, int n_tiles) {
   const int lane = threadIdx.x & 31;
   const int per = (p.E + 31) / 32;
@@ -149,7 +151,7 @@ __device__ void build_schedule(const GemmArgs& p, const Sched& s, int n_tiles) {
     }
     s.rbase[e] = rb;
     s.rext[e] = rx;
-    local += (rx + BM - 1) / BM * n_tiles;
+    local += (rx + kRows - 1) / kRows * n_tiles;
   }
   int incl = local;
 #pragma unroll
@@ -160,7 +162,7 @@ __device__ void build_schedule(const GemmArgs& p, const Sched& s, int n_tiles) {
   int run = incl - local;
   for (int e = e0; e < e1; ++e) {
     s.tile0[e] = run;
-    run += (s.rext[e] + BM - 1) / BM * n_tiles;
+    run += (s.rext[e] + kRows - 1) / kRows * n_tiles;
   }
   if (lane == 31) s.tile0[p.E] = incl;
   if (blockIdx.x == 0) {
@@ -217,17 +219,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0) {
-    build_schedule(p, sched, n_tiles);
-    if (lane == 0) {
-      tma_prefetch_desc(&tmA);
-      tma_prefetch_desc(&tmB);
-    }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  // the local set-up above overlaps the previous kernel; the schedule reads
+  // the counts / offsets it wrote
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if (warp == 0) build_schedule(p, sched, n_tiles);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -519,12 +523,330 @@ int launch_tokens_m(const uint8_t* A, int64_t a_rows, int64_t lda, const uint8_t
   if (grid < 1) grid = 1;
   if (swiglu) {
     if (int st = prepare_kernel(gemm_fp8_tokens_m_kernel<true>, smem, true)) return st;
-    gemm_fp8_tokens_m_kernel<true><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, args);
+    return launch_pdl(gemm_fp8_tokens_m_kernel<true>, static_cast<unsigned>(grid), kThreads, smem, stream, tmA,
+                      tmB, args);
   } else {
     if (int st = prepare_kernel(gemm_fp8_tokens_m_kernel<false>, smem, true)) return st;
-    gemm_fp8_tokens_m_kernel<false><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, args);
+    return launch_pdl(gemm_fp8_tokens_m_kernel<false>, static_cast<unsigned>(grid), kThreads, smem, stream, tmA,
+                      tmB, args);
   }
-  return launch_status();
+}
+
+// =============================================================================
+// Tokens-as-M over a CTA pair (2-CTA cluster, UMMA M = 256).
+//
+// What bounds the single-CTA kernel is each SM's tile feed: 48 KB of A and B
+// per 128-deep block for a 128x256 tile.  Here the two CTAs of a cluster
+// compute a 256x256 tile with one M = 256 UMMA issued by the even CTA: each
+// CTA stages its own 128 token rows of A and half (128 rows) of the 256 weight
+// rows of B, 32 KB per block, and the tensor cores read the peer's half across
+// the pair.  Each CTA's TMEM holds its 128 rows of D, drained and promoted by
+// its own epilogue exactly as in the single-CTA kernel.
+//
+// Signalling (all waits bounded): each CTA's producer fills its own stage and
+// its full barrier; in the odd CTA warp 1 relays that to the even CTA's pfull
+// barrier; the even CTA's MMA thread waits full + pfull + tempty, issues, and
+// its commits arrive on empty and tfull in both CTAs; every epilogue warp of
+// both CTAs arrives on the even CTA's tempty.
+// =============================================================================
+constexpr int BM2 = 256;                              // rows per pair tile
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairATile = 128 * BK;             // this CTA's 128 rows of A
+constexpr uint32_t kPairBTile = 128 * BK;             // this CTA's half of B
+constexpr uint32_t kPairStage = kPairATile + kPairBTile;
+constexpr int kPairBars = 3 * kPairStages + 4;        // full, empty, pfull [S]; tfull, tempty [2]
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_fp8_tokens_m_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                                  const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* a_tiles = smem;
+  uint8_t* b_tiles = smem + kPairStages * kPairATile;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStage);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kPairBars);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int32_t* sched_mem = reinterpret_cast<int32_t*>(tmem_slot + 4);
+  const Sched sched{sched_mem, sched_mem + p.E + 1, sched_mem + 2 * p.E + 1};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool even = rank == 0;
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * kPairStages;
+  const uint32_t pfull0 = empty0 + 8 * kPairStages;
+  const uint32_t tfull0 = pfull0 + 8 * kPairStages;
+  const uint32_t tempty0 = tfull0 + 16;
+  const int n_tiles = p.N / BN;
+  const int KB = p.K / BK;
+  const int NB = p.N / 128;
+  volatile int* abort = abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(pfull0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull0 + 8 * b, 1);
+      mbar_init(tempty0 + 8 * b, 2 * kEpiWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if (warp == 0) build_schedule<BM2>(p, sched, n_tiles);
+  // both CTAs' barriers are initialised before any arrival crosses the pair
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = sched.tile0[p.E];
+  const int t_first = static_cast<int>(cluster_id_x());
+  const int t_step = static_cast<int>(cluster_count_x());
+  if (warp < kEpiWarp0) {
+    regs_release_low();
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0 && !(p.flags & MOE_GEMM_DEBUG_STALL)) {
+      uint32_t it = 0;
+      TileCursor cur;
+      bool ok = true;
+      for (int t = t_first; ok && t < total; t += t_step) {
+        cur.seek(sched, t);
+        const int l = t - sched.tile0[cur.e];
+        const int a_row = sched.rbase[cur.e] + (l / n_tiles) * BM2 + static_cast<int>(rank) * 128;
+        const int b_row = cur.e * p.N + (l % n_tiles) * BN + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const uint32_t s = it % kPairStages, ph = (it / kPairStages) & 1;
+          if (!mbar_wait_bounded_cluster(empty0 + 8 * s, ph ^ 1, abort, p.err, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full0 + 8 * s, kPairStage);
+          tma_load_2d(smem_u32(a_tiles + s * kPairATile), &tmA, full0 + 8 * s, kb * BK, a_row);
+          tma_load_2d(smem_u32(b_tiles + s * kPairBTile), &tmB, full0 + 8 * s, kb * BK, b_row);
+        }
+      }
+      if (!ok) {
+        // drain: let the copies already issued land before the CTA exits
+        const uint32_t first = it > kPairStages ? it - kPairStages : 0;
+        for (uint32_t j = first; j < it; ++j) {
+          int dummy = 0;
+          mbar_wait_bounded(full0 + 8 * (j % kPairStages), (j / kPairStages) & 1, &dummy, nullptr,
+                            p.wait_limit_ns / 10);
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    if (even) {
+      // ---------------------------------------------------------- MMA issuer (even CTA)
+      uint32_t it = 0, acc = 0;
+      bool ok = true;
+      const uint32_t idesc = idesc_e4m3_f32(BM2, BN);
+      for (int t = t_first; ok && t < total; t += t_step) {
+        for (int kb = 0; kb < KB; ++kb, ++it, ++acc) {
+          const uint32_t s = it % kPairStages, ph = (it / kPairStages) & 1;
+          const uint32_t b = acc & 1, tph = (acc >> 1) & 1;
+          if (!mbar_wait_bounded_cluster(tempty0 + 8 * b, tph ^ 1, abort, p.err, p.wait_limit_ns) ||
+              !mbar_wait_bounded(full0 + 8 * s, ph, abort, p.err, p.wait_limit_ns) ||
+              !mbar_wait_bounded_cluster(pfull0 + 8 * s, ph, abort, p.err, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(a_tiles + s * kPairATile));
+          const uint64_t bd = sdesc_kmajor_sw128(smem_u32(b_tiles + s * kPairBTile));
+          const uint32_t d_tmem = tmem_base + b * BN;
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)  // 32 bytes of K per MMA: +2 in the 16-byte address field
+            umma_e4m3_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
+          umma_commit_pair(empty0 + 8 * s, 0x3);
+          umma_commit_pair(tfull0 + 8 * b, 0x3);
+        }
+      }
+      if (acc > 0) {  // the last MMAs (and their commits to both CTAs) are done before teardown
+        int dummy = 0;
+        mbar_wait_bounded(tfull0 + 8 * ((acc - 1) & 1), ((acc - 1) >> 1) & 1, &dummy, nullptr,
+                          ok ? p.wait_limit_ns : p.wait_limit_ns / 10);
+      }
+    } else {
+      // ---------------------------------------------------------- stage relay (odd CTA)
+      uint32_t it = 0;
+      bool ok = true;
+      const uint32_t pfull_even = cluster_map_shared(pfull0, 0);
+      for (int t = t_first; ok && t < total; t += t_step) {
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const uint32_t s = it % kPairStages, ph = (it / kPairStages) & 1;
+          if (!mbar_wait_bounded(full0 + 8 * s, ph, abort, p.err, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(pfull_even + 8 * s);
+        }
+      }
+    }
+  }
+  } else {
+    regs_acquire_high();
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int g = (warp - kEpiWarp0) >> 2;
+    const uint32_t tempty_even = cluster_map_shared(tempty0, 0);
+    uint32_t acc_it = 0;
+    TileCursor cur;
+    bool ok = true;
+    for (int t = t_first; ok && t < total; t += t_step) {
+      cur.seek(sched, t);
+      const int e = cur.e;
+      const int l = t - sched.tile0[e];
+      const int mt = l / n_tiles, nt = l % n_tiles;
+      const int r_local = mt * BM2 + static_cast<int>(rank) * 128 + q * 32 + lane;
+      const int64_t gr = static_cast<int64_t>(sched.rbase[e]) + r_local;
+      bool row_ok = r_local < sched.rext[e];
+      if (row_ok && p.layout == MOE_LAYOUT_CONTIG) row_ok = __ldg(p.m_indices + gr) >= 0;
+      const int n0 = nt * BN + g * 128;
+      const int64_t grp = gr / p.sA_G, pos = gr - grp * p.sA_G;
+      const float* sa_ptr = p.sA + grp * KB * p.sA_G + pos;
+      const float* sb_ptr = p.sB + (static_cast<int64_t>(e) * NB + n0 / 128) * KB;
+      float2 acc[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.f, 0.f);
+      // scales four k-blocks ahead; the loop is unrolled by that depth so each
+      // ring register is loaded once and read four k-blocks later
+      auto load_sa = [&](int k) { return (row_ok && k < KB) ? __ldg(sa_ptr + static_cast<int64_t>(k) * p.sA_G) : 0.f; };
+      auto load_sb = [&](int k) { return k < KB ? __ldg(sb_ptr + k) : 0.f; };
+      float ra[kScaleAhead], rb[kScaleAhead];
+#pragma unroll
+      for (int j = 0; j < kScaleAhead; ++j) {
+        ra[j] = load_sa(j);
+        rb[j] = load_sb(j);
+      }
+#pragma unroll 1
+      for (int kb0 = 0; ok && kb0 < KB; kb0 += kScaleAhead) {
+#pragma unroll
+        for (int j = 0; j < kScaleAhead; ++j) {
+          const int kb = kb0 + j;
+          if (kb >= KB) break;
+          const uint32_t b = acc_it & 1, tph = (acc_it >> 1) & 1;
+          ++acc_it;
+          const float sc = ra[j] * rb[j];
+          ra[j] = load_sa(kb + kScaleAhead);
+          rb[j] = load_sb(kb + kScaleAhead);
+          int got = 1;
+          if (lane == 0) got = mbar_wait_bounded_cluster(tfull0 + 8 * b, tph, abort, p.err, p.wait_limit_ns);
+          got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float2 sc2 = make_float2(sc, sc);
+          const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + g * 128;
+#pragma unroll
+          for (int c = 0; c < 8; c += 2) {   // two 16-column loads in flight
+            uint32_t r0[16], r1[16];
+            tmem_ld_32x32b_x16(tbase + c * 16, r0);
+            tmem_ld_32x32b_x16(tbase + (c + 1) * 16, r1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              acc[c * 8 + i] = __ffma2_rn(sc2, make_float2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1])),
+                                          acc[c * 8 + i]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              acc[(c + 1) * 8 + i] = __ffma2_rn(
+                  sc2, make_float2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])), acc[(c + 1) * 8 + i]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(tempty_even + 8 * b);
+        }
+      }
+      if (!ok) break;
+      if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(p.D + gr * p.ldd + n0);
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+          uint32_t o[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const __nv_bfloat162 bb = __floats2bfloat162_rn(acc[v * 4 + h].x, acc[v * 4 + h].y);
+            o[h] = *reinterpret_cast<const uint32_t*>(&bb);
+          }
+          dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+  }
+
+  // no CTA leaves while its peer may still read its shared memory or arrive
+  // on its barriers
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+size_t pair_smem_bytes(int E) {
+  return 1024 + static_cast<size_t>(kPairStages) * kPairStage + kPairBars * 8 + 16 +
+         sizeof(int32_t) * (3 * E + 1);
+}
+
+// Launch the pair kernel: grid = 2 x the clusters that fit at once (at most
+// one per pair tile), two CTAs per cluster.
+int launch_tokens_m_pair(const uint8_t* A, int64_t a_rows, int64_t lda, const uint8_t* B,
+                         int64_t pair_tiles_upper, GemmArgs& args, cudaStream_t stream) {
+  CUtensorMap tmA, tmB;
+  if (int st = make_tmap_u8_sw128(&tmA, A, a_rows, args.K, lda, 128)) return st;
+  if (int st = make_tmap_u8_sw128(&tmB, B, static_cast<uint64_t>(args.E) * args.N, args.K, args.K, 128))
+    return st;
+  const size_t smem = pair_smem_bytes(args.E);
+  if (args.wait_limit_ns == 0) args.wait_limit_ns = kWaitLimitNs;
+  if (int st = prepare_kernel(gemm_fp8_tokens_m_pair_kernel, smem, true)) return st;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  static int max_clusters_cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  if (max_clusters_cached[dev] == 0) {
+    int n = 0;
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_fp8_tokens_m_pair_kernel, &cfg) != cudaSuccess || n < 1)
+      return MOE_ERR_UNSUPPORTED;
+    max_clusters_cached[dev] = n;
+  }
+  int64_t clusters = max_clusters_cached[dev];
+  if (pair_tiles_upper < clusters) clusters = pair_tiles_upper;
+  if (clusters < 1) clusters = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+  return cudaLaunchKernelEx(&cfg, gemm_fp8_tokens_m_pair_kernel, tmA, tmB, args) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
 }
 
 // =============================================================================
@@ -629,17 +951,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0) {
-    build_schedule_wm<BNT>(p, sched, nblk);
-    if (lane == 0) {
-      tma_prefetch_desc(&tmT);
-      tma_prefetch_desc(&tmW);
-    }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmT);
+    tma_prefetch_desc(&tmW);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if (warp == 0) build_schedule_wm<BNT>(p, sched, nblk);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -869,8 +1191,8 @@ int launch_weights_m(const uint8_t* A, const uint8_t* B, GemmArgs& args, cudaStr
   int64_t grid = num_sms();
   if (tiles_upper < grid) grid = tiles_upper;
   if (grid < 1) grid = 1;
-  gemm_fp8_weights_m_kernel<BNT><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmT, tmW, args);
-  return launch_status();
+  return launch_pdl(gemm_fp8_weights_m_kernel<BNT>, static_cast<unsigned>(grid), kThreads, smem, stream, tmT,
+                    tmW, args);
 }
 
 }  // namespace

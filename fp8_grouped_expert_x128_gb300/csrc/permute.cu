@@ -44,6 +44,8 @@ struct IndexParams {
 // ordered rank pass below runs at shared-memory latency.
 __global__ void __launch_bounds__(kIdxThreads) permute_index_kernel(IndexParams p, int ids_in_smem) {
   extern __shared__ int32_t sm[];
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int E = p.E;
   int32_t* cnt = sm;
   int32_t* base = sm + E;
@@ -143,6 +145,8 @@ __global__ void __launch_bounds__(128) permute_scatter_kernel(
     const uint8_t* __restrict__ q, const float* __restrict__ s, int64_t s_ld,
     const int32_t* __restrict__ dst_row, int64_t n_assign, int32_t k, int64_t H,
     uint8_t* __restrict__ q_out, float* __restrict__ s_out, int64_t G) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (i >= n_assign) return;
@@ -170,6 +174,8 @@ __global__ void __launch_bounds__(32 * kQsWarps) quant_scatter_kernel(
     const uint16_t* __restrict__ x, int64_t ldx, const int32_t* __restrict__ dst_row,
     int64_t n_assign, int32_t k, int64_t H, uint8_t* __restrict__ q_out, float* __restrict__ s_out,
     int64_t G) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int64_t i = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (i >= n_assign) return;
@@ -218,6 +224,8 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(
     const uint16_t* __restrict__ y2, int64_t ldy, int64_t y_rows, const int32_t* __restrict__ dst_row,
     const float* __restrict__ topk_w, int32_t k, int64_t H, uint16_t* __restrict__ out, int64_t ldo,
     int32_t* err) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   __shared__ int32_t s_dst[32];
   __shared__ float s_w[32];
   __shared__ int s_n;
@@ -340,17 +348,15 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(smem)));
   }
-  permute_index_kernel<<<1, kIdxThreads, smem, st>>>(p, ids_in_smem);
-  if (int rc = launch_status()) return rc;
+  if (int rc = launch_pdl(permute_index_kernel, 1, kIdxThreads, smem, st, p, ids_in_smem)) return rc;
   if (T == 0) return MOE_OK;
   const int64_t n = T * k;
   const unsigned grid = static_cast<unsigned>((n + 3) / 4);
   if (x != nullptr)
-    quant_scatter_kernel<<<static_cast<unsigned>(n), 32 * kQsWarps, 0, st>>>(x, ldx, dst_row, n, k, H,
-                                                                          q_out, s_out, G);
-  else
-    permute_scatter_kernel<<<grid, 128, 0, st>>>(q, s, s_ld, dst_row, n, k, H, q_out, s_out, G);
-  return launch_status();
+    return launch_pdl(quant_scatter_kernel, static_cast<unsigned>(n), 32 * kQsWarps, 0, st, x, ldx,
+                      dst_row, n, k, H, q_out, s_out, G);
+  return launch_pdl(permute_scatter_kernel, grid, 128, 0, st, q, s, s_ld, dst_row, n, k, H, q_out,
+                    s_out, G);
 }
 
 }  // namespace moe
@@ -375,7 +381,6 @@ extern "C" int moe_combine(const uint16_t* Y2, int64_t ldy, int64_t y_rows, cons
   MOE_CHECK_ARG(ldy >= H && ldy % 8 == 0 && ldo >= H && ldo % 8 == 0 && y_rows >= 0);
   MOE_CHECK_ARG(T < (1ll << 31));
   if (int st = check_device()) return st;
-  combine_kernel<<<static_cast<unsigned>(T), kCombThreads, 0, as_stream(stream)>>>(
-      Y2, ldy, y_rows, dst_row, topk_w, k, H, out, ldo, err);
-  return launch_status();
+  return launch_pdl(combine_kernel, static_cast<unsigned>(T), kCombThreads, 0, as_stream(stream), Y2,
+                    ldy, y_rows, dst_row, topk_w, k, static_cast<int64_t>(H), out, ldo, err);
 }

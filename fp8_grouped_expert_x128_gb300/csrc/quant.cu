@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __rest
                                                           int64_t M, int64_t KB, int64_t ldx,
                                                           uint8_t* __restrict__ q, int64_t ldq,
                                                           float* __restrict__ s, int64_t s_ld) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int64_t warps_per_row = (KB + 1) / 2;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -51,6 +53,8 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const uint16_t* __re
                                                             int64_t N, int64_t K,
                                                             uint8_t* __restrict__ q,
                                                             float* __restrict__ s) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int64_t NB = N / 128, KB = K / 128;
   const int64_t tile = blockIdx.x;  // over E * NB * KB
   const int64_t e = tile / (NB * KB);
@@ -90,6 +94,8 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(
     const uint16_t* __restrict__ y1, int64_t rows, int64_t I, const int32_t* __restrict__ counts,
     int64_t max_m, const int32_t* __restrict__ m_indices, uint8_t* __restrict__ q,
     float* __restrict__ s, int64_t G) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int64_t KB = I / 128;
   const int64_t warps_per_row = (KB + 1) / 2;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -145,9 +151,8 @@ extern "C" int moe_quant_fp8(const uint16_t* x, int64_t M, int64_t K, int64_t ld
   MOE_CHECK_ARG(ldx >= K && ldx % 8 == 0 && ldq >= K && ldq % 16 == 0 && s_ld >= M);
   if (int st = check_device()) return st;
   const int64_t warps = M * ((K / 128 + 1) / 2);
-  quant_1x128_kernel<<<grid_for_warps(warps), 256, 0, as_stream(stream)>>>(x, M, K / 128, ldx, q,
-                                                                          ldq, s, s_ld);
-  return launch_status();
+  return launch_pdl(quant_1x128_kernel, grid_for_warps(warps), 256, 0, as_stream(stream), x, M,
+                    K / 128, ldx, q, ldq, s, s_ld);
 }
 
 extern "C" int moe_quant_weight_fp8(const uint16_t* w, int64_t E, int64_t N, int64_t K, uint8_t* q,
@@ -159,8 +164,8 @@ extern "C" int moe_quant_weight_fp8(const uint16_t* w, int64_t E, int64_t N, int
   if (int st = check_device()) return st;
   const int64_t tiles = E * (N / 128) * (K / 128);
   MOE_CHECK_ARG(tiles < (1ll << 31));
-  quant_128x128_kernel<<<static_cast<unsigned>(tiles), 256, 0, as_stream(stream)>>>(w, N, K, q, s);
-  return launch_status();
+  return launch_pdl(quant_128x128_kernel, static_cast<unsigned>(tiles), 256, 0, as_stream(stream), w,
+                    N, K, q, s);
 }
 
 extern "C" int moe_swiglu_quant(const uint16_t* Y1, int64_t rows, int32_t I, const int32_t* counts,
@@ -180,7 +185,7 @@ extern "C" int moe_swiglu_quant(const uint16_t* Y1, int64_t rows, int32_t I, con
   }
   if (int st = check_device()) return st;
   const int64_t warps = rows * ((I / 128 + 1) / 2);
-  swiglu_quant_kernel<<<grid_for_warps(warps), 256, 0, as_stream(stream)>>>(
-      Y1, rows, I, counts, max_m, counts ? nullptr : m_indices, q, s, G);
-  return launch_status();
+  return launch_pdl(swiglu_quant_kernel, grid_for_warps(warps), 256, 0, as_stream(stream), Y1,
+                    rows, static_cast<int64_t>(I), counts, static_cast<int64_t>(max_m),
+                    counts ? nullptr : m_indices, q, s, G);
 }
