@@ -40,6 +40,7 @@ MOE_GEMM_DEFAULT = 0
 MOE_GEMM_FORCE_TOKENS_M = 0x1
 MOE_GEMM_FORCE_WEIGHTS_M = 0x2
 MOE_FFN_FUSE_SWIGLU = 0x4
+MOE_GEMM_CTA_PAIR = 0x8
 MOE_GEMM_DEBUG_STALL = 0x100
 
 EXPORTED = [

@@ -630,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b_row = cur.e * p.N + (l % n_tiles) * BN + static_cast<int>(rank) * 128;
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const uint32_t s = it % kPairStages, ph = (it / kPairStages) & 1;
-          if (!mbar_wait_bounded_cluster(empty0 + 8 * s, ph ^ 1, abort, p.err, p.wait_limit_ns)) {
+          if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, p.err, p.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -659,9 +659,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < KB; ++kb, ++it, ++acc) {
           const uint32_t s = it % kPairStages, ph = (it / kPairStages) & 1;
           const uint32_t b = acc & 1, tph = (acc >> 1) & 1;
-          if (!mbar_wait_bounded_cluster(tempty0 + 8 * b, tph ^ 1, abort, p.err, p.wait_limit_ns) ||
+          if (!mbar_wait_bounded(tempty0 + 8 * b, tph ^ 1, abort, p.err, p.wait_limit_ns) ||
               !mbar_wait_bounded(full0 + 8 * s, ph, abort, p.err, p.wait_limit_ns) ||
-              !mbar_wait_bounded_cluster(pfull0 + 8 * s, ph, abort, p.err, p.wait_limit_ns)) {
+              !mbar_wait_bounded(pfull0 + 8 * s, ph, abort, p.err, p.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -745,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ra[j] = load_sa(kb + kScaleAhead);
           rb[j] = load_sb(kb + kScaleAhead);
           int got = 1;
-          if (lane == 0) got = mbar_wait_bounded_cluster(tfull0 + 8 * b, tph, abort, p.err, p.wait_limit_ns);
+          if (lane == 0) got = mbar_wait_bounded(tfull0 + 8 * b, tph, abort, p.err, p.wait_limit_ns);
           got = __shfl_sync(0xffffffffu, got, 0);
           if (!got) {
             ok = false;
@@ -1287,6 +1287,8 @@ extern "C" int moe_gemm_fp8_contig(const uint8_t* A, int64_t lda, const float* s
   a.layout = MOE_LAYOUT_CONTIG;
   a.err = err;
   a.flags = flags;
+  if ((flags & MOE_GEMM_CTA_PAIR) && N % BN == 0)
+    return launch_tokens_m_pair(A, M_capacity, lda, B, (M_capacity / BM) * (N / BN), a, as_stream(stream));
   const int64_t tiles = (M_capacity / BM) * ((N + BN - 1) / BN);
   return launch_tokens_m(A, M_capacity, lda, B, tiles, a, as_stream(stream));
 }
@@ -1342,6 +1344,9 @@ extern "C" int moe_gemm_fp8_masked(const uint8_t* A, const float* sA, const uint
   if (variant == 64) return launch_weights_m<64>(A, B, a, st);
   if (variant == 128) return launch_weights_m<128>(A, B, a, st);
   if (variant == 256) return launch_weights_m<256>(A, B, a, st);
+  if ((flags & MOE_GEMM_CTA_PAIR) && N % BN == 0)
+    return launch_tokens_m_pair(A, static_cast<int64_t>(E) * max_m, K, B,
+                                static_cast<int64_t>(E) * ((max_m + BM2 - 1) / BM2) * (N / BN), a, st);
   const int64_t tiles = static_cast<int64_t>(E) * ((max_m + BM - 1) / BM) * ((N + BN - 1) / BN);
   return launch_tokens_m(A, static_cast<int64_t>(E) * max_m, K, B, tiles, a, st);
 }

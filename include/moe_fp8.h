@@ -73,6 +73,9 @@ extern "C" {
                                          GEMM1, run SwiGLU + 1x128 requantisation in its
                                          epilogue instead of writing bf16 Y1 and calling
                                          moe_swiglu_quant (same bytes either way)         */
+#define MOE_GEMM_CTA_PAIR 0x8         /* tokens-as-M: run each 256x256 tile on a 2-CTA
+                                         cluster (one M = 256 UMMA, each SM stages half
+                                         of B); needs N % 256 == 0, else ignored        */
 #define MOE_GEMM_DEBUG_STALL 0x100    /* test only: the TMA producer never issues, so the
                                          consumer's bounded wait expires and the call
                                          reports MOE_DEV_TIMEOUT (no hang, no trap)      */

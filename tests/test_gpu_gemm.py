@@ -33,14 +33,14 @@ def _masked(lib, A, sA, B, sB, counts, flags=0, expected_m=0):
     return bits(D), status
 
 
-def _contig(lib, A, sA, B, sB, offsets, m_indices):
+def _contig(lib, A, sA, B, sB, offsets, m_indices, flags=0):
     M_cap, K = A.shape
     N = B.shape[1]
     D = torch.full((M_cap, N), SENTINEL_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
     err = lib.new_error_word()
     lib.moe_gemm_fp8_contig(to_dev(A), to_dev(sA), to_dev(B), to_dev(sB),
                             to_dev(np.asarray(offsets, np.int32)), to_dev(np.asarray(m_indices, np.int32)),
-                            D, err=err)
+                            D, flags=flags, err=err)
     status, _ = lib.moe_read_device_status(err)
     return bits(D), status
 
@@ -161,7 +161,7 @@ def _decode_gemm_inputs(cfg_name, which):
     return cfg, p["q"].reshape(cfg.E, cfg.max_m, K), p["s"], p["counts"]
 
 
-@pytest.mark.parametrize("flags", [0, 0x1], ids=["default", "tokens_m"])
+@pytest.mark.parametrize("flags", [0, 0x1, 0x9], ids=["default", "tokens_m", "tokens_m_pair"])
 @pytest.mark.parametrize("which", ["w13", "w2"])
 def test_gemm_masked_decode_full_size(lib, which, flags):
     cfg, A, sA, counts = _decode_gemm_inputs("c2", which)
@@ -173,7 +173,8 @@ def test_gemm_masked_decode_full_size(lib, which, flags):
     _check_masked(got, ref, valid, f"c2 {which}")
 
 
-def test_gemm_contig_prefill_sampled_rows(lib):
+@pytest.mark.parametrize("flags", [0, 0x8], ids=["single", "pair"])
+def test_gemm_contig_prefill_sampled_rows(lib, flags):
     cfg = synth.get_config("c3")
     r = routing("c3")
     T = r["T"]
@@ -196,7 +197,7 @@ def test_gemm_contig_prefill_sampled_rows(lib):
     experts = tuple(range(cfg.E))
     Bq, Bs = oracle_weights("c3", "w13", experts)
     D = torch.full((cap, 2 * cfg.I), SENTINEL_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
-    lib.moe_gemm_fp8_contig(A, sA, to_dev(Bq), to_dev(Bs), offsets, mi, D)
+    lib.moe_gemm_fp8_contig(A, sA, to_dev(Bq), to_dev(Bs), offsets, mi, D, flags=flags)
     torch.cuda.synchronize()
     got = bits(D)
     off = offsets.cpu().numpy()
@@ -229,7 +230,8 @@ def test_gemm_stall_reports_timeout_and_recovers(lib):
     A, B = rand_codes(rng, (E, max_m, K)), rand_codes(rng, (E, N, K))
     sA = np.ones((E, K // 128, max_m), np.float32)
     sB = np.ones((E, N // 128, K // 128), np.float32)
-    for kernel in (lib.MOE_GEMM_FORCE_TOKENS_M, lib.MOE_GEMM_FORCE_WEIGHTS_M):
+    for kernel in (lib.MOE_GEMM_FORCE_TOKENS_M, lib.MOE_GEMM_FORCE_WEIGHTS_M,
+                   lib.MOE_GEMM_FORCE_TOKENS_M | lib.MOE_GEMM_CTA_PAIR):
         got, st = _masked(lib, A, sA, B, sB, [5], flags=lib.MOE_GEMM_DEBUG_STALL | kernel)
         assert st == lib.MOE_ERR_TIMEOUT
         assert (got == SENTINEL_BF16).all()
@@ -237,3 +239,83 @@ def test_gemm_stall_reports_timeout_and_recovers(lib):
     assert st == 0
     ref, valid = oracle.gemm_masked(A, sA, B, sB, [5])
     _check_masked(got, ref, valid, "after timeout")
+
+
+# ---------------------------------------------------------------- CTA pairs
+# The pair kernel (MOE_GEMM_CTA_PAIR) cuts an expert's rows into 256-row blocks;
+# the cases below give experts an odd number of 128-row blocks (a pair block
+# that runs into the next expert's rows or past the buffer), a ragged count,
+# an empty expert, and more than one 256-column tile.
+
+def test_gemm_pair_integer_exact_masked(lib):
+    rng = np.random.default_rng(31)
+    E, max_m, N, K = 3, 384, 512, 512
+    counts = [384, 0, 77]
+    a = rng.integers(-16, 17, (E, max_m, K))
+    b = rng.integers(-16, 17, (E, N, K))
+    A, B = oracle.e4m3_encode(a.astype(np.float64)), oracle.e4m3_encode(b.astype(np.float64))
+    sA = np.ones((E, K // 128, max_m), np.float32)
+    sB = np.ones((E, N // 128, K // 128), np.float32)
+    got, st = _masked(lib, A, sA, B, sB, counts, flags=lib.MOE_GEMM_FORCE_TOKENS_M | lib.MOE_GEMM_CTA_PAIR)
+    assert st == 0
+    for e in range(E):
+        c = counts[e]
+        exact = (a[e, :c] @ b[e].T).astype(np.float64)
+        assert np.array_equal(got[e, :c], oracle.bf16_encode(exact)), f"expert {e}"
+        assert (got[e, c:] == SENTINEL_BF16).all()
+
+
+def _pair_contig_layout(seg):
+    offsets = [0]
+    for c in seg:
+        offsets.append(offsets[-1] + -(-c // 128) * 128)
+    M_cap = offsets[-1]
+    mi = -np.ones(M_cap, np.int64)
+    for e, c in enumerate(seg):
+        mi[offsets[e]:offsets[e] + c] = e
+    return offsets, M_cap, mi
+
+
+def test_gemm_pair_integer_exact_contig(lib):
+    rng = np.random.default_rng(32)
+    N, K = 256, 384
+    seg = [130, 0, 300, 128, 1]             # 2, 0, 3, 1, 1 row blocks of 128
+    offsets, M_cap, mi = _pair_contig_layout(seg)
+    a = rng.integers(-16, 17, (M_cap, K))
+    b = rng.integers(-16, 17, (len(seg), N, K))
+    A, B = oracle.e4m3_encode(a.astype(np.float64)), oracle.e4m3_encode(b.astype(np.float64))
+    sA = np.ones((K // 128, M_cap), np.float32)
+    sB = np.ones((len(seg), N // 128, K // 128), np.float32)
+    got, st = _contig(lib, A, sA, B, sB, offsets, mi, flags=lib.MOE_GEMM_CTA_PAIR)
+    assert st == 0
+    for e, c in enumerate(seg):
+        lo = offsets[e]
+        if c:
+            exact = (a[lo:lo + c] @ b[e].T).astype(np.float64)
+            assert np.array_equal(got[lo:lo + c], oracle.bf16_encode(exact)), f"expert {e}"
+    assert (got[mi < 0] == SENTINEL_BF16).all()
+
+
+def test_gemm_pair_random_scales(lib):
+    rng = np.random.default_rng(33)
+    N, K = 768, 1024
+    seg = [5, 260, 0, 640, 1]
+    offsets, M_cap, mi = _pair_contig_layout(seg)
+    A, B = rand_codes(rng, (M_cap, K)), rand_codes(rng, (len(seg), N, K))
+    sA = np.exp(rng.uniform(-6, 2, (K // 128, M_cap))).astype(np.float32)
+    sB = np.exp(rng.uniform(-6, 2, (len(seg), N // 128, K // 128))).astype(np.float32)
+    got, st = _contig(lib, A, sA, B, sB, offsets, mi, flags=lib.MOE_GEMM_CTA_PAIR)
+    assert st == 0
+    ref, valid = oracle.gemm_contig(A, sA, B, sB, offsets, mi)
+    check_tol(got[valid], ref[valid], "pair contig random")
+    assert (got[~valid] == SENTINEL_BF16).all()
+    # masked layout, counts around the 256-row pair block
+    E, max_m = 4, 640
+    counts = [1, 256, 0, 513]
+    A, B = rand_codes(rng, (E, max_m, K)), rand_codes(rng, (E, N, K))
+    sA = np.exp(rng.uniform(-8, 2, (E, K // 128, max_m))).astype(np.float32)
+    sB = np.exp(rng.uniform(-8, 2, (E, N // 128, K // 128))).astype(np.float32)
+    got, st = _masked(lib, A, sA, B, sB, counts, flags=lib.MOE_GEMM_FORCE_TOKENS_M | lib.MOE_GEMM_CTA_PAIR)
+    assert st == 0
+    ref, valid = oracle.gemm_masked(A, sA, B, sB, counts)
+    _check_masked(got, ref, valid, "pair masked random")
