@@ -96,7 +96,7 @@ def test_contig_bound_and_workspace_plan(so):
 def test_register_split_kernels_compile_to_the_launch_budget(tmp_path):
     """The GEMM kernels that hand registers between warpgroups with setmaxnreg
     are only safe when they launch with exactly the register count the split
-    was computed for: weights-as-M<256> and both tokens-as-M kernels, 384
+    was computed for: weights-as-M<256> and the three tokens-as-M kernels, 384
     threads, 128*40 + 256*232 = 384*168.  Compile gemm.cu and read ptxas's
     register report (the library also re-checks at launch)."""
     import shutil
@@ -123,6 +123,6 @@ def test_register_split_kernels_compile_to_the_launch_budget(tmp_path):
             assert int(m.group(1)) <= 64, f"{current} spills {m.group(1)} bytes"
     tok = [k for k in report if "tokens_m" in k]
     wm = [k for k in report if "weights_m_kernelILi256" in k]
-    assert len(tok) == 2 and len(wm) == 1      # tokens-as-M plain + fused SwiGLU, weights-as-M<256>
+    assert len(tok) == 3 and len(wm) == 1      # tokens-as-M plain, fused SwiGLU, CTA pair; weights-as-M<256>
     for k in tok + wm:
         assert report[k] == 168, (k, report[k])
