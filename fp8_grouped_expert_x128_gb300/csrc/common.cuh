@@ -406,16 +406,35 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& u, float (&f)[8]) {
   }
 }
 
-// Quantise 8 values with scale s into 8 E4M3 bytes (element 0 in the low byte).
+// x / s rounded to nearest-even for a finite, positive, normal s, given
+// r = 1/s rounded to nearest: the product y = x*r is corrected once by the
+// residual x - y*s, the final step of correctly rounded division by a known
+// reciprocal in P. Markstein, "IA-64 and Elementary Functions" (2000).  A zero
+// quotient takes x's sign, as the quotient itself would.  Every element of a
+// 1x128 block divides by the same scale, so the reciprocal is taken once.
+__device__ __forceinline__ float div_rn_by(float x, float s, float r) {
+  const float y = x * r;
+  const float e = fmaf(-y, s, x);
+  return copysignf(fmaf(e, r, y), x);
+}
+
+// Quantise 8 values with scale s into 8 E4M3 bytes (element 0 in the low byte):
+// q = e4m3(x / s), the division correctly rounded in float32.
 __device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
+  float q[8];
+  if (isfinite(s)) {
+    const float r = __frcp_rn(s);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = div_rn_by(f[i], s, r);
+  } else {  // only from non-finite inputs
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(f[i], s);
+  }
   uint32_t lo = 0, hi = 0;
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const uint32_t a = e4m3x2_rn_satfinite(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
-    const uint32_t b =
-        e4m3x2_rn_satfinite(__fdiv_rn(f[4 + 2 * i], s), __fdiv_rn(f[4 + 2 * i + 1], s));
-    lo |= a << (16 * i);
-    hi |= b << (16 * i);
+    lo |= e4m3x2_rn_satfinite(q[2 * i], q[2 * i + 1]) << (16 * i);
+    hi |= e4m3x2_rn_satfinite(q[4 + 2 * i], q[4 + 2 * i + 1]) << (16 * i);
   }
   return make_uint2(lo, hi);
 }

@@ -23,6 +23,8 @@ namespace {
 
 constexpr int kIdxThreads = 1024;
 constexpr int kIdxWarps = kIdxThreads / 32;
+constexpr int kIdxPer = 4;  // assignments per thread per ranking chunk
+static_assert(kIdxWarps == 32, "the scan over warps runs one warp lane per warp");
 constexpr int kMaxExperts = 1024;
 constexpr size_t kIdxSmemLimit = 200 * 1024;
 
@@ -59,8 +61,22 @@ __global__ void __launch_bounds__(kIdxThreads) permute_index_kernel(IndexParams 
 
   // 1. stage ids, histogram (order-free; one atomic per distinct expert per warp)
   for (int e = tid; e < E; e += kIdxThreads) cnt[e] = 0;
-  if (ids_in_smem)
-    for (int64_t i = tid; i < p.n_assign; i += kIdxThreads) ids[i] = p.topk_ids[i];
+  if (ids_in_smem) {
+    // eight loads in flight per thread before their shared-memory stores
+    for (int64_t i0 = 0; i0 < p.n_assign; i0 += 8 * kIdxThreads) {
+      int32_t v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int64_t i = i0 + j * kIdxThreads + tid;
+        v[j] = i < p.n_assign ? __ldg(p.topk_ids + i) : 0;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int64_t i = i0 + j * kIdxThreads + tid;
+        if (i < p.n_assign) ids[i] = v[j];
+      }
+    }
+  }
   __syncthreads();
   for (int64_t c0 = 0; c0 < p.n_assign; c0 += kIdxThreads) {
     const int64_t i = c0 + tid;
@@ -101,40 +117,65 @@ __global__ void __launch_bounds__(kIdxThreads) permute_index_kernel(IndexParams 
   for (int e = tid; e < E; e += kIdxThreads) cnt[e] = 0;  // becomes the running rank
   __syncthreads();
 
-  // 3. ranks in ascending assignment order, chunk by chunk
-  for (int64_t c0 = 0; c0 < p.n_assign; c0 += kIdxThreads) {
-    const int64_t i = c0 + tid;
-    const int e = i < p.n_assign ? local_expert(i) : -1;
+  // 3. ranks in ascending assignment order, in chunks of kIdxThreads * kIdxPer:
+  //    warp w owns the chunk's assignments [w, w+1) * 32 * kIdxPer, visited in
+  //    kIdxPer rounds of 32 consecutive ones.
+  const uint32_t lanes_below = (1u << lane) - 1u;
+  for (int64_t c0 = 0; c0 < p.n_assign; c0 += static_cast<int64_t>(kIdxThreads) * kIdxPer) {
     for (int x = tid; x < kIdxWarps * E; x += kIdxThreads) wc[x] = 0;
     __syncthreads();
-    const uint32_t same = __match_any_sync(0xffffffffu, e);
-    const int rank_in_warp = __popc(same & ((1u << lane) - 1u));
-    if (e >= 0 && rank_in_warp == 0) wc[warp * E + e] = __popc(same);
-    __syncthreads();
-    for (int ee = tid; ee < E; ee += kIdxThreads) {  // exclusive scan over warps
-      int run = cnt[ee];
-      for (int w = 0; w < kIdxWarps; ++w) {
-        const int v = wc[w * E + ee];
-        wc[w * E + ee] = run;
-        run += v;
-      }
-      cnt[ee] = run;
+    // (a) per-warp count of each expert, and each assignment's rank in its warp
+    int e_r[kIdxPer], rk_r[kIdxPer];
+#pragma unroll
+    for (int r = 0; r < kIdxPer; ++r) {
+      const int64_t i = c0 + (static_cast<int64_t>(warp) * kIdxPer + r) * 32 + lane;
+      const int e = i < p.n_assign ? local_expert(i) : -1;
+      const uint32_t same = __match_any_sync(0xffffffffu, e);
+      const int lower = __popc(same & lanes_below);
+      const int before = e >= 0 ? wc[warp * E + e] : 0;   // this expert in earlier rounds
+      __syncwarp();
+      if (e >= 0 && lower == 0) wc[warp * E + e] = before + __popc(same);
+      __syncwarp();
+      e_r[r] = e;
+      rk_r[r] = before + lower;
     }
     __syncthreads();
-    if (e >= 0) {
-      const int rank = wc[warp * E + e] + rank_in_warp;
-      int32_t dst = -1;
-      if (p.layout == MOE_LAYOUT_CONTIG || rank < p.max_m) {
-        const int64_t row = static_cast<int64_t>(base[e]) + rank;
-        if (row < map_rows) {
-          dst = static_cast<int32_t>(row);
-          p.row_src[row] = static_cast<int32_t>(i);
-          if (p.layout == MOE_LAYOUT_CONTIG) p.m_indices[row] = e;
-        }
+    // (b) per expert, exclusive scan over the warps (lane = warp), on top of
+    //     the running count of earlier chunks
+    for (int ee = warp; ee < E; ee += kIdxWarps) {
+      const int v = wc[lane * E + ee];
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
       }
-      p.dst_row[i] = dst;
-    } else if (i < p.n_assign) {
-      p.dst_row[i] = -1;
+      const int run = cnt[ee];
+      __syncwarp();
+      wc[lane * E + ee] = run + incl - v;
+      if (lane == 31) cnt[ee] = run + incl;
+    }
+    __syncthreads();
+    // (c) destinations
+#pragma unroll
+    for (int r = 0; r < kIdxPer; ++r) {
+      const int64_t i = c0 + (static_cast<int64_t>(warp) * kIdxPer + r) * 32 + lane;
+      const int e = e_r[r];
+      if (e >= 0) {
+        const int rank = wc[warp * E + e] + rk_r[r];
+        int32_t dst = -1;
+        if (p.layout == MOE_LAYOUT_CONTIG || rank < p.max_m) {
+          const int64_t row = static_cast<int64_t>(base[e]) + rank;
+          if (row < map_rows) {
+            dst = static_cast<int32_t>(row);
+            p.row_src[row] = static_cast<int32_t>(i);
+            if (p.layout == MOE_LAYOUT_CONTIG) p.m_indices[row] = e;
+          }
+        }
+        p.dst_row[i] = dst;
+      } else if (i < p.n_assign) {
+        p.dst_row[i] = -1;
+      }
     }
     __syncthreads();
   }
@@ -162,27 +203,31 @@ __global__ void __launch_bounds__(128) permute_scatter_kernel(
   for (int64_t kb = lane; kb < KB; kb += 32) s_out[(grp * KB + kb) * G + pos] = __ldg(s + kb * s_ld + t);
 }
 
-// Fused 1x128 quantisation + scatter for moe_ffn: one CTA per routed row; its
-// kQsWarps warps share the row's 128-column block pairs (a half-warp per
-// block), loads issued before use, and quantise the token's bf16 row straight
-// into its expert slot (the bytes equal moe_quant_fp8 followed by moe_permute:
-// same helpers, same arithmetic).  Non-local assignments leave at once.
-constexpr int kQsWarps = 8;
-constexpr int kQsPairs = 4;  // block pairs per warp per pass (H up to 8192 in one pass)
+// Fused 1x128 quantisation + scatter for moe_ffn: one resident wave of CTAs
+// walks the assignments (grid stride), skipping non-local ones; for a routed
+// row the CTA's kQsWarps warps share its 128-column block pairs (a half-warp
+// per block), loads issued before use, and quantise the token's bf16 row
+// straight into its expert slot (the bytes equal moe_quant_fp8 followed by
+// moe_permute: same helpers, same arithmetic).
+// Small CTAs with a whole row's loads in flight: at H = 7168 a CTA's 4 warps
+// issue all 28 block pairs (14 KB) before quantising, and ~9 CTAs fit per SM.
+constexpr int kQsWarps = 4;
+constexpr int kQsPairs = 7;  // block pairs per warp per pass (H up to 7168 in one pass)
 
-__global__ void __launch_bounds__(32 * kQsWarps) quant_scatter_kernel(
+__global__ void __launch_bounds__(32 * kQsWarps, 6) quant_scatter_kernel(
     const uint16_t* __restrict__ x, int64_t ldx, const int32_t* __restrict__ dst_row,
     int64_t n_assign, int32_t k, int64_t H, uint8_t* __restrict__ q_out, float* __restrict__ s_out,
     int64_t G) {
   grid_dependency_wait();
   grid_launch_dependents();
-  const int64_t i = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (i >= n_assign) return;
-  const int32_t dst = __ldg(dst_row + i);
-  if (dst < 0) return;
-  const int64_t t = i / k;
   const int64_t KB = H / 128, NP = (KB + 1) / 2;
+  int32_t dst_next = blockIdx.x < n_assign ? __ldg(dst_row + blockIdx.x) : -1;
+  for (int64_t i = blockIdx.x; i < n_assign; i += gridDim.x) {
+  const int32_t dst = dst_next;   // the next destination is read before this row's work
+  dst_next = i + gridDim.x < n_assign ? __ldg(dst_row + i + gridDim.x) : -1;
+  if (dst < 0) continue;
+  const int64_t t = i / k;
   const int64_t grp = dst / G, pos = dst - grp * G;
   const uint16_t* xr = x + t * ldx;
   uint8_t* qr = q_out + static_cast<int64_t>(dst) * H;
@@ -209,6 +254,7 @@ __global__ void __launch_bounds__(32 * kQsWarps) quant_scatter_kernel(
         if ((lane & 15) == 0) s_out[(grp * KB + kb) * G + pos] = sc;
       }
     }
+  }
   }
 }
 
@@ -352,9 +398,19 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
   if (T == 0) return MOE_OK;
   const int64_t n = T * k;
   const unsigned grid = static_cast<unsigned>((n + 3) / 4);
-  if (x != nullptr)
-    return launch_pdl(quant_scatter_kernel, static_cast<unsigned>(n), 32 * kQsWarps, 0, st, x, ldx,
-                      dst_row, n, k, H, q_out, s_out, G);
+  if (x != nullptr) {
+    static int per_sm[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    if (per_sm[dev] == 0 &&
+        (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[dev], quant_scatter_kernel, 32 * kQsWarps, 0) !=
+             cudaSuccess ||
+         per_sm[dev] < 1))
+      return MOE_ERR_CUDA;
+    const int64_t wave = static_cast<int64_t>(num_sms()) * per_sm[dev];
+    return launch_pdl(quant_scatter_kernel, static_cast<unsigned>(n < wave ? n : wave), 32 * kQsWarps, 0,
+                      st, x, ldx, dst_row, n, k, H, q_out, s_out, G);
+  }
   return launch_pdl(permute_scatter_kernel, grid, 128, 0, st, q, s, s_ld, dst_row, n, k, H, q_out,
                     s_out, G);
 }

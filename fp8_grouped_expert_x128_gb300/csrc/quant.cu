@@ -96,8 +96,10 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(
     float* __restrict__ s, int64_t G) {
   grid_dependency_wait();
   grid_launch_dependents();
+  // a warp covers blocks 4w + h and 4w + h + 2 of one row (h = its half), with
+  // all four 16-byte loads (g and u of both blocks) issued before any use
   const int64_t KB = I / 128;
-  const int64_t warps_per_row = (KB + 1) / 2;
+  const int64_t warps_per_row = (KB + 3) / 4;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t r = gw / warps_per_row;
@@ -108,28 +110,41 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(
   } else if (m_indices != nullptr) {
     if (__ldg(m_indices + r) < 0) return;
   }
-  const int64_t kb = (gw % warps_per_row) * 2 + (lane >> 4);
-  const bool active = kb < KB;
-  float h[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  const int64_t col = kb * 128 + (lane & 15) * 8;
-  if (active) {
-    const uint16_t* row = y1 + r * 2 * I;
-    float g[8], u[8];
-    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(row + col)), g);
-    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(row + I + col)), u);
+  const int64_t kb0 = (gw % warps_per_row) * 4 + (lane >> 4);
+  const uint16_t* row = y1 + r * 2 * I;
+  uint4 gv[2], uv[2];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) h[i] = __fdiv_rn(g[i], 1.0f + expf(-g[i])) * u[i];
+  for (int j = 0; j < 2; ++j) {
+    const int64_t kb = kb0 + 2 * j;
+    const int64_t col = kb * 128 + (lane & 15) * 8;
+    gv[j] = kb < KB ? __ldg(reinterpret_cast<const uint4*>(row + col)) : make_uint4(0, 0, 0, 0);
+    uv[j] = kb < KB ? __ldg(reinterpret_cast<const uint4*>(row + I + col)) : make_uint4(0, 0, 0, 0);
   }
-  float amax = 0.f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(h[i]));
-  amax = half_warp_max(amax);
-  if (!active) return;
-  const float sc = block_scale(amax);
-  *reinterpret_cast<uint2*>(q + r * I + col) = quant8(h, sc);
-  if ((lane & 15) == 0) {
-    const int64_t grp = r / G, pos = r - grp * G;
-    s[(grp * KB + kb) * G + pos] = sc;
+  for (int j = 0; j < 2; ++j) {
+    const int64_t kb = kb0 + 2 * j;
+    const bool active = kb < KB;
+    const int64_t col = kb * 128 + (lane & 15) * 8;
+    float h[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (active) {
+      float g[8], u[8];
+      unpack_bf16x8(gv[j], g);
+      unpack_bf16x8(uv[j], u);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) h[i] = __fdiv_rn(g[i], 1.0f + expf(-g[i])) * u[i];
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(h[i]));
+    amax = half_warp_max(amax);
+    if (active) {
+      const float sc = block_scale(amax);
+      *reinterpret_cast<uint2*>(q + r * I + col) = quant8(h, sc);
+      if ((lane & 15) == 0) {
+        const int64_t grp = r / G, pos = r - grp * G;
+        s[(grp * KB + kb) * G + pos] = sc;
+      }
+    }
   }
 }
 
@@ -184,7 +199,7 @@ extern "C" int moe_swiglu_quant(const uint16_t* Y1, int64_t rows, int32_t I, con
     G = s_ld;
   }
   if (int st = check_device()) return st;
-  const int64_t warps = rows * ((I / 128 + 1) / 2);
+  const int64_t warps = rows * ((I / 128 + 3) / 4);
   return launch_pdl(swiglu_quant_kernel, grid_for_warps(warps), 256, 0, as_stream(stream), Y1,
                     rows, static_cast<int64_t>(I), counts, static_cast<int64_t>(max_m),
                     counts ? nullptr : m_indices, q, s, G);

@@ -59,6 +59,37 @@ def test_quant_every_bf16_value(lib):
     assert np.array_equal(q, ref)
 
 
+def test_quant_division_every_bf16_under_many_scales(lib):
+    # The quotient x / s must be the correctly rounded float32 division for every
+    # scale: 48 block maxima spread over the exponent range with random
+    # mantissas give 48 scales s = fp32(amax / 448); each block pairs its
+    # maximum with every finite bf16 value of smaller magnitude, both signs.
+    rng = np.random.default_rng(41)
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    allv = oracle.bf16_decode(allbits)
+    fin = np.isfinite(allv)
+    exps = rng.integers(-20, 100, 48)
+    mants = rng.integers(0, 128, 48)
+    mants[:4] = [0, 127, 64, 1]
+    blocks = []
+    for e, m in zip(exps, mants):
+        amax_bits = np.uint16(((int(e) + 127) << 7) | int(m))
+        amax = float(oracle.bf16_decode(np.array([amax_bits]))[0])
+        vals = allbits[fin & (np.abs(allv) <= amax)]
+        nb = -(-vals.size // 127)
+        b = np.zeros((nb, 128), np.uint16)
+        b[:, 0] = amax_bits
+        flat = np.zeros(nb * 127, np.uint16)
+        flat[:vals.size] = vals
+        b[:, 1:] = flat.reshape(nb, 127)
+        blocks.append(b)
+    blocks = np.concatenate(blocks)
+    pad = (-blocks.shape[0]) % 4
+    blocks = np.concatenate([blocks, np.zeros((pad, 128), np.uint16)])
+    xb = blocks.reshape(-1, 512)
+    _assert_quant_equal(lib, xb)
+
+
 def test_quant_edge_cases(lib):
     rng = np.random.default_rng(5)
     M, K = 37, 384                     # M not a multiple of 4, three blocks
