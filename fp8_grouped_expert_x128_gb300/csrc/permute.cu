@@ -209,12 +209,12 @@ __global__ void __launch_bounds__(128) permute_scatter_kernel(
 // per block), loads issued before use, and quantise the token's bf16 row
 // straight into its expert slot (the bytes equal moe_quant_fp8 followed by
 // moe_permute: same helpers, same arithmetic).
-// Small CTAs with a whole row's loads in flight: at H = 7168 a CTA's 4 warps
-// issue all 28 block pairs (14 KB) before quantising, and ~9 CTAs fit per SM.
-constexpr int kQsWarps = 4;
-constexpr int kQsPairs = 7;  // block pairs per warp per pass (H up to 7168 in one pass)
-
-__global__ void __launch_bounds__(32 * kQsWarps, 6) quant_scatter_kernel(
+// Two shapes, both with a whole row's loads in flight (H <= 7168 in one pass):
+// many routed rows (prefill) take 4-warp CTAs, 7 block pairs per warp, ~6
+// CTAs per SM for the bytes in flight; a few hundred rows (decode) take
+// 8-warp CTAs, 4 pairs per warp, so each row finishes sooner.
+template <int kQsWarps, int kQsPairs>
+__global__ void __launch_bounds__(32 * kQsWarps, kQsWarps == 4 ? 6 : 4) quant_scatter_kernel(
     const uint16_t* __restrict__ x, int64_t ldx, const int32_t* __restrict__ dst_row,
     int64_t n_assign, int32_t k, int64_t H, uint8_t* __restrict__ q_out, float* __restrict__ s_out,
     int64_t G) {
@@ -258,10 +258,12 @@ __global__ void __launch_bounds__(32 * kQsWarps, 6) quant_scatter_kernel(
   }
 }
 
-// One CTA per token.  The token's valid routing slots are compacted first
-// (order kept); then for each slot a thread issues all of its 16-byte row loads
-// (kCombVec chunks of 8 columns, strided by the block) before accumulating, so
-// the loads of one token overlap instead of running one after another.
+// A resident wave of CTAs walks the tokens (grid stride), one token at a
+// time per CTA.  Warp 0 holds the token's routing slots: it compacts the valid
+// ones (order kept) into shared memory and, while the CTA works on this token,
+// already loads the next token's slots, so only the row loads sit on the
+// per-token path.  For each slot a thread issues all of its 16-byte row loads
+// (kCombVec chunks of 8 columns, strided by the block) before accumulating.
 // Accumulation per element is fp32 fmaf in slot order.
 constexpr int kCombThreads = 128;
 constexpr int kCombVec = 8;
@@ -269,72 +271,84 @@ constexpr int kCombVec = 8;
 __global__ void __launch_bounds__(kCombThreads) combine_kernel(
     const uint16_t* __restrict__ y2, int64_t ldy, int64_t y_rows, const int32_t* __restrict__ dst_row,
     const float* __restrict__ topk_w, int32_t k, int64_t H, uint16_t* __restrict__ out, int64_t ldo,
-    int32_t* err) {
+    int64_t T, int32_t* err) {
   grid_dependency_wait();
   grid_launch_dependents();
   __shared__ int32_t s_dst[32];
   __shared__ float s_w[32];
   __shared__ int s_n;
-  const int64_t t = blockIdx.x;
   const int tid = threadIdx.x;
-  if (tid < 32) {
-    int32_t d = -1;
-    float w = 0.f;
-    if (tid < k) {
-      d = dst_row[t * k + tid];
+  int32_t d_next = -1;
+  float w_next = 0.f;
+  if (tid < k && blockIdx.x < T) {
+    d_next = __ldg(dst_row + static_cast<int64_t>(blockIdx.x) * k + tid);
+    w_next = __ldg(topk_w + static_cast<int64_t>(blockIdx.x) * k + tid);
+  }
+  for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+    if (tid < 32) {
+      int32_t d = d_next;
+      const float w = w_next;
       if (d >= y_rows) {
         set_err(err, MOE_DEV_BAD_INDEX);
         d = -1;
       }
-      w = topk_w[t * k + tid];
+      const uint32_t valid = __ballot_sync(0xffffffffu, d >= 0);
+      if (d >= 0) {
+        const int slot = __popc(valid & ((1u << tid) - 1u));
+        s_dst[slot] = d;
+        s_w[slot] = w;
+      }
+      if (tid == 0) s_n = __popc(valid);
+      // the next token's slots load while this one is combined
+      const int64_t tn = t + gridDim.x;
+      d_next = -1;
+      w_next = 0.f;
+      if (tid < k && tn < T) {
+        d_next = __ldg(dst_row + tn * k + tid);
+        w_next = __ldg(topk_w + tn * k + tid);
+      }
     }
-    const uint32_t valid = __ballot_sync(0xffffffffu, d >= 0);
-    if (d >= 0) {
-      const int slot = __popc(valid & ((1u << tid) - 1u));
-      s_dst[slot] = d;
-      s_w[slot] = w;
-    }
-    if (tid == 0) s_n = __popc(valid);
-  }
-  __syncthreads();
-  const int n = s_n;
-  for (int64_t base = 0; base < H; base += static_cast<int64_t>(kCombThreads) * 8 * kCombVec) {
-    float acc[kCombVec][8];
+    __syncthreads();
+    const int n = s_n;
+    for (int64_t base = 0; base < H; base += static_cast<int64_t>(kCombThreads) * 8 * kCombVec) {
+      float acc[kCombVec][8];
 #pragma unroll
-    for (int v = 0; v < kCombVec; ++v)
+      for (int v = 0; v < kCombVec; ++v)
 #pragma unroll
-      for (int h = 0; h < 8; ++h) acc[v][h] = 0.f;
-    for (int jj = 0; jj < n; ++jj) {
-      const uint16_t* row = y2 + static_cast<int64_t>(s_dst[jj]) * ldy;
-      const float w = s_w[jj];
-      uint4 u[kCombVec];
+        for (int h = 0; h < 8; ++h) acc[v][h] = 0.f;
+      for (int jj = 0; jj < n; ++jj) {
+        const uint16_t* row = y2 + static_cast<int64_t>(s_dst[jj]) * ldy;
+        const float w = s_w[jj];
+        uint4 u[kCombVec];
+#pragma unroll
+        for (int v = 0; v < kCombVec; ++v) {
+          const int64_t c = base + (static_cast<int64_t>(v) * kCombThreads + tid) * 8;
+          u[v] = c < H ? __ldg(reinterpret_cast<const uint4*>(row + c)) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int v = 0; v < kCombVec; ++v) {
+          const uint32_t x[4] = {u[v].x, u[v].y, u[v].z, u[v].w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            acc[v][2 * h] = fmaf(w, __uint_as_float(x[h] << 16), acc[v][2 * h]);
+            acc[v][2 * h + 1] = fmaf(w, __uint_as_float(x[h] & 0xFFFF0000u), acc[v][2 * h + 1]);
+          }
+        }
+      }
 #pragma unroll
       for (int v = 0; v < kCombVec; ++v) {
         const int64_t c = base + (static_cast<int64_t>(v) * kCombThreads + tid) * 8;
-        u[v] = c < H ? __ldg(reinterpret_cast<const uint4*>(row + c)) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int v = 0; v < kCombVec; ++v) {
-        const uint32_t x[4] = {u[v].x, u[v].y, u[v].z, u[v].w};
+        if (c >= H) continue;
+        uint32_t o[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          acc[v][2 * h] = fmaf(w, __uint_as_float(x[h] << 16), acc[v][2 * h]);
-          acc[v][2 * h + 1] = fmaf(w, __uint_as_float(x[h] & 0xFFFF0000u), acc[v][2 * h + 1]);
+          const __nv_bfloat162 b = __floats2bfloat162_rn(acc[v][2 * h], acc[v][2 * h + 1]);
+          o[h] = *reinterpret_cast<const uint32_t*>(&b);
         }
+        *reinterpret_cast<uint4*>(out + t * ldo + c) = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
-#pragma unroll
-    for (int v = 0; v < kCombVec; ++v) {
-      const int64_t c = base + (static_cast<int64_t>(v) * kCombThreads + tid) * 8;
-      if (c >= H) continue;
-      uint32_t o[4];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[v][2 * h], acc[v][2 * h + 1]);
-        o[h] = *reinterpret_cast<const uint32_t*>(&b);
-      }
-      *reinterpret_cast<uint4*>(out + t * ldo + c) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
+    __syncthreads();   // s_dst / s_w / s_n are rewritten for the next token
   }
 }
 
@@ -399,17 +413,19 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
   const int64_t n = T * k;
   const unsigned grid = static_cast<unsigned>((n + 3) / 4);
   if (x != nullptr) {
-    static int per_sm[64] = {0};
+    // many rows: throughput shape; decode batches: latency shape
+    const bool many = T >= 16384;
+    auto kern = many ? quant_scatter_kernel<4, 7> : quant_scatter_kernel<8, 4>;
+    const int threads = many ? 128 : 256;
+    static int per_sm[2][64] = {{0}};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-    if (per_sm[dev] == 0 &&
-        (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[dev], quant_scatter_kernel, 32 * kQsWarps, 0) !=
-             cudaSuccess ||
-         per_sm[dev] < 1))
+    int& occ = per_sm[many ? 1 : 0][dev];
+    if (occ == 0 && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, 0) != cudaSuccess || occ < 1))
       return MOE_ERR_CUDA;
-    const int64_t wave = static_cast<int64_t>(num_sms()) * per_sm[dev];
-    return launch_pdl(quant_scatter_kernel, static_cast<unsigned>(n < wave ? n : wave), 32 * kQsWarps, 0,
-                      st, x, ldx, dst_row, n, k, H, q_out, s_out, G);
+    const int64_t wave = static_cast<int64_t>(num_sms()) * occ;
+    return launch_pdl(kern, static_cast<unsigned>(n < wave ? n : wave), threads, 0, st, x, ldx, dst_row, n, k,
+                      static_cast<int64_t>(H), q_out, s_out, G);
   }
   return launch_pdl(permute_scatter_kernel, grid, 128, 0, st, q, s, s_ld, dst_row, n, k, H, q_out,
                     s_out, G);
@@ -437,6 +453,15 @@ extern "C" int moe_combine(const uint16_t* Y2, int64_t ldy, int64_t y_rows, cons
   MOE_CHECK_ARG(ldy >= H && ldy % 8 == 0 && ldo >= H && ldo % 8 == 0 && y_rows >= 0);
   MOE_CHECK_ARG(T < (1ll << 31));
   if (int st = check_device()) return st;
-  return launch_pdl(combine_kernel, static_cast<unsigned>(T), kCombThreads, 0, as_stream(stream), Y2,
-                    ldy, y_rows, dst_row, topk_w, k, static_cast<int64_t>(H), out, ldo, err);
+  static int per_sm[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  if (per_sm[dev] == 0 &&
+      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[dev], combine_kernel, kCombThreads, 0) != cudaSuccess ||
+       per_sm[dev] < 1))
+    return MOE_ERR_CUDA;
+  const int64_t wave = static_cast<int64_t>(num_sms()) * per_sm[dev];
+  return launch_pdl(combine_kernel, static_cast<unsigned>(T < wave ? T : wave), kCombThreads, 0,
+                    as_stream(stream), Y2, ldy, y_rows, dst_row, topk_w, k, static_cast<int64_t>(H), out, ldo, T,
+                    err);
 }

@@ -187,6 +187,23 @@ CONFIGS = {
         shared_expert=True,
         description="single-GPU decode layer: 256 routed experts + 1 shared, T=64, top-8 "
                     "from softmax of N(0,1) logits, masked layout"),
+    # small-batch / latency regime of the same layer: 1, 4 or 16 tokens per
+    # step (one decode token, multi-token-prediction-like drafts)
+    "c5t1": MoEConfig(
+        "c5t1_all_experts_decode_T1", 5, E=257, H=7168, I=2048, layout="masked", max_m=16, T=1, topk=8,
+        shared_expert=True,
+        description="single-GPU decode layer, latency regime: 256 routed experts + 1 shared, "
+                    "T=1, top-8 from softmax of N(0,1) logits, masked max_m=16"),
+    "c5t4": MoEConfig(
+        "c5t4_all_experts_decode_T4", 6, E=257, H=7168, I=2048, layout="masked", max_m=16, T=4, topk=8,
+        shared_expert=True,
+        description="single-GPU decode layer, latency regime: 256 routed experts + 1 shared, "
+                    "T=4, top-8 from softmax of N(0,1) logits, masked max_m=16"),
+    "c5t16": MoEConfig(
+        "c5t16_all_experts_decode_T16", 7, E=257, H=7168, I=2048, layout="masked", max_m=16, T=16, topk=8,
+        shared_expert=True,
+        description="single-GPU decode layer, latency regime: 256 routed experts + 1 shared, "
+                    "T=16, top-8 from softmax of N(0,1) logits, masked max_m=16"),
 }
 
 

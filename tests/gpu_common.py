@@ -69,6 +69,21 @@ def check_tol(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = ""):
 CHAIN_FRAC = 1e-3
 
 
+def e4m3_flip_step(q2: np.ndarray, s2_cols: np.ndarray) -> np.ndarray:
+    """Per element of h: the larger gap from its E4M3 code to a neighbouring
+    code, times the element's block scale (s2_cols: the scale of each column)."""
+    mag = (q2 & 0x7F).astype(np.int64)
+    here = oracle.e4m3_decode(mag.astype(np.uint8))
+    up = np.abs(oracle.e4m3_decode(np.minimum(mag + 1, 0x7E).astype(np.uint8)) - here)
+    dn = np.abs(here - oracle.e4m3_decode(np.maximum(mag - 1, 0).astype(np.uint8)))
+    return np.maximum(up, dn) * s2_cols
+
+
+def w2_colmax(w2q_e: np.ndarray, w2s_e: np.ndarray) -> np.ndarray:
+    """max_i |W2[n, i]| of one expert's dequantised W2, per output column n."""
+    return np.abs(oracle.e4m3_decode(w2q_e) * np.repeat(np.repeat(w2s_e, 128, 0), 128, 1)).max(axis=1)
+
+
 def flip_bound(ref: dict, topk_w: np.ndarray, w2q: np.ndarray, w2s: np.ndarray) -> np.ndarray:
     """Oracle-side bound [T, H] on how far one E4M3 flip of h per routed row can
     move each output: sum_j w_j * max_i(step(q2[r_j, i]) * s2[r_j, i]) * max_i |W2[e_j][n, i]|,
@@ -80,14 +95,10 @@ def flip_bound(ref: dict, topk_w: np.ndarray, w2q: np.ndarray, w2s: np.ndarray) 
     s2 = ref["s2"]
     if s2.ndim == 3:                                     # masked [E, KB, max_m] -> [KB, rows]
         s2 = s2.transpose(1, 0, 2).reshape(KB2, -1)
-    mag = (q2 & 0x7F).astype(np.int64)
-    up = np.abs(oracle.e4m3_decode(np.minimum(mag + 1, 0x7E).astype(np.uint8)) - oracle.e4m3_decode(mag.astype(np.uint8)))
-    dn = np.abs(oracle.e4m3_decode(mag.astype(np.uint8)) - oracle.e4m3_decode(np.maximum(mag - 1, 0).astype(np.uint8)))
-    step = np.maximum(up, dn) * np.repeat(s2.T, 128, axis=1)          # [rows, I]
+    step = e4m3_flip_step(q2, np.repeat(s2.T, 128, axis=1))          # [rows, I]
     rowflip = np.where(rows_valid, step.max(axis=1), 0.0)             # [rows]
     E = w2q.shape[0]
-    colmax = np.stack([np.abs(oracle.e4m3_decode(w2q[e]) * np.repeat(np.repeat(w2s[e], 128, 0), 128, 1)).max(axis=1)
-                       for e in range(E)])                            # [E, H]
+    colmax = np.stack([w2_colmax(w2q[e], w2s[e]) for e in range(E)])  # [E, H]
     dst = ref["perm"]["dst_row"].reshape(topk_w.shape)
     T, k = topk_w.shape
     rows_per_e = rows_valid.size // E if ref["perm"].get("offsets") is None else None

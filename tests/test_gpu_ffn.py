@@ -13,8 +13,8 @@ import torch
 import oracle
 import synth
 from bench import build_workload, make_desc
-from tests.gpu_common import (bits, check_swiglu, check_tol, check_tol_chain, flip_bound,
-                              from_bits, oracle_weights, to_dev, u8)
+from tests.gpu_common import (bits, check_swiglu, check_tol, check_tol_chain, e4m3_flip_step,
+                              flip_bound, from_bits, oracle_weights, to_dev, u8, w2_colmax)
 
 pytestmark = pytest.mark.gpu
 
@@ -41,7 +41,8 @@ def _oracle_full(name, wl):
 
 
 def _oracle_tokens(name, wl, tokens):
-    """The oracle chain restricted to `tokens` (rows are independent)."""
+    """The oracle chain restricted to `tokens` (rows are independent), and the
+    end-to-end allowance of one E4M3 flip of h per routed row (as flip_bound)."""
     cfg = wl["cfg"]
     r = wl["routing"]
     xb = bits(wl["x"])[tokens]
@@ -51,9 +52,11 @@ def _oracle_tokens(name, wl, tokens):
     w13q, w13s = oracle_weights(name, "w13", need)
     w2q, w2s = oracle_weights(name, "w2", need)
     slot = {e: i for i, e in enumerate(need)}
-    out = []
+    colmax = {}
+    out, extra = [], []
     for i, t in enumerate(tokens):
         y2, w = [], []
+        flip = np.zeros(cfg.H)
         for j in range(r["k"]):
             e = int(r["topk_ids"][t, j]) - r["expert_begin"]
             if not 0 <= e < cfg.E:
@@ -63,8 +66,13 @@ def _oracle_tokens(name, wl, tokens):
             q2, s2 = oracle.swiglu_quant(y1)
             y2.append(oracle.bf16_encode(oracle.gemm_block_scaled(q2, s2, w2q[n], w2s[n]))[0])
             w.append(float(r["topk_w"][t, j]))
+            if n not in colmax:
+                colmax[n] = w2_colmax(w2q[n], w2s[n])
+            rowflip = e4m3_flip_step(q2[0], np.repeat(s2[:, 0], 128)).max()
+            flip += w[-1] * rowflip * colmax[n]
         out.append(oracle.combine(np.stack(y2), np.arange(len(w)), np.array([w], np.float32))[0])
-    return np.stack(out)
+        extra.append(flip)
+    return np.stack(out), np.stack(extra)
 
 
 def test_ffn_tiny_config_end_to_end(lib):
@@ -130,7 +138,22 @@ def test_ffn_all_experts_layer_sampled_tokens(lib):
     got, st = _gpu_ffn(lib, wl)
     assert st == 0
     tokens = [0, 63]
-    check_tol(got[tokens], _oracle_tokens("c5", wl, tokens), "c5 ffn tokens")
+    ref, extra = _oracle_tokens("c5", wl, tokens)
+    check_tol_chain(got[tokens], ref, extra, "c5 ffn tokens")
+    assert np.isfinite(oracle.bf16_decode(got)).all()
+
+
+@pytest.mark.parametrize("name", ["c5t1", "c5t4", "c5t16"])
+def test_ffn_all_experts_small_batch(lib, name):
+    # the latency regime of the all-experts layer: 1-16 tokens, ~9-100 active
+    # experts, 1-2 rows each (weights-as-M with 16-wide token tiles)
+    wl = build_workload(name)
+    got, st = _gpu_ffn(lib, wl)
+    assert st == 0
+    T = wl["T"]
+    tokens = sorted({0, T - 1})
+    ref, extra = _oracle_tokens(name, wl, tokens)
+    check_tol_chain(got[tokens], ref, extra, f"{name} ffn tokens")
     assert np.isfinite(oracle.bf16_decode(got)).all()
 
 
@@ -144,7 +167,8 @@ def test_ffn_prefill_contiguous_sampled_tokens(lib):
     for e in range(wl["cfg"].E):                 # a few tokens of every expert
         tokens += list(rng.choice(np.nonzero(r["topk_ids"][:, 0] == e)[0], 3, replace=False))
     tokens = sorted(tokens)
-    check_tol(got[tokens], _oracle_tokens("c3", wl, tokens), "c3 ffn tokens")
+    ref, extra = _oracle_tokens("c3", wl, tokens)
+    check_tol_chain(got[tokens], ref, extra, "c3 ffn tokens")
 
 
 @pytest.mark.parametrize("name,fuse", [("c1", False), ("c2", False), ("c3", False), ("c2", True), ("c3", True)])

@@ -40,6 +40,11 @@ def test_routing_recipes():
     c5 = synth.make_routing(synth.get_config("c5"))
     assert c5["topk_ids"].shape == (64, 9) and (c5["topk_ids"][:, 8] == 256).all()
     assert (c5["topk_w"][:, 8] == 1).all() and np.allclose(c5["topk_w"][:, :8].sum(1), 1, atol=1e-6)
+    for name, T in (("c5t1", 1), ("c5t4", 4), ("c5t16", 16)):
+        r = synth.make_routing(synth.get_config(name))
+        assert r["topk_ids"].shape == (T, 9) and (r["topk_ids"][:, 8] == 256).all()
+        counts = np.bincount(r["topk_ids"].reshape(-1), minlength=257)
+        assert counts.max() <= synth.get_config(name).max_m
     for name in ("c2", "c4"):
         cfg = synth.get_config(name)
         r = synth.make_routing(cfg)
