@@ -26,6 +26,7 @@ constexpr int kIdxWarps = kIdxThreads / 32;
 constexpr int kIdxPer = 4;  // assignments per thread per ranking chunk
 static_assert(kIdxWarps == 32, "the scan over warps runs one warp lane per warp");
 constexpr int kMaxExperts = 1024;
+static_assert(kMaxExperts <= kIdxThreads, "one expert per thread in the index pass");
 constexpr size_t kIdxSmemLimit = 200 * 1024;
 
 struct IndexParams {
@@ -86,26 +87,51 @@ __global__ void __launch_bounds__(kIdxThreads) permute_index_kernel(IndexParams 
   }
   __syncthreads();
 
-  // 2. segment bases, counts, offsets; fill row maps with -1
-  if (tid == 0) {
-    int64_t row = 0;
-    bool overflow = false;
-    for (int e = 0; e < E; ++e) {
-      if (p.layout == MOE_LAYOUT_MASKED) {
+  // 2. segment bases, counts, offsets, one expert per thread (E <= kIdxThreads);
+  //    the contiguous offsets are a block-wide exclusive scan of the padded counts
+  {
+    __shared__ int64_t wsum[kIdxWarps];
+    const int e = tid;
+    const int c = e < E ? cnt[e] : 0;
+    if (p.layout == MOE_LAYOUT_MASKED) {
+      if (e < E) {
         base[e] = e * p.max_m;
-        const int c = cnt[e];
-        overflow |= c > p.max_m;
         p.counts[e] = c < p.max_m ? c : p.max_m;
-      } else {
-        base[e] = static_cast<int32_t>(row);
-        p.offsets[e] = static_cast<int32_t>(row);
-        p.counts[e] = cnt[e];
-        row += (cnt[e] + 127) / 128 * 128;
+        if (c > p.max_m) set_err(p.err, MOE_DEV_OVERFLOW);
+      }
+    } else {
+      const int64_t padded = (static_cast<int64_t>(c) + 127) / 128 * 128;
+      int64_t incl = padded;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) wsum[warp] = incl;
+      __syncthreads();
+      if (warp == 0) {
+        const int64_t v = wsum[lane];
+        int64_t w_incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int64_t y = __shfl_up_sync(0xffffffffu, w_incl, o);
+          if (lane >= o) w_incl += y;
+        }
+        wsum[lane] = w_incl - v;   // rows before this warp's experts
+      }
+      __syncthreads();
+      const int64_t excl = wsum[warp] + incl - padded;
+      if (e < E) {
+        base[e] = static_cast<int32_t>(excl);
+        p.offsets[e] = static_cast<int32_t>(excl);
+        p.counts[e] = c;
+      }
+      if (e == E - 1) {
+        const int64_t row = excl + padded;
+        p.offsets[E] = static_cast<int32_t>(row);
+        if (row > p.rows_capacity) set_err(p.err, MOE_DEV_BAD_INDEX);
       }
     }
-    if (p.layout == MOE_LAYOUT_CONTIG) p.offsets[E] = static_cast<int32_t>(row);
-    if (overflow) set_err(p.err, MOE_DEV_OVERFLOW);
-    if (row > p.rows_capacity) set_err(p.err, MOE_DEV_BAD_INDEX);
   }
   __syncthreads();
   const int64_t map_rows =
@@ -352,6 +378,94 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(
   }
 }
 
+// Latency shape for a few tokens (all-experts decode: up to 9 routing slots
+// per token): one CTA of kCombLatThreads per token, each thread owning
+// kCombLatVec chunks of 8 columns, with the row loads of kCombLatSlots slots
+// in flight at once.  Same per-element arithmetic and slot order as above, so
+// the bytes are the same.
+constexpr int kCombLatThreads = 512;
+constexpr int kCombLatVec = 2;
+constexpr int kCombLatSlots = 4;
+
+__global__ void __launch_bounds__(kCombLatThreads) combine_latency_kernel(
+    const uint16_t* __restrict__ y2, int64_t ldy, int64_t y_rows, const int32_t* __restrict__ dst_row,
+    const float* __restrict__ topk_w, int32_t k, int64_t H, uint16_t* __restrict__ out, int64_t ldo,
+    int32_t* err) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  __shared__ int32_t s_dst[32];
+  __shared__ float s_w[32];
+  __shared__ int s_n;
+  const int64_t t = blockIdx.x;
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    int32_t d = -1;
+    float w = 0.f;
+    if (tid < k) {
+      d = __ldg(dst_row + t * k + tid);
+      if (d >= y_rows) {
+        set_err(err, MOE_DEV_BAD_INDEX);
+        d = -1;
+      }
+      w = __ldg(topk_w + t * k + tid);
+    }
+    const uint32_t valid = __ballot_sync(0xffffffffu, d >= 0);
+    if (d >= 0) {
+      const int slot = __popc(valid & ((1u << tid) - 1u));
+      s_dst[slot] = d;
+      s_w[slot] = w;
+    }
+    if (tid == 0) s_n = __popc(valid);
+  }
+  __syncthreads();
+  const int n = s_n;
+  for (int64_t base = 0; base < H; base += static_cast<int64_t>(kCombLatThreads) * 8 * kCombLatVec) {
+    float acc[kCombLatVec][8];
+#pragma unroll
+    for (int v = 0; v < kCombLatVec; ++v)
+#pragma unroll
+      for (int h = 0; h < 8; ++h) acc[v][h] = 0.f;
+    for (int j0 = 0; j0 < n; j0 += kCombLatSlots) {
+      uint4 u[kCombLatSlots][kCombLatVec];
+#pragma unroll
+      for (int j = 0; j < kCombLatSlots; ++j) {
+        const uint16_t* row = y2 + static_cast<int64_t>(j0 + j < n ? s_dst[j0 + j] : 0) * ldy;
+#pragma unroll
+        for (int v = 0; v < kCombLatVec; ++v) {
+          const int64_t c = base + (static_cast<int64_t>(v) * kCombLatThreads + tid) * 8;
+          u[j][v] = (j0 + j < n && c < H) ? __ldg(reinterpret_cast<const uint4*>(row + c)) : make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kCombLatSlots; ++j) {
+        if (j0 + j >= n) break;
+        const float w = s_w[j0 + j];
+#pragma unroll
+        for (int v = 0; v < kCombLatVec; ++v) {
+          const uint32_t x[4] = {u[j][v].x, u[j][v].y, u[j][v].z, u[j][v].w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            acc[v][2 * h] = fmaf(w, __uint_as_float(x[h] << 16), acc[v][2 * h]);
+            acc[v][2 * h + 1] = fmaf(w, __uint_as_float(x[h] & 0xFFFF0000u), acc[v][2 * h + 1]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < kCombLatVec; ++v) {
+      const int64_t c = base + (static_cast<int64_t>(v) * kCombLatThreads + tid) * 8;
+      if (c >= H) continue;
+      uint32_t o[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[v][2 * h], acc[v][2 * h + 1]);
+        o[h] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      *reinterpret_cast<uint4*>(out + t * ldo + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -453,6 +567,10 @@ extern "C" int moe_combine(const uint16_t* Y2, int64_t ldy, int64_t y_rows, cons
   MOE_CHECK_ARG(ldy >= H && ldy % 8 == 0 && ldo >= H && ldo % 8 == 0 && y_rows >= 0);
   MOE_CHECK_ARG(T < (1ll << 31));
   if (int st = check_device()) return st;
+  // a few tokens (up to one per SM): one wide CTA per token, slots' loads in flight together
+  if (T <= num_sms())
+    return launch_pdl(combine_latency_kernel, static_cast<unsigned>(T), kCombLatThreads, 0, as_stream(stream), Y2,
+                      ldy, y_rows, dst_row, topk_w, k, static_cast<int64_t>(H), out, ldo, err);
   static int per_sm[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
