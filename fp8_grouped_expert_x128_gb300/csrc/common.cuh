@@ -439,8 +439,13 @@ __device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
   return make_uint2(lo, hi);
 }
 
+// s = max(amax, 1e-4) / 448 rounded to nearest: the same one-step correction
+// of a product by the rounded reciprocal (of the constant 448); non-finite
+// block maxima take the full division.
 __device__ __forceinline__ float block_scale(float amax) {
-  return __fdiv_rn(fmaxf(amax, kQuantFloor), kQuantMax);
+  const float a = fmaxf(amax, kQuantFloor);
+  if (!isfinite(a)) return __fdiv_rn(a, kQuantMax);
+  return div_rn_by(a, kQuantMax, __frcp_rn(kQuantMax));
 }
 
 

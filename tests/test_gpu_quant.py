@@ -90,6 +90,19 @@ def test_quant_division_every_bf16_under_many_scales(lib):
     _assert_quant_equal(lib, xb)
 
 
+def test_quant_scale_every_bf16_block_maximum(lib):
+    # s = fp32(max(amax, 1e-4) / 448) for every finite bf16 magnitude as a
+    # block's maximum (with its negative in the block too): scales and codes
+    # bit-exact against the oracle's float32 division.
+    allbits = np.arange(0x7F80, dtype=np.uint32).astype(np.uint16)      # +0 .. max finite
+    nb = allbits.size
+    blocks = np.zeros((nb + (-nb) % 4, 128), np.uint16)
+    blocks[:nb, 0] = allbits
+    blocks[:nb, 1] = allbits | 0x8000
+    blocks[:nb, 2] = allbits >> 1
+    _assert_quant_equal(lib, blocks.reshape(-1, 512))
+
+
 def test_quant_edge_cases(lib):
     rng = np.random.default_rng(5)
     M, K = 37, 384                     # M not a multiple of 4, three blocks
