@@ -22,7 +22,10 @@
  *    caller.  The library never allocates device memory and never synchronises,
  *    except moe_read_device_status.  Work is enqueued on `stream` (a
  *    cudaStream_t passed as void*; NULL = the legacy default stream), so a call
- *    sequence can be captured in a CUDA graph.
+ *    sequence can be captured in a CUDA graph.  Kernels are launched with
+ *    programmatic dependent launch: one may begin its local set-up while the
+ *    previous kernel on the stream finishes, but it waits for that kernel's
+ *    completion before touching memory, so stream order is kept.
  *  - bf16 tensors are passed as uint16_t bit patterns; FP8 tensors are uint8_t
  *    OCP E4M3FN codes (bias 7, max 448, NaN 0x7F/0xFF).
  *  - Every base pointer must be 16-byte aligned; K, H and I are multiples of 128.
