@@ -100,6 +100,18 @@ def gemm1_fused(wl):
     return gemm1_variant(wl).endswith("<swiglu>")
 
 
+def combine_fused(wl):
+    """moe_ffn folds a single-slot combine (k = 1) into GEMM2 where the
+    tokens-as-M kernel serves it."""
+    import fp8_grouped_expert_x128_gb300 as moe
+    flags = wl.get("gemm_flags", 0)
+    if wl["k"] != 1 or flags & moe.MOE_GEMM_CTA_PAIR:
+        return False
+    if wl["layout"] == moe.MOE_LAYOUT_MASKED:
+        return moe.moe_gemm_fp8_masked_variant(wl["cfg"].max_m, wl["expected_m"], flags) == 0
+    return True
+
+
 def algorithmic_counts(wl):
     """Algorithmic FLOPs and bytes per step and per GEMM1 launch."""
     cfg = wl["cfg"]
@@ -580,13 +592,13 @@ def main():
                        "timing": "CUDA events on the launching stream around each step; stage split from a separate instrumented replay",
                        "parallelism": f"replicas x{world}"},
             "stage_ms": {n: round(v, 4) for n, v in zip(
-                ["quant (fused into permute)", "quant+permute", "gemm1", "swiglu_quant (fused into gemm1 when 0)", "gemm2", "combine"], stage_ms)},
+                ["quant (fused into permute)", "quant+permute", "gemm1", "swiglu_quant (fused into gemm1 when 0)", "gemm2", "combine (fused into gemm2 when 0)"], stage_ms)},
             "tflops": alg["flops"] / (ms_per_step / 1e3) / 1e12,
             "weight_gbs": alg["weight_bytes"] / (ms_per_step / 1e3) / 1e9,
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": (5 if gemm1_fused(wl) else 6) * args.steps,
+            "gpu_launches": (6 - int(gemm1_fused(wl)) - int(combine_fused(wl))) * args.steps,
             "clocks": clk.summary(),
             "device_status": moe.moe_status_string(status),
             "wall_s_timed": t_wall,

@@ -210,20 +210,29 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
     return MOE_OK;
   };
   int rc;
+  const int32_t gflags = d->gemm_flags & ~MOE_FFN_FUSE_SWIGLU;
+  // One routing slot per token (k = 1, e.g. the prefill layout): GEMM2's
+  // epilogue writes each routed row to its token's output with the combine's
+  // arithmetic, and the quant-scatter pass zeroes the rows of tokens not routed
+  // here, so the combine kernel and the Y2 round trip drop out.  Where the
+  // weights-as-M or the CTA-pair kernel would serve GEMM2, the plain path runs.
+  const bool fuse_combine =
+      d->k == 1 && !(gflags & MOE_GEMM_CTA_PAIR) &&
+      (!masked || moe_gemm_fp8_masked_variant(d->max_m, d->expected_m, gflags) == 0);
   // stages 1+2: routing index pass, then each routed token row is quantised
   // straight into its expert slot (no token-order FP8 copy in between)
   if ((rc = mark(0))) return rc;
   if ((rc = mark(1))) return rc;
   if ((rc = permute_launch(nullptr, nullptr, 0, d->x, d->H, d->topk_ids, d->T, d->H, d->k,
                            d->expert_begin, d->E, d->layout, d->max_m, a1, sa1, p.s_ld1, counts,
-                           offsets, mind, rowsrc, dst, p.rows, d->err, st)))
+                           offsets, mind, rowsrc, dst, p.rows, d->err, st, fuse_combine ? d->out : nullptr,
+                           d->H)))
     return rc;
   if ((rc = mark(2))) return rc;
   // stages 3+4: on request (MOE_FFN_FUSE_SWIGLU) and where the tokens-as-M
   // kernel serves GEMM1, SwiGLU and the FP8 requantisation run in its
   // epilogue (no bf16 Y1 round trip); otherwise GEMM1 writes Y1 and the
   // SwiGLU kernel requantises it.
-  const int32_t gflags = d->gemm_flags & ~MOE_FFN_FUSE_SWIGLU;
   const bool fuse_swiglu =
       (d->gemm_flags & MOE_FFN_FUSE_SWIGLU) &&
       (!masked || moe_gemm_fp8_masked_variant(d->max_m, d->expected_m, d->gemm_flags) == 0);
@@ -251,7 +260,13 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
       return rc;
     if ((rc = mark(4))) return rc;
   }
-  if (masked)
+  if (fuse_combine && masked)
+    rc = gemm_masked_combine1(a2, sa2, d->w2, d->w2_s, counts, d->E, d->max_m, d->H, d->I, rowsrc,
+                              d->topk_w, d->out, d->H, gflags, d->err, st);
+  else if (fuse_combine)
+    rc = gemm_contig_combine1(a2, d->I, sa2, p.s_ld2, d->w2, d->w2_s, offsets, mind, p.rows, d->E, d->H,
+                              d->I, rowsrc, d->topk_w, d->out, d->H, gflags, d->err, st);
+  else if (masked)
     rc = moe_gemm_fp8_masked(a2, sa2, d->w2, d->w2_s, counts, d->E, d->max_m, d->H, d->I,
                              d->expected_m, y2, gflags, d->err, stream);
   else
@@ -259,8 +274,8 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
                              d->H, d->I, y2, d->H, gflags, d->err, stream);
   if (rc) return rc;
   if ((rc = mark(5))) return rc;
-  if ((rc = moe_combine(y2, d->H, p.rows, dst, d->topk_w, d->T, d->k, d->H, d->out, d->H, d->err,
-                        stream)))
+  if (!fuse_combine &&
+      (rc = moe_combine(y2, d->H, p.rows, dst, d->topk_w, d->T, d->k, d->H, d->out, d->H, d->err, stream)))
     return rc;
   return mark(6);
 }

@@ -66,13 +66,24 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
                    int32_t expert_begin, int32_t E, int32_t layout, int32_t max_m,
                    uint8_t* q_out, float* s_out, int64_t s_out_ld, int32_t* counts,
                    int32_t* offsets, int32_t* m_indices, int32_t* row_src, int32_t* dst_row,
-                   int64_t rows_capacity, int32_t* err, cudaStream_t st);
+                   int64_t rows_capacity, int32_t* err, cudaStream_t st,
+                   uint16_t* zero_out = nullptr, int64_t ldo = 0);
 
 // GEMM1 with SwiGLU + 1x128 requantisation fused into the tokens-as-M
 // epilogue (bytes equal GEMM1 -> moe_swiglu_quant); used inside moe_ffn.
 int gemm_masked_swiglu(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                        const int32_t* counts, int32_t E, int32_t max_m, int32_t N, int32_t K,
                        uint8_t* Q2, float* S2, int32_t flags, int32_t* err, cudaStream_t st);
+// GEMM2 with the single-slot combine in its epilogue (k = 1): routed row r is
+// written to out[row_src[r]] as bf16(w * bf16(D[r])), w = topk_w[row_src[r]].
+int gemm_masked_combine1(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                         const int32_t* counts, int32_t E, int32_t max_m, int32_t N, int32_t K,
+                         const int32_t* row_src, const float* topk_w, uint16_t* out, int64_t ldo,
+                         int32_t flags, int32_t* err, cudaStream_t st);
+int gemm_contig_combine1(const uint8_t* A, int64_t lda, const float* sA, int64_t sA_ld, const uint8_t* B,
+                         const float* sB, const int32_t* offsets, const int32_t* m_indices, int64_t M_capacity,
+                         int32_t E, int32_t N, int32_t K, const int32_t* row_src, const float* topk_w,
+                         uint16_t* out, int64_t ldo, int32_t flags, int32_t* err, cudaStream_t st);
 int gemm_contig_swiglu(const uint8_t* A, int64_t lda, const float* sA, int64_t sA_ld,
                        const uint8_t* B, const float* sB, const int32_t* offsets,
                        const int32_t* m_indices, int64_t M_capacity, int32_t E, int32_t N, int32_t K,

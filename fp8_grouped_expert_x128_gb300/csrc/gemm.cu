@@ -112,6 +112,12 @@ struct GemmArgs {
   uint8_t* Q2;       // [rows, N/2] FP8
   float* S2;         // grouped scales, group size S2_G
   int64_t S2_G;
+  // one routing slot per token (plain mode): write out[token] = bf16(w * bf16(D))
+  // instead of D, the combine's arithmetic for a single slot
+  const int32_t* row_src;
+  const float* topk_w;
+  uint16_t* out;
+  int64_t ldo;
 };
 
 struct Sched {
@@ -338,6 +344,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t gr = static_cast<int64_t>(sched.rbase[e]) + r_local;
       bool row_ok = r_local < sched.rext[e];
       if (row_ok && p.layout == MOE_LAYOUT_CONTIG) row_ok = __ldg(p.m_indices + gr) >= 0;
+      // single-slot combine: the row's token and weight, read now so the
+      // loads are long done when the tile is stored
+      int64_t tok = 0;
+      float wtok = 0.f;
+      if (!kSwiGLU && p.out != nullptr && row_ok) {
+        tok = __ldg(p.row_src + gr);
+        wtok = __ldg(p.topk_w + tok);
+      }
       const int n0 = nt * BN + g * 128;
       const int64_t grp = gr / p.sA_G, pos = gr - grp * p.sA_G;
       const float* sa_ptr = p.sA + grp * KB * p.sA_G + pos;
@@ -424,7 +438,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       if (!kSwiGLU) {
-        if (active && row_ok) {
+        if (active && row_ok && p.out != nullptr) {
+          // the row's only routing slot: the combine's bf16(fmaf(w, bf16(y), 0))
+          // written straight to the token's output row
+          const float w = wtok;
+          uint4* dst = reinterpret_cast<uint4*>(p.out + tok * p.ldo + n0);
+          auto rb = [](float v) { return __bfloat162float(__float2bfloat16_rn(v)); };
+#pragma unroll
+          for (int v = 0; v < 16; ++v) {
+            uint32_t o[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const __nv_bfloat162 bb = __floats2bfloat162_rn(fmaf(w, rb(acc[v * 4 + h].x), 0.f),
+                                                              fmaf(w, rb(acc[v * 4 + h].y), 0.f));
+              o[h] = *reinterpret_cast<const uint32_t*>(&bb);
+            }
+            dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        } else if (active && row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(p.D + gr * p.ldd + n0);
 #pragma unroll
           for (int v = 0; v < 16; ++v) {
@@ -1254,6 +1285,67 @@ int gemm_contig_swiglu(const uint8_t* A, int64_t lda, const float* sA, int64_t s
   a.S2_G = s2_ld;
   const int64_t tiles = (M_capacity / BM) * (N / BN);
   return launch_tokens_m(A, M_capacity, lda, B, tiles, a, st, true);
+}
+
+// GEMM2 with the single-slot combine folded into the epilogue (moe_ffn, k = 1):
+// each routed row r goes to out[row_src[r]] scaled by topk_w[row_src[r]].
+int gemm_masked_combine1(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                         const int32_t* counts, int32_t E, int32_t max_m, int32_t N, int32_t K,
+                         const int32_t* row_src, const float* topk_w, uint16_t* out, int64_t ldo,
+                         int32_t flags, int32_t* err, cudaStream_t st) {
+  MOE_CHECK_ARG(E >= 1 && E <= kMaxExperts && N > 0 && N % 128 == 0 && K > 0 && K % 128 == 0);
+  MOE_CHECK_ARG(max_m > 0 && static_cast<int64_t>(E) * max_m < (1ll << 31));
+  MOE_CHECK_ARG(A && sA && B && sB && counts && row_src && topk_w && out && aligned16(A) && aligned16(B) &&
+                aligned16(out) && ldo >= N && ldo % 8 == 0);
+  if (int rc = check_device()) return rc;
+  GemmArgs a{};
+  a.sA = sA;
+  a.sA_G = max_m;
+  a.sB = sB;
+  a.counts = counts;
+  a.E = E;
+  a.N = N;
+  a.K = K;
+  a.max_m = max_m;
+  a.layout = MOE_LAYOUT_MASKED;
+  a.err = err;
+  a.flags = flags & ~MOE_GEMM_DEBUG_STALL;
+  a.row_src = row_src;
+  a.topk_w = topk_w;
+  a.out = out;
+  a.ldo = ldo;
+  const int64_t tiles = static_cast<int64_t>(E) * ((max_m + BM - 1) / BM) * ((N + BN - 1) / BN);
+  return launch_tokens_m(A, static_cast<int64_t>(E) * max_m, K, B, tiles, a, st);
+}
+
+int gemm_contig_combine1(const uint8_t* A, int64_t lda, const float* sA, int64_t sA_ld, const uint8_t* B,
+                         const float* sB, const int32_t* offsets, const int32_t* m_indices, int64_t M_capacity,
+                         int32_t E, int32_t N, int32_t K, const int32_t* row_src, const float* topk_w,
+                         uint16_t* out, int64_t ldo, int32_t flags, int32_t* err, cudaStream_t st) {
+  MOE_CHECK_ARG(E >= 1 && E <= kMaxExperts && N > 0 && N % 128 == 0 && K > 0 && K % 128 == 0);
+  MOE_CHECK_ARG(M_capacity > 0 && M_capacity % BM == 0 && M_capacity < (1ll << 31));
+  MOE_CHECK_ARG(A && sA && B && sB && offsets && m_indices && row_src && topk_w && out);
+  MOE_CHECK_ARG(aligned16(A) && aligned16(B) && aligned16(out) && lda % 16 == 0 && sA_ld >= M_capacity &&
+                ldo >= N && ldo % 8 == 0);
+  if (int rc = check_device()) return rc;
+  GemmArgs a{};
+  a.sA = sA;
+  a.sA_G = sA_ld;
+  a.sB = sB;
+  a.offsets = offsets;
+  a.m_indices = m_indices;
+  a.E = E;
+  a.N = N;
+  a.K = K;
+  a.layout = MOE_LAYOUT_CONTIG;
+  a.err = err;
+  a.flags = flags & ~MOE_GEMM_DEBUG_STALL;
+  a.row_src = row_src;
+  a.topk_w = topk_w;
+  a.out = out;
+  a.ldo = ldo;
+  const int64_t tiles = (M_capacity / BM) * ((N + BN - 1) / BN);
+  return launch_tokens_m(A, M_capacity, lda, B, tiles, a, st);
 }
 
 }  // namespace moe

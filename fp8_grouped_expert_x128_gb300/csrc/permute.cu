@@ -243,7 +243,7 @@ template <int kQsWarps, int kQsPairs>
 __global__ void __launch_bounds__(32 * kQsWarps, kQsWarps == 4 ? 6 : 4) quant_scatter_kernel(
     const uint16_t* __restrict__ x, int64_t ldx, const int32_t* __restrict__ dst_row,
     int64_t n_assign, int32_t k, int64_t H, uint8_t* __restrict__ q_out, float* __restrict__ s_out,
-    int64_t G) {
+    int64_t G, uint16_t* __restrict__ zero_out, int64_t ldo) {
   grid_dependency_wait();
   grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -252,7 +252,14 @@ __global__ void __launch_bounds__(32 * kQsWarps, kQsWarps == 4 ? 6 : 4) quant_sc
   for (int64_t i = blockIdx.x; i < n_assign; i += gridDim.x) {
   const int32_t dst = dst_next;   // the next destination is read before this row's work
   dst_next = i + gridDim.x < n_assign ? __ldg(dst_row + i + gridDim.x) : -1;
-  if (dst < 0) continue;
+  if (dst < 0) {
+    // one slot per token and it is not routed here: the token's output row is
+    // zero (what the combine writes for a token without local slots)
+    if (zero_out != nullptr)
+      for (int64_t c = threadIdx.x; c < H / 8; c += blockDim.x)
+        reinterpret_cast<uint4*>(zero_out + i * ldo)[c] = make_uint4(0, 0, 0, 0);
+    continue;
+  }
   const int64_t t = i / k;
   const int64_t grp = dst / G, pos = dst - grp * G;
   const uint16_t* xr = x + t * ldx;
@@ -486,7 +493,8 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
                    int32_t expert_begin, int32_t E, int32_t layout, int32_t max_m,
                    uint8_t* q_out, float* s_out, int64_t s_out_ld, int32_t* counts,
                    int32_t* offsets, int32_t* m_indices, int32_t* row_src, int32_t* dst_row,
-                   int64_t rows_capacity, int32_t* err, cudaStream_t st) {
+                   int64_t rows_capacity, int32_t* err, cudaStream_t st, uint16_t* zero_out,
+                   int64_t ldo) {
   MOE_CHECK_ARG(T >= 0 && H > 0 && H % 128 == 0 && k >= 1 && k <= 32);
   MOE_CHECK_ARG(E >= 1 && E <= kMaxExperts);
   MOE_CHECK_ARG(layout == MOE_LAYOUT_MASKED || layout == MOE_LAYOUT_CONTIG);
@@ -539,7 +547,7 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
       return MOE_ERR_CUDA;
     const int64_t wave = static_cast<int64_t>(num_sms()) * occ;
     return launch_pdl(kern, static_cast<unsigned>(n < wave ? n : wave), threads, 0, st, x, ldx, dst_row, n, k,
-                      static_cast<int64_t>(H), q_out, s_out, G);
+                      static_cast<int64_t>(H), q_out, s_out, G, k == 1 ? zero_out : nullptr, ldo);
   }
   return launch_pdl(permute_scatter_kernel, grid, 128, 0, st, q, s, s_ld, dst_row, n, k, H, q_out,
                     s_out, G);
