@@ -367,21 +367,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.f, 0.f);
       // The scales run kScaleAhead k-blocks ahead of their use in a register
-      // ring (rotated, so every index is static): a global load has several
-      // k-blocks of work to hide behind, not one.
+      // ring: a global load has several k-blocks of work to hide behind, not
+      // one.  The k-block loop is unrolled by the ring depth, so entry m is
+      // loaded once and read kScaleAhead k-blocks later with no register
+      // moves in between (a rotating ring's moves would each wait for the
+      // load just issued, leaving one k-block of cover).
       auto load_sa = [&](int k) { return (row_ok && k < KB) ? __ldg(sa_ptr + static_cast<int64_t>(k) * p.sA_G) : 0.f; };
       auto load_sb = [&](int k) { return k < KB ? __ldg(sb_ptr + k) : 0.f; };
       auto load_sb2 = [&](int k) { return (kSwiGLU && k < KB) ? __ldg(sb2_ptr + k) : 0.f; };
-      float sa0 = load_sa(0), sa1 = load_sa(1), sa2 = load_sa(2), sa3 = load_sa(3);
-      float sb0 = load_sb(0), sb1 = load_sb(1), sb2 = load_sb(2), sb3 = load_sb(3);
-      float su0 = load_sb2(0), su1 = load_sb2(1), su2 = load_sb2(2), su3 = load_sb2(3);
-      for (int kb = 0; kb < KB; ++kb, ++acc_it) {
+      static_assert(kScaleAhead == 4, "ring below assumes 4");
+      float ra[kScaleAhead], rb[kScaleAhead], ru[kScaleAhead];
+#pragma unroll
+      for (int m = 0; m < kScaleAhead; ++m) {
+        ra[m] = load_sa(m);
+        rb[m] = load_sb(m);
+        ru[m] = load_sb2(m);
+      }
+#pragma unroll 1
+      for (int kb0 = 0; ok && kb0 < KB; kb0 += kScaleAhead) {
+#pragma unroll
+      for (int m = 0; m < kScaleAhead; ++m) {
+        const int kb = kb0 + m;
+        if (kb >= KB) break;
         const uint32_t b = acc_it & 1, tph = (acc_it >> 1) & 1;
-        const float sc = sa0 * sb0;
-        const float scu = sa0 * su0;
-        sa0 = sa1; sa1 = sa2; sa2 = sa3; sa3 = load_sa(kb + kScaleAhead);
-        sb0 = sb1; sb1 = sb2; sb2 = sb3; sb3 = load_sb(kb + kScaleAhead);
-        if (kSwiGLU) { su0 = su1; su1 = su2; su2 = su3; su3 = load_sb2(kb + kScaleAhead); }
+        ++acc_it;
+        const float sc = ra[m] * rb[m];
+        const float scu = ra[m] * ru[m];
+        ra[m] = load_sa(kb + kScaleAhead);
+        rb[m] = load_sb(kb + kScaleAhead);
+        if (kSwiGLU) ru[m] = load_sb2(kb + kScaleAhead);
         // one lane waits, the warp follows it: tcgen05.ld is warp-collective
         int got = 1;
         if (lane == 0) got = mbar_wait_bounded(tfull0 + 8 * b, tph, abort, p.err, p.wait_limit_ns);
@@ -435,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty0 + 8 * b);
+      }
       }
       if (!ok) break;
       if (!kSwiGLU) {
@@ -891,7 +906,9 @@ int launch_tokens_m_pair(const uint8_t* A, int64_t a_rows, int64_t lda, const ui
 // (column)]; the epilogue scales column c by sB[nb, kb] * sA[token c, kb].
 // Stages are small (16 KB of weights + the token rows), so the ring is deep
 // (4..8 stages) to keep enough bytes in flight per SM, and TMEM holds 2..8
-// accumulation buffers.
+// accumulation buffers.  A tile's token rows come in as few copies as
+// possible: four tensor maps with boxes of 128, 64, 32 and 16 rows, the
+// tile's rows split into 128-row boxes and at most one of each smaller box.
 // =============================================================================
 template <int BNT>
 struct WeightsM {
@@ -944,9 +961,16 @@ __device__ void build_schedule_wm(const GemmArgs& p, const Sched& s, int nblk) {
   }
 }
 
+// Token-side tensor maps: the same [E*max_m, K] matrix with boxes of 16 << i
+// rows (a map whose box would exceed the matrix repeats the 16-row map; the
+// kernel never picks a box taller than the tile's rows).
+struct TokenMaps {
+  CUtensorMap box[4];
+};
+
 template <int BNT>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_fp8_weights_m_kernel(const __grid_constant__ CUtensorMap tmT,   // tokens  [E*max_m, K]
+    gemm_fp8_weights_m_kernel(const __grid_constant__ TokenMaps tmT,     // tokens  [E*max_m, K]
                               const __grid_constant__ CUtensorMap tmW,   // weights [E*N, K]
                               const GemmArgs p) {
   using C = WeightsM<BNT>;
@@ -982,10 +1006,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmT);
-    tma_prefetch_desc(&tmW);
-  }
+  if (warp == 0 && lane < 4) tma_prefetch_desc(&tmT.box[lane]);
+  if (warp == 0 && lane == 4) tma_prefetch_desc(&tmW);
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -1025,8 +1047,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st_base = smem_u32(smem + s * C::kStage);
           mbar_arrive_expect_tx(full0 + 8 * s, C::kWBytes + ncols * BK);
           tma_load_2d_hint(st_base, &tmW, full0 + 8 * s, kb * BK, w_row, pol_w);
-          for (int r = 0; r < ncols; r += 16)
-            tma_load_2d(st_base + C::kWBytes + r * BK, &tmT, full0 + 8 * s, kb * BK, t_row + r);
+          // rows [0, ncols) in boxes of 128 while they last, then at most one
+          // each of 64, 32 and 16 (ncols is a multiple of 16)
+          for (int r = 0; r < ncols;) {
+            const int left = ncols - r;
+            const int i = left >= 128 ? 3 : left >= 64 ? 2 : left >= 32 ? 1 : 0;
+            tma_load_2d(st_base + C::kWBytes + r * BK, &tmT.box[i], full0 + 8 * s, kb * BK, t_row + r);
+            r += 16 << i;
+          }
         }
       }
       if (!ok) {
@@ -1095,15 +1123,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j = l / nblk, nb = l % nblk;
       const int ntok = min(BNT, sched.rext[e] - j * BNT);
       const int ncols = (ntok + 15) & ~15;
-      const int col0 = g * C::kHalf;
-      const int my_cols = max(0, min(C::kHalf, ncols - col0));
+      // the two warpgroups split the tile's columns evenly (in 16-column
+      // chunks), so a part-filled tile does not leave one group all the work
+      const int cols_g0 = ((ncols / 16 + 1) / 2) * 16;
+      const int col0 = g ? cols_g0 : 0;
+      const int my_cols = g ? ncols - cols_g0 : cols_g0;
       const int nchunk = my_cols / 16;
       const float* sa_base = p.sA + static_cast<int64_t>(e) * KB * p.max_m + j * BNT + col0;
       const float* sb_ptr = p.sB + (static_cast<int64_t>(e) * nblk + nb) * KB;
       // Token scales run kScaleAhead k-blocks ahead of their use: one float4
       // per lane in a register ring, parked in this warp's shared double buffer
-      // one k-block before use, so no global load latency sits on the
-      // per-k-block path.  The k-block loop is unrolled by the ring depth, so
+      // one k-block before use already multiplied by that k-block's weight
+      // scale (sB * sA, the same product the definition forms), so no global
+      // load latency and no scale product sits on the per-k-block path.  The k-block loop is unrolled by the ring depth, so
       // each ring entry is loaded once and read kScaleAhead k-blocks later with
       // no register moves in between (a move would wait for its load).
       const bool ld_lane = lane * 4 < my_cols;
@@ -1121,10 +1153,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       pa[1] = load_sa4(1); pa[2] = load_sa4(2); pa[3] = load_sa4(3); pa[0] = load_sa4(4);
 #pragma unroll
       for (int m = 0; m < kScaleAhead; ++m) rs[m] = load_sb(m);
+      auto park = [&](float* dst, float4 a, float sb) {
+        if (ld_lane)
+          reinterpret_cast<float4*>(dst)[lane] =
+              make_float4(__fmul_rn(sb, a.x), __fmul_rn(sb, a.y), __fmul_rn(sb, a.z), __fmul_rn(sb, a.w));
+      };
       {
         const float4 pa0 = load_sa4(0);
         __syncwarp();
-        if (ld_lane) reinterpret_cast<float4*>(my_sa)[lane] = pa0;
+        park(my_sa, pa0, rs[0]);
         __syncwarp();
       }
       float2 acc[C::kHalf / 2];
@@ -1138,7 +1175,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kb >= KB) break;
           const uint32_t b = acc_it % C::kBufs, tph = (acc_it / C::kBufs) & 1;
           ++acc_it;
-          const float sb = rs[m];
           rs[m] = load_sb(kb + kScaleAhead);
           int got = 1;
           if (lane == 0) got = mbar_wait_bounded(tfull0 + 8 * b, tph, abort, p.err, p.wait_limit_ns);
@@ -1163,7 +1199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                   for (int i = 0; i < 8; ++i) {
                     const int c = (ch + h) * 16 + 2 * i;
-                    const float2 s2 = __fmul2_rn(make_float2(sb, sb), make_float2(sa_cur[c], sa_cur[c + 1]));
+                    const float2 s2 = *reinterpret_cast<const float2*>(sa_cur + c);
                     acc[c / 2] = __ffma2_rn(
                         s2, make_float2(__uint_as_float(r[h][2 * i]), __uint_as_float(r[h][2 * i + 1])), acc[c / 2]);
                   }
@@ -1177,7 +1213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // park the next k-block's token scales, then refill that ring entry
           const int mn = (m + 1) % kScaleAhead;
           if (kb + 1 < KB) {
-            if (ld_lane) reinterpret_cast<float4*>(my_sa + ((kb + 1) & 1) * C::kHalf)[lane] = pa[mn];
+            park(my_sa + ((kb + 1) & 1) * C::kHalf, pa[mn], rs[mn]);   // rs[mn]: sB of k-block kb + 1
             __syncwarp();
           }
           pa[mn] = load_sa4(kb + 1 + kScaleAhead);
@@ -1209,10 +1245,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BNT>
 int launch_weights_m(const uint8_t* A, const uint8_t* B, GemmArgs& args, cudaStream_t stream) {
   using C = WeightsM<BNT>;
-  CUtensorMap tmT, tmW;
-  if (int st = make_tmap_u8_sw128(&tmT, A, static_cast<uint64_t>(args.E) * args.max_m, args.K,
-                                  args.K, 16))
-    return st;
+  TokenMaps tmT;
+  CUtensorMap tmW;
+  const uint64_t t_rows = static_cast<uint64_t>(args.E) * args.max_m;
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t h = (16u << i) <= t_rows ? (16u << i) : 16u;
+    if (int st = make_tmap_u8_sw128(&tmT.box[i], A, t_rows, args.K, args.K, h)) return st;
+  }
   if (int st = make_tmap_u8_sw128(&tmW, B, static_cast<uint64_t>(args.E) * args.N, args.K, args.K, 128))
     return st;
   const size_t smem = C::smem_bytes(args.E);

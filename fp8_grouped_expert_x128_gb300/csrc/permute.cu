@@ -230,65 +230,85 @@ __global__ void __launch_bounds__(128) permute_scatter_kernel(
 }
 
 // Fused 1x128 quantisation + scatter for moe_ffn: one resident wave of CTAs
-// walks the assignments (grid stride), skipping non-local ones; for a routed
-// row the CTA's kQsWarps warps share its 128-column block pairs (a half-warp
-// per block), loads issued before use, and quantise the token's bf16 row
-// straight into its expert slot (the bytes equal moe_quant_fp8 followed by
-// moe_permute: same helpers, same arithmetic).
+// walks the tokens (grid stride); the CTA's kQsWarps warps share the token's
+// 128-column block pairs (a half-warp per block), loads issued before use,
+// quantise the bf16 row once and write it into each of the token's local
+// expert slots (the bytes equal moe_quant_fp8 followed by moe_permute: same
+// helpers, same arithmetic).  The quantisation needs only x, so a CTA's first
+// row is loaded and quantised before the kernel waits on the routing index
+// kernel launched just before it (programmatic dependent launch): the index
+// work hides behind the first row's loads.  Nothing the index kernel writes is
+// read, and nothing is written, before that wait.
 // Two shapes, both with a whole row's loads in flight (H <= 7168 in one pass):
-// many routed rows (prefill) take 4-warp CTAs, 7 block pairs per warp, ~6
-// CTAs per SM for the bytes in flight; a few hundred rows (decode) take
-// 8-warp CTAs, 4 pairs per warp, so each row finishes sooner.
+// many tokens (prefill) take 4-warp CTAs, 7 block pairs per warp, ~6 CTAs per
+// SM for the bytes in flight; a few hundred tokens (decode) take 8-warp CTAs,
+// 4 pairs per warp, so each row finishes sooner.
 template <int kQsWarps, int kQsPairs>
 __global__ void __launch_bounds__(32 * kQsWarps, kQsWarps == 4 ? 6 : 4) quant_scatter_kernel(
     const uint16_t* __restrict__ x, int64_t ldx, const int32_t* __restrict__ dst_row,
-    int64_t n_assign, int32_t k, int64_t H, uint8_t* __restrict__ q_out, float* __restrict__ s_out,
+    int64_t T, int32_t k, int64_t H, uint8_t* __restrict__ q_out, float* __restrict__ s_out,
     int64_t G, uint16_t* __restrict__ zero_out, int64_t ldo) {
-  grid_dependency_wait();
-  grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t KB = H / 128, NP = (KB + 1) / 2;
-  int32_t dst_next = blockIdx.x < n_assign ? __ldg(dst_row + blockIdx.x) : -1;
-  for (int64_t i = blockIdx.x; i < n_assign; i += gridDim.x) {
-  const int32_t dst = dst_next;   // the next destination is read before this row's work
-  dst_next = i + gridDim.x < n_assign ? __ldg(dst_row + i + gridDim.x) : -1;
-  if (dst < 0) {
-    // one slot per token and it is not routed here: the token's output row is
-    // zero (what the combine writes for a token without local slots)
-    if (zero_out != nullptr)
-      for (int64_t c = threadIdx.x; c < H / 8; c += blockDim.x)
-        reinterpret_cast<uint4*>(zero_out + i * ldo)[c] = make_uint4(0, 0, 0, 0);
-    continue;
-  }
-  const int64_t t = i / k;
-  const int64_t grp = dst / G, pos = dst - grp * G;
-  const uint16_t* xr = x + t * ldx;
-  uint8_t* qr = q_out + static_cast<int64_t>(dst) * H;
-  for (int64_t p0 = warp; p0 < NP; p0 += static_cast<int64_t>(kQsWarps) * kQsPairs) {
-    uint4 u[kQsPairs];
-#pragma unroll
-    for (int j = 0; j < kQsPairs; ++j) {
-      const int64_t kb = (p0 + j * kQsWarps) * 2 + (lane >> 4);
-      u[j] = kb < KB ? __ldg(reinterpret_cast<const uint4*>(xr + kb * 128 + (lane & 15) * 8))
-                     : make_uint4(0, 0, 0, 0);
+  bool waited = false;
+  auto wait_index = [&]() {
+    if (!waited) {
+      grid_dependency_wait();
+      grid_launch_dependents();
+      waited = true;
     }
+  };
+  for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+    const uint16_t* xr = x + t * ldx;
+    for (int64_t p0 = warp; p0 < NP; p0 += static_cast<int64_t>(kQsWarps) * kQsPairs) {
+      uint4 u[kQsPairs];
 #pragma unroll
-    for (int j = 0; j < kQsPairs; ++j) {
-      const int64_t kb = (p0 + j * kQsWarps) * 2 + (lane >> 4);
-      float f[8];
-      unpack_bf16x8(u[j], f);
-      float amax = 0.f;
+      for (int j = 0; j < kQsPairs; ++j) {
+        const int64_t kb = (p0 + j * kQsWarps) * 2 + (lane >> 4);
+        u[j] = kb < KB ? __ldg(reinterpret_cast<const uint4*>(xr + kb * 128 + (lane & 15) * 8))
+                       : make_uint4(0, 0, 0, 0);
+      }
+      uint2 code[kQsPairs];
+      float sc[kQsPairs];
 #pragma unroll
-      for (int v = 0; v < 8; ++v) amax = fmaxf(amax, fabsf(f[v]));
-      amax = half_warp_max(amax);
-      if (kb < KB) {
-        const float sc = block_scale(amax);
-        *reinterpret_cast<uint2*>(qr + kb * 128 + (lane & 15) * 8) = quant8(f, sc);
-        if ((lane & 15) == 0) s_out[(grp * KB + kb) * G + pos] = sc;
+      for (int j = 0; j < kQsPairs; ++j) {
+        float f[8];
+        unpack_bf16x8(u[j], f);
+        float amax = 0.f;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) amax = fmaxf(amax, fabsf(f[v]));
+        amax = half_warp_max(amax);
+        sc[j] = block_scale(amax);
+        code[j] = quant8(f, sc[j]);
+      }
+      wait_index();
+      // the token's routing slots, one per lane
+      const int32_t dl = lane < k ? __ldg(dst_row + t * k + lane) : -1;
+      for (int j2 = 0; j2 < k; ++j2) {
+        const int32_t dst = __shfl_sync(0xffffffffu, dl, j2);
+        if (dst < 0) continue;
+        const int64_t grp = dst / G, pos = dst - grp * G;
+        uint8_t* qr = q_out + static_cast<int64_t>(dst) * H;
+#pragma unroll
+        for (int j = 0; j < kQsPairs; ++j) {
+          const int64_t kb = (p0 + j * kQsWarps) * 2 + (lane >> 4);
+          if (kb < KB) {
+            *reinterpret_cast<uint2*>(qr + kb * 128 + (lane & 15) * 8) = code[j];
+            if ((lane & 15) == 0) s_out[(grp * KB + kb) * G + pos] = sc[j];
+          }
+        }
       }
     }
+    if (zero_out != nullptr) {
+      // one slot per token and it is not routed here: the token's output row
+      // is zero (what the combine writes for a token without local slots)
+      wait_index();
+      if (__ldg(dst_row + t) < 0)
+        for (int64_t c = threadIdx.x; c < H / 8; c += blockDim.x)
+          reinterpret_cast<uint4*>(zero_out + t * ldo)[c] = make_uint4(0, 0, 0, 0);
+    }
   }
-  }
+  wait_index();   // a CTA with no token still orders its exit after the index kernel
 }
 
 // A resident wave of CTAs walks the tokens (grid stride), one token at a
@@ -546,7 +566,7 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
     if (occ == 0 && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, 0) != cudaSuccess || occ < 1))
       return MOE_ERR_CUDA;
     const int64_t wave = static_cast<int64_t>(num_sms()) * occ;
-    return launch_pdl(kern, static_cast<unsigned>(n < wave ? n : wave), threads, 0, st, x, ldx, dst_row, n, k,
+    return launch_pdl(kern, static_cast<unsigned>(T < wave ? T : wave), threads, 0, st, x, ldx, dst_row, T, k,
                       static_cast<int64_t>(H), q_out, s_out, G, k == 1 ? zero_out : nullptr, ldo);
   }
   return launch_pdl(permute_scatter_kernel, grid, 128, 0, st, q, s, s_ld, dst_row, n, k, H, q_out,
