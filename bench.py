@@ -519,29 +519,51 @@ def main():
         w_d = torch.empty_like(wl["topk_w"])
         d2 = make_desc(wl, out, err=err, x=x_d, ids=ids_d, w=w_d)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        for _ in range(3):
+
+        def host_step():
             x_d.copy_(x_h, non_blocking=True); ids_d.copy_(ids_h, non_blocking=True)
             w_d.copy_(w_h, non_blocking=True)
             moe.moe_ffn(d2, ws)
             out_h.copy_(out, non_blocking=True)
-        torch.cuda.synchronize(dev)
-        e2e_ms = []
-        for _ in range(args.steps):
-            l2_flush.fill_(1)
-            e0.record(stream)
-            x_d.copy_(x_h, non_blocking=True); ids_d.copy_(ids_h, non_blocking=True)
-            w_d.copy_(w_h, non_blocking=True)
-            moe.moe_ffn(d2, ws)
-            out_h.copy_(out, non_blocking=True)
-            e1.record(stream)
+
+        def time_e2e(run):
+            for _ in range(3):
+                run()
             torch.cuda.synchronize(dev)
-            e2e_ms.append(e0.elapsed_time(e1))
-        e2e_s = _max_over_ranks(world, sum(e2e_ms) / 1e3)
+            ms = []
+            for _ in range(args.steps):
+                l2_flush.fill_(1)
+                e0.record(stream)
+                run()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                ms.append(e0.elapsed_time(e1))
+            return _max_over_ranks(world, sum(ms) / 1e3)
+
+        # Eager: each step calls moe_ffn from the host.  Graph (as the decode
+        # path runs in serving): the copies in, moe_ffn and the copy out are
+        # captured once as one CUDA graph and replayed per step; both take
+        # every byte across the host link inside the timed region.
+        eager_s = time_e2e(host_step)
+        e2e_graph = None
+        if graph is not None:
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(side):
+                host_step()
+            torch.cuda.current_stream(dev).wait_stream(side)
+            e2e_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(e2e_graph):
+                host_step()
+        e2e_s = time_e2e(e2e_graph.replay) if e2e_graph is not None else eager_s
         h2d = x_h.numel() * 2 + ids_h.numel() * 4 + w_h.numel() * 4
         e2e = {"value": rows_all / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(out_h.numel() * 2),
                "ms_per_step": 1e3 * e2e_s / args.steps,
-               "how": "per step: pinned-host x, topk_ids, topk_w -> device, eager moe_ffn, out -> pinned host"}
+               "eager": {"value": rows_all / eager_s, "ms_per_step": 1e3 * eager_s / args.steps},
+               "how": ("per step: pinned-host x, topk_ids, topk_w -> device, moe_ffn, out -> pinned host, "
+                       + ("captured once as one CUDA graph and replayed" if e2e_graph is not None
+                          else "eager calls") + "; 'eager' = the same with eager calls")}
 
     # ------------------------------------------------------------------ roofline (GEMM1)
     peaks, peak_src = load_peaks()
