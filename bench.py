@@ -540,30 +540,49 @@ def main():
                 ms.append(e0.elapsed_time(e1))
             return _max_over_ranks(world, sum(ms) / 1e3)
 
-        # Eager: each step calls moe_ffn from the host.  Graph (as the decode
-        # path runs in serving): the copies in, moe_ffn and the copy out are
-        # captured once as one CUDA graph and replayed per step; both take
-        # every byte across the host link inside the timed region.
-        eager_s = time_e2e(host_step)
-        e2e_graph = None
-        if graph is not None:
+        def graphed(fn):
             side = torch.cuda.Stream(dev)
             side.wait_stream(torch.cuda.current_stream(dev))
             with torch.cuda.stream(side):
-                host_step()
+                fn()
             torch.cuda.current_stream(dev).wait_stream(side)
-            e2e_graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(e2e_graph):
-                host_step()
-        e2e_s = time_e2e(e2e_graph.replay) if e2e_graph is not None else eager_s
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                fn()
+            return gr
+
+        # Three ways from host buffers, every byte crossing the host link inside
+        # the timed region of each step:
+        #  host I/O  moe_ffn given the pinned host x / routing / out directly:
+        #            the kernels read and write them in place, overlapped with
+        #            the compute (the library's host-buffer path; the value);
+        #  copies    explicit copies in, moe_ffn, copy out;
+        #  eager     the copies path with eager calls instead of a graph.
+        # The graph variants are captured once and replayed (as the decode
+        # path runs in serving); without graphs (--eager) all are eager.
+        eager_s = time_e2e(host_step)
+        copies_s = time_e2e(graphed(host_step).replay) if graph is not None else eager_s
+        d_host = make_desc(wl, out_h, err=err, x=x_h, ids=ids_h, w=w_h)
+        host_io = lambda: moe.moe_ffn(d_host, ws)
+        try:
+            host_io()
+            torch.cuda.synchronize(dev)
+            host_s = time_e2e(graphed(host_io).replay if graph is not None else host_io)
+        except moe.MoeError as exc:
+            print(f"host-buffer moe_ffn refused ({exc}); e2e = the copies path", file=sys.stderr)
+            host_s = None
+        e2e_s = host_s if host_s is not None else copies_s
         h2d = x_h.numel() * 2 + ids_h.numel() * 4 + w_h.numel() * 4
         e2e = {"value": rows_all / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(out_h.numel() * 2),
                "ms_per_step": 1e3 * e2e_s / args.steps,
+               "copies": {"value": rows_all / copies_s, "ms_per_step": 1e3 * copies_s / args.steps},
                "eager": {"value": rows_all / eager_s, "ms_per_step": 1e3 * eager_s / args.steps},
-               "how": ("per step: pinned-host x, topk_ids, topk_w -> device, moe_ffn, out -> pinned host, "
-                       + ("captured once as one CUDA graph and replayed" if e2e_graph is not None
-                          else "eager calls") + "; 'eager' = the same with eager calls")}
+               "how": ("moe_ffn on pinned host x, topk_ids, topk_w and out (read and written in place "
+                       "by the kernels across the host link)" if host_s is not None else
+                       "pinned-host x, topk_ids, topk_w -> device, moe_ffn, out -> pinned host")
+                      + ("; one CUDA graph replay per step" if graph is not None else "; eager calls")
+                      + "; 'copies' = explicit copies in and out around moe_ffn; 'eager' = copies, eager calls"}
 
     # ------------------------------------------------------------------ roofline (GEMM1)
     peaks, peak_src = load_peaks()

@@ -167,6 +167,30 @@ extern "C" int moe_read_device_status(int32_t* err, void* stream, int* status_ou
   return MOE_OK;
 }
 
+namespace {
+
+// Where a pointer handed to moe_ffn may live.  `host_ok`: the token I/O (x,
+// topk_ids, topk_w, out) may also be page-locked host memory that CUDA maps at
+// the same address (cudaHostAlloc, cudaMallocHost, cudaHostRegister with the
+// mapped flag); the kernels then read and write it in place across the host
+// link.  Anything else (pageable host memory, another GPU's memory) would fault
+// in a kernel, so it is refused before any launch.
+int check_placement(const void* ptr, bool host_ok) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_ERR_INVALID_ARG;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (a.type == cudaMemoryTypeDevice) return a.device == dev ? MOE_OK : MOE_ERR_INVALID_ARG;
+  if (a.type == cudaMemoryTypeManaged) return MOE_OK;
+  if (host_ok && a.type == cudaMemoryTypeHost && a.devicePointer == ptr) return MOE_OK;
+  return MOE_ERR_INVALID_ARG;
+}
+
+}  // namespace
+
 extern "C" size_t moe_ffn_workspace_size(const moe_ffn_desc* desc) {
   FfnPlan p;
   if (plan_ffn(desc, &p) != MOE_OK) return 0;
@@ -181,6 +205,12 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
   MOE_CHECK_ARG(workspace_bytes >= p.total);
   MOE_CHECK_ARG(d->x && d->topk_ids && d->topk_w && d->w13 && d->w13_s && d->w2 && d->w2_s && d->out);
   if (int st = check_device()) return st;
+  const void* io[4] = {d->x, d->topk_ids, d->topk_w, d->out};
+  for (const void* ptr : io)
+    if (int rc = check_placement(ptr, true)) return rc;
+  const void* on_device[5] = {d->w13, d->w13_s, d->w2, d->w2_s, workspace};
+  for (const void* ptr : on_device)
+    if (int rc = check_placement(ptr, false)) return rc;
   cudaStream_t st = as_stream(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   auto at = [&](size_t off) { return static_cast<void*>(ws + off); };

@@ -243,6 +243,15 @@ int moe_combine(const uint16_t *Y2, int64_t ldy, int64_t y_rows,
  *   -> moe_combine.
  * Weights: w13 [E, 2I, H] (gate rows [0, I), up rows [I, 2I)) with w13_s
  * [E, 2I/128, H/128]; w2 [E, H, I] with w2_s [E, H/128, I/128] (device).
+ * Token I/O: x, topk_ids, topk_w and out may be device memory of the current
+ * GPU or page-locked host memory that CUDA maps at the same address
+ * (cudaHostAlloc / cudaMallocHost / cudaHostRegister with the mapped flag):
+ * the kernels then read x, the routing and the weights of each slot and write
+ * out in place across the host link, overlapped with the compute, with no
+ * separate copies (the end-to-end path from host buffers).  Weights and the
+ * workspace must be device memory of the current GPU.  Any other placement
+ * (pageable host memory, another GPU's memory) returns MOE_ERR_INVALID_ARG
+ * before anything is launched (checked with cudaPointerGetAttributes).
  * workspace: device, at least moe_ffn_workspace_size(desc) bytes, 256-byte
  * aligned; holds every intermediate.  stage_events (optional, may be NULL):
  * 7 cudaEvent_t handles recorded on `stream` before stage 1 and after each of

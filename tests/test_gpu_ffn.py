@@ -218,3 +218,41 @@ def test_ffn_equals_the_stage_entry_points(lib, name, fuse):
     lib.moe_combine(Y2, dst, wl["topk_w"], out)
     torch.cuda.synchronize()
     assert np.array_equal(bits(out), got)
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c5t4"])
+def test_ffn_host_buffers_equal_device_buffers(lib, name):
+    # x, the routing and out in mapped page-locked host memory: the kernels read
+    # and write them in place across the host link; the bytes of out equal the
+    # device-buffer call's (c3 covers the single-slot path: out rows written by
+    # GEMM2's epilogue, zero rows by the quant-scatter pass)
+    wl = build_workload(name)
+    ref, st = _gpu_ffn(lib, wl)
+    T, H = wl["T"], wl["cfg"].H
+    x_h = wl["x"].cpu().pin_memory()
+    ids_h = wl["topk_ids"].cpu().pin_memory()
+    w_h = wl["topk_w"].cpu().pin_memory()
+    out_h = torch.full((T, H), 0x7E57, dtype=torch.int16).pin_memory().view(torch.bfloat16)
+    err = lib.new_error_word()
+    desc = make_desc(wl, out_h, err=err, x=x_h, ids=ids_h, w=w_h)
+    ws = lib.alloc_workspace(desc)
+    lib.moe_ffn(desc, ws)
+    torch.cuda.synchronize()
+    st_h, _ = lib.moe_read_device_status(err)
+    assert st_h == st
+    assert np.array_equal(bits(out_h), ref)
+
+
+def test_ffn_refuses_pageable_host_buffers(lib):
+    # pageable host memory is not mapped for the GPU: refused before any launch
+    wl = build_workload("c1")
+    T, H = wl["T"], wl["cfg"].H
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    for which in ("x", "out"):
+        x = wl["x"].cpu() if which == "x" else wl["x"]
+        o = torch.empty((T, H), dtype=torch.bfloat16) if which == "out" else out
+        desc = make_desc(wl, o, x=x)
+        ws = lib.alloc_workspace(desc)
+        with pytest.raises(lib.MoeError) as ei:
+            lib.moe_ffn(desc, ws)
+        assert ei.value.status == lib.MOE_ERR_INVALID_ARG
