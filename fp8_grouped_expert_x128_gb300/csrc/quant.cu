@@ -88,29 +88,13 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const uint16_t* __re
 }
 
 // ---------------------------------------------------------------- a5
-// h = silu(g) * u in fp32, quantised by the a1 rule.  Row selection by masked
-// counts or by contiguous m_indices.
-__global__ void __launch_bounds__(256) swiglu_quant_kernel(
-    const uint16_t* __restrict__ y1, int64_t rows, int64_t I, const int32_t* __restrict__ counts,
-    int64_t max_m, const int32_t* __restrict__ m_indices, uint8_t* __restrict__ q,
-    float* __restrict__ s, int64_t G) {
-  grid_dependency_wait();
-  grid_launch_dependents();
-  // a warp covers blocks 4w + h and 4w + h + 2 of one row (h = its half), with
-  // all four 16-byte loads (g and u of both blocks) issued before any use
-  const int64_t KB = I / 128;
-  const int64_t warps_per_row = (KB + 3) / 4;
-  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int64_t r = gw / warps_per_row;
-  if (r >= rows) return;
-  if (counts != nullptr) {
-    const int64_t e = r / max_m;
-    if (r - e * max_m >= static_cast<int64_t>(__ldg(counts + e))) return;
-  } else if (m_indices != nullptr) {
-    if (__ldg(m_indices + r) < 0) return;
-  }
-  const int64_t kb0 = (gw % warps_per_row) * 4 + (lane >> 4);
+// h = silu(g) * u in fp32, quantised by the a1 rule.  A warp covers blocks
+// 4w + h and 4w + h + 2 of one row (w = `part`, h = its half-warp), with all
+// four 16-byte loads (g and u of both blocks) issued before any use.
+__device__ __forceinline__ void swiglu_row_part(const uint16_t* __restrict__ y1, int64_t I, int64_t KB,
+                                                int64_t r, int64_t part, int lane, uint8_t* __restrict__ q,
+                                                float* __restrict__ s, int64_t G) {
+  const int64_t kb0 = part * 4 + (lane >> 4);
   const uint16_t* row = y1 + r * 2 * I;
   uint4 gv[2], uv[2];
 #pragma unroll
@@ -145,6 +129,71 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(
         s[(grp * KB + kb) * G + pos] = sc;
       }
     }
+  }
+}
+
+// Contiguous layout (rows selected by m_indices, or all rows): one warp per
+// (row, part), the grid covering every row.
+__global__ void __launch_bounds__(256) swiglu_quant_kernel(
+    const uint16_t* __restrict__ y1, int64_t rows, int64_t I, const int32_t* __restrict__ m_indices,
+    uint8_t* __restrict__ q, float* __restrict__ s, int64_t G) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int64_t KB = I / 128;
+  const int64_t warps_per_row = (KB + 3) / 4;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t r = gw / warps_per_row;
+  if (r >= rows) return;
+  if (m_indices != nullptr && __ldg(m_indices + r) < 0) return;
+  swiglu_row_part(y1, I, KB, r, gw % warps_per_row, threadIdx.x & 31, q, s, G);
+}
+
+// Masked layout: only the rows below each expert's count hold tokens (a few
+// hundred of E * max_m at decode).  A resident wave of CTAs walks the valid
+// rows alone: each CTA turns the counts into a prefix over the experts in
+// shared memory, and a warp task (valid row, part) finds its expert by binary
+// search over the prefix.
+constexpr int kSwMaxExperts = 1024;
+
+__global__ void __launch_bounds__(256) swiglu_quant_masked_kernel(
+    const uint16_t* __restrict__ y1, int64_t I, const int32_t* __restrict__ counts, int32_t E,
+    int64_t max_m, uint8_t* __restrict__ q, float* __restrict__ s) {
+  __shared__ int32_t pre[kSwMaxExperts + 1];   // pre[e] = valid rows of the experts before e
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) {
+    int run = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      // rows r of expert e with r < min(count, max_m), as the per-row rule reads
+      const int c = e < E ? min(max(__ldg(counts + e), 0), static_cast<int>(max_m)) : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (e < E) pre[e] = run + incl - c;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) pre[E] = run;
+  }
+  __syncthreads();
+  const int64_t KB = I / 128, warps_per_row = (KB + 3) / 4;
+  const int64_t tasks = static_cast<int64_t>(pre[E]) * warps_per_row;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t task = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp; task < tasks;
+       task += nwarps) {
+    const int vr = static_cast<int>(task / warps_per_row);
+    int lo = 0, hi = E - 1;   // the last expert e with pre[e] <= vr (it has rows: pre[e + 1] > vr)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= vr) lo = mid;
+      else hi = mid - 1;
+    }
+    const int64_t r = static_cast<int64_t>(lo) * max_m + (vr - pre[lo]);
+    swiglu_row_part(y1, I, KB, r, task % warps_per_row, lane, q, s, max_m);
   }
 }
 
@@ -200,7 +249,17 @@ extern "C" int moe_swiglu_quant(const uint16_t* Y1, int64_t rows, int32_t I, con
   }
   if (int st = check_device()) return st;
   const int64_t warps = rows * ((I / 128 + 3) / 4);
-  return launch_pdl(swiglu_quant_kernel, grid_for_warps(warps), 256, 0, as_stream(stream), Y1,
-                    rows, static_cast<int64_t>(I), counts, static_cast<int64_t>(max_m),
-                    counts ? nullptr : m_indices, q, s, G);
+  if (counts != nullptr) {
+    const int64_t E = rows / max_m;
+    MOE_CHECK_ARG(E <= kSwMaxExperts);
+    // one resident wave at most (8 CTAs of 256 threads per SM), fewer when
+    // even a full layout has fewer warp tasks
+    const int64_t wave = static_cast<int64_t>(num_sms()) * 8;
+    const int64_t need = grid_for_warps(warps);
+    return launch_pdl(swiglu_quant_masked_kernel, static_cast<unsigned>(need < wave ? need : wave), 256, 0,
+                      as_stream(stream), Y1, static_cast<int64_t>(I), counts, static_cast<int32_t>(E),
+                      static_cast<int64_t>(max_m), q, s);
+  }
+  return launch_pdl(swiglu_quant_kernel, grid_for_warps(warps), 256, 0, as_stream(stream), Y1, rows,
+                    static_cast<int64_t>(I), m_indices, q, s, G);
 }

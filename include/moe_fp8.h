@@ -216,7 +216,8 @@ int moe_gemm_fp8_masked_variant(int32_t max_m, int32_t expected_m, int32_t flags
  * quantised by the a1 rule into q [rows, I] (row stride I) and s (groups of G rows).
  * Y1 : device bf16 [rows, 2I] (row stride 2I).
  * Row selection: masked -> counts != NULL, G = max_m, row r is processed iff
- *   r % max_m < counts[r / max_m]; contig -> counts == NULL, m_indices != NULL,
+ *   r % max_m < counts[r / max_m] (at most 1024 experts = rows / max_m);
+ *   contig -> counts == NULL, m_indices != NULL,
  *   G = s_ld, row r processed iff r < rows and m_indices[r] >= 0.
  * Unprocessed rows of q and s are left untouched.
  */
