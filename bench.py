@@ -397,7 +397,7 @@ def main():
     ap.add_argument("--workload", default="c2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
-    ap.add_argument("--ref-step-s", type=float, default=4.0)
+    ap.add_argument("--ref-step-s", type=float, default=2.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager moe_ffn calls instead of a CUDA graph")
     ap.add_argument("--expected-m", type=int, default=None,
