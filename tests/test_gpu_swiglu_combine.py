@@ -39,6 +39,27 @@ def test_swiglu_quant_masked_rows(lib):
     assert (qh[~valid] == SENTINEL_U8).all() and (sflat[:, ~valid] == SENTINEL_F32).all()
 
 
+def test_swiglu_quant_masked_counts_clamped_and_many_experts(lib):
+    # a count above max_m covers the whole slot range, a negative count none;
+    # 300 experts, most of them empty, exercise the expert search over the
+    # counts prefix (rows of the nonempty ones land in the right slots)
+    max_m, I = 32, 256
+    counts = np.zeros(300, np.int32)
+    counts[[0, 1, 2, 150, 298, 299]] = [100, -5, 7, 32, 1, 19]
+    E = counts.size
+    y1 = _y1(E * max_m, I, 6)
+    q = torch.full((E * max_m, I), SENTINEL_U8, dtype=torch.uint8, device="cuda")
+    s = torch.full((E, I // 128, max_m), SENTINEL_F32, device="cuda")
+    lib.moe_swiglu_quant(from_bits(y1), q, s, counts=to_dev(counts), max_m=max_m)
+    torch.cuda.synchronize()
+    qh, sh = u8(q), s.cpu().numpy()
+    kept = np.clip(counts, 0, max_m)
+    valid = np.concatenate([np.arange(max_m) < c for c in kept])
+    sflat = sh.transpose(1, 0, 2).reshape(I // 128, -1)
+    check_swiglu(qh, sflat[:, valid], y1, valid)
+    assert (qh[~valid] == SENTINEL_U8).all() and (sflat[:, ~valid] == SENTINEL_F32).all()
+
+
 def test_swiglu_quant_contig_selection_and_full_width(lib):
     rows, I = 512, 2048
     mi = np.full(rows, -1, np.int32)
