@@ -175,7 +175,8 @@ namespace {
 // mapped flag); the kernels then read and write it in place across the host
 // link.  Anything else (pageable host memory, another GPU's memory) would fault
 // in a kernel, so it is refused before any launch.
-int check_placement(const void* ptr, bool host_ok) {
+// `on_host` (may be NULL) is set when the pointer is page-locked host memory.
+int check_placement(const void* ptr, bool host_ok, bool* on_host = nullptr) {
   cudaPointerAttributes a{};
   if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
     (void)cudaGetLastError();
@@ -183,9 +184,13 @@ int check_placement(const void* ptr, bool host_ok) {
   }
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (on_host) *on_host = false;
   if (a.type == cudaMemoryTypeDevice) return a.device == dev ? MOE_OK : MOE_ERR_INVALID_ARG;
   if (a.type == cudaMemoryTypeManaged) return MOE_OK;
-  if (host_ok && a.type == cudaMemoryTypeHost && a.devicePointer == ptr) return MOE_OK;
+  if (host_ok && a.type == cudaMemoryTypeHost && a.devicePointer == ptr) {
+    if (on_host) *on_host = true;
+    return MOE_OK;
+  }
   return MOE_ERR_INVALID_ARG;
 }
 
@@ -205,9 +210,11 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
   MOE_CHECK_ARG(workspace_bytes >= p.total);
   MOE_CHECK_ARG(d->x && d->topk_ids && d->topk_w && d->w13 && d->w13_s && d->w2 && d->w2_s && d->out);
   if (int st = check_device()) return st;
-  const void* io[4] = {d->x, d->topk_ids, d->topk_w, d->out};
+  const void* io[3] = {d->x, d->topk_ids, d->topk_w};
   for (const void* ptr : io)
     if (int rc = check_placement(ptr, true)) return rc;
+  bool out_on_host = false;
+  if (int rc = check_placement(d->out, true, &out_on_host)) return rc;
   const void* on_device[5] = {d->w13, d->w13_s, d->w2, d->w2_s, workspace};
   for (const void* ptr : on_device)
     if (int rc = check_placement(ptr, false)) return rc;
@@ -245,9 +252,12 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
   // epilogue writes each routed row to its token's output with the combine's
   // arithmetic, and the quant-scatter pass zeroes the rows of tokens not routed
   // here, so the combine kernel and the Y2 round trip drop out.  Where the
-  // weights-as-M or the CTA-pair kernel would serve GEMM2, the plain path runs.
+  // weights-as-M or the CTA-pair kernel would serve GEMM2, the plain path runs,
+  // and so it does when out is in host memory: GEMM2's epilogue writes each
+  // row in 16-byte pieces from 32 rows at a time, which the host link serves
+  // far worse than the combine kernel's whole-row stores.
   const bool fuse_combine =
-      d->k == 1 && !(gflags & MOE_GEMM_CTA_PAIR) &&
+      d->k == 1 && !out_on_host && !(gflags & MOE_GEMM_CTA_PAIR) &&
       (!masked || moe_gemm_fp8_masked_variant(d->max_m, d->expected_m, gflags) == 0);
   // stages 1+2: routing index pass, then each routed token row is quantised
   // straight into its expert slot (no token-order FP8 copy in between)
