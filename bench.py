@@ -100,18 +100,6 @@ def gemm1_fused(wl):
     return gemm1_variant(wl).endswith("<swiglu>")
 
 
-def combine_fused(wl):
-    """moe_ffn folds a single-slot combine (k = 1) into GEMM2 where the
-    tokens-as-M kernel serves it."""
-    import fp8_grouped_expert_x128_gb300 as moe
-    flags = wl.get("gemm_flags", 0)
-    if wl["k"] != 1 or flags & moe.MOE_GEMM_CTA_PAIR:
-        return False
-    if wl["layout"] == moe.MOE_LAYOUT_MASKED:
-        return moe.moe_gemm_fp8_masked_variant(wl["cfg"].max_m, wl["expected_m"], flags) == 0
-    return True
-
-
 def algorithmic_counts(wl):
     """Algorithmic FLOPs and bytes per step and per GEMM1 launch."""
     cfg = wl["cfg"]
@@ -639,7 +627,7 @@ def main():
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": (6 - int(gemm1_fused(wl)) - int(combine_fused(wl))) * args.steps,
+            "gpu_launches": moe.moe_ffn_kernel_count(desc) * args.steps,
             "clocks": clk.summary(),
             "device_status": moe.moe_status_string(status),
             "wall_s_timed": t_wall,

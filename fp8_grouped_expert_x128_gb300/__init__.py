@@ -47,7 +47,7 @@ EXPORTED = [
     "moe_status_string", "moe_version", "moe_read_device_status", "moe_quant_fp8",
     "moe_quant_weight_fp8", "moe_contig_rows_bound", "moe_permute", "moe_gemm_fp8_contig",
     "moe_gemm_fp8_masked", "moe_gemm_fp8_masked_variant", "moe_swiglu_quant", "moe_combine", "moe_ffn_workspace_size", "moe_ffn",
-    "moe_ffn_noalloc", "moe_ffn_noalloc_capacity",
+    "moe_ffn_noalloc", "moe_ffn_noalloc_capacity", "moe_ffn_kernel_count",
 ]
 
 _P = ctypes.c_void_p
@@ -89,6 +89,7 @@ _sig("moe_gemm_fp8_masked_variant", ctypes.c_int, [_I32, _I32, _I32])
 _sig("moe_swiglu_quant", ctypes.c_int, [_P, _I64, _I32, _P, _I32, _P, _P, _P, _I64, _P, _P])
 _sig("moe_combine", ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I32, _I32, _P, _I64, _P, _P])
 _sig("moe_ffn_workspace_size", ctypes.c_size_t, [ctypes.POINTER(moe_ffn_desc)])
+_sig("moe_ffn_kernel_count", ctypes.c_int, [ctypes.POINTER(moe_ffn_desc)])
 _sig("moe_ffn", ctypes.c_int, [ctypes.POINTER(moe_ffn_desc), _P, ctypes.c_size_t, _P])
 _sig("moe_ffn_noalloc", ctypes.c_int, [ctypes.POINTER(moe_ffn_desc), _P])
 _sig("moe_ffn_noalloc_capacity", ctypes.c_size_t, [])
@@ -260,6 +261,13 @@ def make_ffn_desc(x, topk_ids, topk_w, w13, w13_s, w2, w2_s, out, expert_begin, 
         d._events_keepalive = arr
         d.stage_events = ctypes.cast(arr, ctypes.c_void_p)
     return d
+
+
+def moe_ffn_kernel_count(desc: moe_ffn_desc) -> int:
+    """Kernels one moe_ffn call with `desc` launches (host-only)."""
+    n = int(_lib.moe_ffn_kernel_count(ctypes.byref(desc)))
+    _check(n if n < 0 else MOE_OK, "moe_ffn_kernel_count")
+    return n
 
 
 def moe_ffn_workspace_size(desc: moe_ffn_desc) -> int:

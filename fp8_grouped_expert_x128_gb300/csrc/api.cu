@@ -194,7 +194,49 @@ int check_placement(const void* ptr, bool host_ok, bool* on_host = nullptr) {
   return MOE_ERR_INVALID_ARG;
 }
 
+// moe_ffn's fusion choices for a descriptor (shared with moe_ffn_kernel_count).
+struct FfnFusion {
+  bool swiglu;    // SwiGLU + requant in GEMM1's epilogue
+  bool combine;   // single-slot combine in GEMM2's epilogue (no combine kernel)
+};
+
+FfnFusion ffn_fusion(const moe_ffn_desc* d, bool out_on_host) {
+  const bool masked = d->layout == MOE_LAYOUT_MASKED;
+  const int32_t gflags = d->gemm_flags & ~MOE_FFN_FUSE_SWIGLU;
+  FfnFusion f;
+  // stages 3+4: on request (MOE_FFN_FUSE_SWIGLU) and where the tokens-as-M
+  // kernel serves GEMM1, SwiGLU and the FP8 requantisation run in its
+  // epilogue (no bf16 Y1 round trip); otherwise GEMM1 writes Y1 and the
+  // SwiGLU kernel requantises it.
+  f.swiglu = (d->gemm_flags & MOE_FFN_FUSE_SWIGLU) &&
+             (!masked || moe_gemm_fp8_masked_variant(d->max_m, d->expected_m, d->gemm_flags) == 0);
+  // One routing slot per token (k = 1, e.g. the prefill layout): GEMM2's
+  // epilogue writes each routed row to its token's output with the combine's
+  // arithmetic, and the quant-scatter pass zeroes the rows of tokens not routed
+  // here, so the combine kernel and the Y2 round trip drop out.  Where the
+  // weights-as-M or the CTA-pair kernel would serve GEMM2, the plain path runs,
+  // and so it does when out is in host memory: GEMM2's epilogue writes each
+  // row in 16-byte pieces from 32 rows at a time, which the host link serves
+  // far worse than the combine kernel's whole-row stores.
+  f.combine = d->k == 1 && !out_on_host && !(gflags & MOE_GEMM_CTA_PAIR) &&
+              (!masked || moe_gemm_fp8_masked_variant(d->max_m, d->expected_m, gflags) == 0);
+  return f;
+}
+
 }  // namespace
+
+extern "C" int moe_ffn_kernel_count(const moe_ffn_desc* d) {
+  FfnPlan p;
+  if (plan_ffn(d, &p) != MOE_OK || d->out == nullptr) return MOE_ERR_INVALID_ARG;
+  bool out_on_host = false;
+  if (int rc = check_placement(d->out, true, &out_on_host)) return rc;
+  const FfnFusion f = ffn_fusion(d, out_on_host);
+  int n = d->T == 0 ? 1 : 2;                                              // index pass (+ quant-scatter)
+  n += f.swiglu ? 1 : 2;                                                  // GEMM1 (+ SwiGLU)
+  n += 1;                                                                 // GEMM2
+  n += f.combine ? 0 : 1;                                                 // combine
+  return n;
+}
 
 extern "C" size_t moe_ffn_workspace_size(const moe_ffn_desc* desc) {
   FfnPlan p;
@@ -248,17 +290,8 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
   };
   int rc;
   const int32_t gflags = d->gemm_flags & ~MOE_FFN_FUSE_SWIGLU;
-  // One routing slot per token (k = 1, e.g. the prefill layout): GEMM2's
-  // epilogue writes each routed row to its token's output with the combine's
-  // arithmetic, and the quant-scatter pass zeroes the rows of tokens not routed
-  // here, so the combine kernel and the Y2 round trip drop out.  Where the
-  // weights-as-M or the CTA-pair kernel would serve GEMM2, the plain path runs,
-  // and so it does when out is in host memory: GEMM2's epilogue writes each
-  // row in 16-byte pieces from 32 rows at a time, which the host link serves
-  // far worse than the combine kernel's whole-row stores.
-  const bool fuse_combine =
-      d->k == 1 && !out_on_host && !(gflags & MOE_GEMM_CTA_PAIR) &&
-      (!masked || moe_gemm_fp8_masked_variant(d->max_m, d->expected_m, gflags) == 0);
+  const FfnFusion fusion = ffn_fusion(d, out_on_host);
+  const bool fuse_combine = fusion.combine;
   // stages 1+2: routing index pass, then each routed token row is quantised
   // straight into its expert slot (no token-order FP8 copy in between)
   if ((rc = mark(0))) return rc;
@@ -269,13 +302,7 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
                            d->H)))
     return rc;
   if ((rc = mark(2))) return rc;
-  // stages 3+4: on request (MOE_FFN_FUSE_SWIGLU) and where the tokens-as-M
-  // kernel serves GEMM1, SwiGLU and the FP8 requantisation run in its
-  // epilogue (no bf16 Y1 round trip); otherwise GEMM1 writes Y1 and the
-  // SwiGLU kernel requantises it.
-  const bool fuse_swiglu =
-      (d->gemm_flags & MOE_FFN_FUSE_SWIGLU) &&
-      (!masked || moe_gemm_fp8_masked_variant(d->max_m, d->expected_m, d->gemm_flags) == 0);
+  const bool fuse_swiglu = fusion.swiglu;
   if (fuse_swiglu) {
     if (masked)
       rc = gemm_masked_swiglu(a1, sa1, d->w13, d->w13_s, counts, d->E, d->max_m, 2 * d->I, d->H,

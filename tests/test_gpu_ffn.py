@@ -6,6 +6,8 @@ Configs: the tiny masked config in full; the EP72-like and 48-GPU-domain
 decode configs in full (every routed row); the all-experts decode layer and the
 prefill (contiguous) config on sampled tokens, each sampled token's output
 computed by the oracle alone from x, its routing and its experts' weights."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -171,17 +173,24 @@ def test_ffn_prefill_contiguous_sampled_tokens(lib):
     check_tol_chain(got[tokens], ref, extra, "c3 ffn tokens")
 
 
-@pytest.mark.parametrize("name,fuse", [("c1", False), ("c2", False), ("c3", False), ("c2", True), ("c3", True)])
+@pytest.mark.parametrize("name,fuse", [("c1", False), ("c2", False), ("c3", False), ("c2", True), ("c3", True),
+                                       ("c5t1", False), ("c1_overflow", False)])
 def test_ffn_equals_the_stage_entry_points(lib, name, fuse):
     """moe_ffn fuses quantisation into the permute (and, with MOE_FFN_FUSE_SWIGLU,
     SwiGLU + requantisation into the tokens-as-M GEMM1 epilogue); its output must
     be bit-identical to the public stage calls made one by one (quant, permute,
-    GEMM1, SwiGLU+quant, GEMM2, combine)."""
-    wl = build_workload(name)
+    GEMM1, SwiGLU+quant, GEMM2, combine).
+    c1_overflow: the tiny config with 16 slots per expert, so every expert
+    overflows and the ranks past max_m are dropped the same way on both paths."""
+    overflow = name == "c1_overflow"
+    wl = build_workload("c1" if overflow else name)
+    if overflow:
+        wl["cfg"] = dataclasses.replace(wl["cfg"], max_m=16)
     cfg = wl["cfg"]
     if fuse:
         wl["gemm_flags"] = lib.MOE_FFN_FUSE_SWIGLU
     got, st = _gpu_ffn(lib, wl)
+    assert st == (lib.MOE_ERR_OVERFLOW if overflow else lib.MOE_OK)
     T, H, I, E, k = wl["T"], cfg.H, cfg.I, cfg.E, wl["k"]
     dev = "cuda"
     q = torch.empty((T, H), dtype=torch.uint8, device=dev)
