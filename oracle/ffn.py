@@ -58,6 +58,37 @@ def quant_1x128(x) -> tuple[np.ndarray, np.ndarray]:
     return q, np.ascontiguousarray(s.T)
 
 
+def _block_scale_ue8m0(amax_f32: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """Power-of-two scale of the other reading of "packed" input scales (UE8M0:
+    an unsigned 8-bit exponent, s = 2^(byte - 127)): the smallest power of two
+    s with max(amax, 1e-4) / s <= 448, i.e. s = 2^ceil(log2(max(amax, 1e-4) / 448)).
+    The exponent is found by exact comparisons of a against 448 * 2^e (both
+    exact in float64), not by a rounded logarithm.  Returns (s float32, byte uint8)."""
+    a = np.maximum(amax_f32.astype(np.float32), SCALE_FLOOR).astype(np.float64)
+    e = np.ceil(np.log2(a / E4M3_MAX)).astype(np.int64)          # estimate, then make exact
+    e = np.where(a > E4M3_MAX * np.exp2(e.astype(np.float64)), e + 1, e)
+    e = np.where(a <= E4M3_MAX * np.exp2((e - 1).astype(np.float64)), e - 1, e)
+    return np.exp2(e.astype(np.float64)).astype(np.float32), (e + 127).astype(np.uint8)
+
+
+def quant_1x128_ue8m0(x) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """1x128 E4M3 quantisation with power-of-two (UE8M0) block scales -- the
+    alternative reading of the DeepGEMM bullet's "packing of the input scales"
+    (the hardware block-scaled MMA consumes such scales).  Per row and block:
+    s = _block_scale_ue8m0(amax); q = e4m3(x / s), the quotient exact (a division
+    by a power of two).  Returns q [M, K] uint8, s [K/128, M] float32 and the
+    UE8M0 bytes [K/128, M] uint8 (s = 2^(byte - 127))."""
+    x = np.asarray(x, dtype=np.float32)
+    M, K = x.shape
+    assert K % BLOCK == 0
+    blocks = x.reshape(M, K // BLOCK, BLOCK)
+    amax = np.abs(blocks).max(axis=2)
+    s, byte = _block_scale_ue8m0(amax)
+    y = blocks.astype(np.float64) / s[:, :, None].astype(np.float64)   # exact
+    q = e4m3_encode(y).reshape(M, K)
+    return q, np.ascontiguousarray(s.T), np.ascontiguousarray(byte.T)
+
+
 def quant_128x128(w) -> tuple[np.ndarray, np.ndarray]:
     """128x128 block E4M3 quantisation of a K-major weight [N, K] (float32 values):
     the same rule as ``quant_1x128`` with amax over the whole tile.

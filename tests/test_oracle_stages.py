@@ -67,6 +67,77 @@ def test_quant_error_bound_and_layout():
     assert (err <= bound).all()
 
 
+def _smallest_pow2_exponent(a: float) -> int:
+    """Brute force with exact rationals: the smallest e with a <= 448 * 2^e."""
+    from fractions import Fraction
+    fa = Fraction(float(a))
+    e = -200
+    while fa > 448 * Fraction(2) ** e:
+        e += 1
+    return e
+
+
+def test_ue8m0_scale_is_the_smallest_power_of_two():
+    # amax over a wide exponent range, with the exact boundaries 448 * 2^j and
+    # their float32 neighbours, the 1e-4 floor and values below it
+    j = np.arange(-30, 40)
+    edges = (448.0 * np.exp2(j)).astype(np.float32)
+    amax = np.concatenate([edges, np.nextafter(edges, np.float32(np.inf)),
+                           np.nextafter(edges, np.float32(0)),
+                           np.exp2(RNG.uniform(-30, 40, 300)).astype(np.float32),
+                           np.float32([0.0, 1e-30, 1e-4, 2e-4])])
+    x = np.zeros((amax.size, 128), np.float32)
+    x[:, 5] = amax
+    x[:, 9] = -amax / 2
+    q, s, byte = oracle.quant_1x128_ue8m0(x)
+    for r, a in enumerate(amax):
+        e = _smallest_pow2_exponent(max(float(a), float(np.float32(1e-4))))
+        assert s[0, r] == np.float32(2.0 ** e), (a, s[0, r], e)
+        assert int(byte[0, r]) == e + 127
+    # the block maximum never saturates and lands in the top binade of E4M3
+    big = amax >= np.float32(1e-4)
+    top = e4m3_decode(q[big, 5])
+    assert (top <= 448.0).all() and (top >= 224.0).all()
+
+
+def test_ue8m0_codes_are_the_bruteforce_encoding_of_x_over_s():
+    # blocks whose maximum is 448 * 2^j: s = 2^j exactly and every element's code
+    # is the brute-force nearest E4M3 of x / 2^j
+    allv = bf16_decode(np.arange(65536, dtype=np.uint32).astype(np.uint16))
+    vals = allv[np.isfinite(allv) & (np.abs(allv) <= 448.0)].astype(np.float32)
+    for jexp in (-9, 0, 5):
+        scale = np.float32(2.0 ** jexp)
+        v = vals * scale
+        nb = -(-v.size // 127)
+        blocks = np.zeros((nb, 128), np.float32)
+        blocks[:, 0] = np.float32(448.0) * scale
+        flat = np.zeros(nb * 127, np.float32)
+        flat[:v.size] = v
+        blocks[:, 1:] = flat.reshape(nb, 127)
+        q, s, _ = oracle.quant_1x128_ue8m0(blocks)
+        assert (s == scale).all()
+        ref = oracle.e4m3_encode_bruteforce(blocks.astype(np.float64) / float(scale))
+        assert np.array_equal(q, ref)
+        assert (q[:, 0] == 0x7E).all()
+
+
+def test_ue8m0_against_fp32_scales():
+    # the power-of-two scale is the fp32 scale rounded up to a power of two
+    # (never below it, less than twice it), and both dequantise within the
+    # E4M3 rounding bound of x: half a step, 2^-4 relative for normal codes,
+    # 2^-10 * s absolute below the normal range
+    x = (RNG.standard_normal((64, 1024)) * np.exp2(RNG.integers(-6, 6, (64, 1))) ).astype(np.float32)
+    x = bf16_decode(bf16_encode(x)).astype(np.float32)
+    q32, s32 = quant_1x128(x)
+    q8, s8, _ = oracle.quant_1x128_ue8m0(x)
+    assert (s8 >= s32).all() and (s8 < 2 * s32).all()
+    for q, s in ((q32, s32), (q8, s8)):
+        sc = np.repeat(s.T, 128, axis=1).astype(np.float64)
+        deq = e4m3_decode(q) * sc
+        err = np.abs(deq - x)
+        assert (err <= np.abs(x) * 2.0 ** -4 + sc * 2.0 ** -10 + 1e-30).all()
+
+
 def test_quant_128x128_tiles_are_independent():
     w = _bf16(RNG.standard_normal((256, 384)) * 0.05)
     q, s = quant_128x128(w)
