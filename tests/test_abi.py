@@ -126,3 +126,21 @@ def test_register_split_kernels_compile_to_the_launch_budget(tmp_path):
     assert len(tok) == 3 and len(wm) == 1      # tokens-as-M plain, fused SwiGLU, CTA pair; weights-as-M<256>
     for k in tok + wm:
         assert report[k] == 168, (k, report[k])
+
+
+def test_masked_gemm_dispatch_is_host_logic(so):
+    # the masked GEMM's kernel choice is made on the host from (max_m, count
+    # hint, flags) alone: weights-as-M for a few rows per expert, tile width by
+    # the hint; tokens-as-M otherwise; the force flags override
+    import fp8_grouped_expert_x128_gb300 as moe
+    v = moe.moe_gemm_fp8_masked_variant
+    assert v(128, 2) == 64 and v(128, 32) == 64           # all-experts decode
+    assert v(1024, 134) == 0 and v(2048, 1024) == 0        # EP decode: tokens-as-M
+    assert v(1024, 0) == 0                                 # no hint: max_m decides
+    assert v(16, 0) == 64                                  # ... a tiny max_m is the hint
+    assert v(128, 2, moe.MOE_GEMM_FORCE_TOKENS_M) == 0
+    assert v(1024, 40, moe.MOE_GEMM_FORCE_WEIGHTS_M) == 64
+    assert v(1024, 100, moe.MOE_GEMM_FORCE_WEIGHTS_M) == 128
+    assert v(1024, 200, moe.MOE_GEMM_FORCE_WEIGHTS_M) == 256
+    assert v(1000, 200, moe.MOE_GEMM_FORCE_WEIGHTS_M) == moe.MOE_ERR_UNSUPPORTED   # max_m % 16
+    assert v(1000, 2) == 0                                 # weights-as-M needs max_m % 16 == 0
