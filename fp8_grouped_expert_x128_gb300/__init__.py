@@ -47,7 +47,8 @@ EXPORTED = [
     "moe_status_string", "moe_version", "moe_read_device_status", "moe_quant_fp8",
     "moe_quant_weight_fp8", "moe_contig_rows_bound", "moe_permute", "moe_gemm_fp8_contig",
     "moe_gemm_fp8_masked", "moe_gemm_fp8_masked_variant", "moe_swiglu_quant", "moe_combine", "moe_ffn_workspace_size", "moe_ffn",
-    "moe_ffn_noalloc", "moe_ffn_noalloc_capacity", "moe_ffn_kernel_count",
+    "moe_ffn_noalloc", "moe_ffn_noalloc_capacity", "moe_ffn_kernel_count", "moe_quant_fp8_ue8m0",
+    "moe_ue8m0_scale",
 ]
 
 _P = ctypes.c_void_p
@@ -76,6 +77,8 @@ _sig("moe_version", ctypes.c_int, [])
 _sig("moe_read_device_status", ctypes.c_int,
      [_P, _P, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(_I32)])
 _sig("moe_quant_fp8", ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P])
+_sig("moe_quant_fp8_ue8m0", ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _I64, _P, _P])
+_sig("moe_ue8m0_scale", ctypes.c_float, [ctypes.c_float, ctypes.POINTER(ctypes.c_uint8)])
 _sig("moe_quant_weight_fp8", ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P])
 _sig("moe_contig_rows_bound", _I64, [_I64, _I32])
 _sig("moe_permute", ctypes.c_int,
@@ -165,6 +168,24 @@ def moe_quant_fp8(x, q, s, s_ld=None, err=None, stream=None):
     _check(_lib.moe_quant_fp8(_ptr(x), M, K, x.stride(0), _ptr(_u8(q)), q.stride(0), _ptr(s), s_ld,
                               _ptr(err), _stream(stream)), "moe_quant_fp8")
     return q, s
+
+
+def moe_quant_fp8_ue8m0(x, q, s, e8=None, s_ld=None, err=None, stream=None):
+    """a1 with power-of-two block scales: s fp32 [K/128, s_ld] holds 2^e, e8 uint8
+    (optional, same shape) holds e + 127."""
+    _dev(x, torch.bfloat16, "x"); _dev(q, _U8, "q"); _dev(s, torch.float32, "s"); _dev(e8, _U8, "e8")
+    M, K = x.shape
+    s_ld = s.shape[-1] if s_ld is None else s_ld
+    _check(_lib.moe_quant_fp8_ue8m0(_ptr(x), M, K, x.stride(0), _ptr(_u8(q)), q.stride(0), _ptr(s),
+                                    _ptr(e8), s_ld, _ptr(err), _stream(stream)), "moe_quant_fp8_ue8m0")
+    return q, s
+
+
+def moe_ue8m0_scale(amax: float) -> tuple[float, int]:
+    """The UE8M0 block-scale rule for one block maximum (host): (2^e, e + 127)."""
+    b = ctypes.c_uint8(0)
+    s = float(_lib.moe_ue8m0_scale(ctypes.c_float(amax), ctypes.byref(b)))
+    return s, int(b.value)
 
 
 def moe_quant_weight_fp8(w, q, s, stream=None):

@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include <utility>
 
@@ -448,6 +449,32 @@ __device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
     hi |= e4m3x2_rn_satfinite(q[4 + 2 * i], q[4 + 2 * i + 1]) << (16 * i);
   }
   return make_uint2(lo, hi);
+}
+
+// UE8M0 (power-of-two) block scale, the other reading of the packed input
+// scales: the smallest s = 2^e with max(amax, 1e-4) / s <= 448.  Writing
+// a = (1 + m / 2^23) * 2^E and 448 = 1.75 * 2^8, a <= 1.75 * 2^(e + 8) first
+// holds at e = E - 8 when m <= 0.75 * 2^23 and at e = E - 7 otherwise; the
+// floor keeps a normal, so e stays in [-22, 120].  *byte = e + 127, so that
+// s = 2^(byte - 127).  An infinite maximum gives s = inf and byte 0xFF (the
+// codes then follow the non-finite division path).  x / s is then exact (a
+// power-of-two divisor), so quant8 with this s gives e4m3(x / s).  Host and
+// device share this code (the host copy is exported for the tests).
+__host__ __device__ inline float block_scale_ue8m0(float amax, uint8_t* byte) {
+  const float a = fmaxf(amax, kQuantFloor);
+  uint32_t bits;
+  memcpy(&bits, &a, sizeof(bits));
+  const int E = static_cast<int>((bits >> 23) & 0xFFu) - 127;
+  if (E == 128) {
+    *byte = 0xFF;
+    return a;
+  }
+  const int e = E - 8 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  *byte = static_cast<uint8_t>(e + 127);
+  const uint32_t sbits = static_cast<uint32_t>(e + 127) << 23;
+  float s;
+  memcpy(&s, &sbits, sizeof(s));
+  return s;
 }
 
 // s = max(amax, 1e-4) / 448 rounded to nearest: the same one-step correction

@@ -17,10 +17,14 @@ namespace {
 
 // ---------------------------------------------------------------- a1
 // One warp covers 256 columns of one row: lanes 0-15 block 2w, 16-31 block 2w+1.
+// kUE8M0: power-of-two block scales (block_scale_ue8m0), their exponent bytes
+// also stored to e8 when it is given.
+template <bool kUE8M0>
 __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __restrict__ x,
                                                           int64_t M, int64_t KB, int64_t ldx,
                                                           uint8_t* __restrict__ q, int64_t ldq,
-                                                          float* __restrict__ s, int64_t s_ld) {
+                                                          float* __restrict__ s, int64_t s_ld,
+                                                          uint8_t* __restrict__ e8) {
   grid_dependency_wait();
   grid_launch_dependents();
   const int64_t warps_per_row = (KB + 1) / 2;
@@ -41,9 +45,13 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __rest
   for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
   amax = half_warp_max(amax);
   if (!active) return;
-  const float sc = block_scale(amax);
+  uint8_t byte = 0;
+  const float sc = kUE8M0 ? block_scale_ue8m0(amax, &byte) : block_scale(amax);
   *reinterpret_cast<uint2*>(q + m * ldq + col) = quant8(f, sc);
-  if ((lane & 15) == 0) s[kb * s_ld + m] = sc;
+  if ((lane & 15) == 0) {
+    s[kb * s_ld + m] = sc;
+    if (kUE8M0 && e8 != nullptr) e8[kb * s_ld + m] = byte;
+  }
 }
 
 // ---------------------------------------------------------------- a3
@@ -215,8 +223,29 @@ extern "C" int moe_quant_fp8(const uint16_t* x, int64_t M, int64_t K, int64_t ld
   MOE_CHECK_ARG(ldx >= K && ldx % 8 == 0 && ldq >= K && ldq % 16 == 0 && s_ld >= M);
   if (int st = check_device()) return st;
   const int64_t warps = M * ((K / 128 + 1) / 2);
-  return launch_pdl(quant_1x128_kernel, grid_for_warps(warps), 256, 0, as_stream(stream), x, M,
-                    K / 128, ldx, q, ldq, s, s_ld);
+  return launch_pdl(quant_1x128_kernel<false>, grid_for_warps(warps), 256, 0, as_stream(stream), x, M,
+                    K / 128, ldx, q, ldq, s, s_ld, static_cast<uint8_t*>(nullptr));
+}
+
+extern "C" int moe_quant_fp8_ue8m0(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                                   int64_t ldq, float* s, uint8_t* e8, int64_t s_ld, int32_t* err,
+                                   void* stream) {
+  (void)err;
+  MOE_CHECK_ARG(M >= 0 && K > 0 && K % 128 == 0);
+  if (M == 0) return MOE_OK;
+  MOE_CHECK_ARG(x && q && s && aligned16(x) && aligned16(q) && aligned16(s));
+  MOE_CHECK_ARG(ldx >= K && ldx % 8 == 0 && ldq >= K && ldq % 16 == 0 && s_ld >= M);
+  if (int st = check_device()) return st;
+  const int64_t warps = M * ((K / 128 + 1) / 2);
+  return launch_pdl(quant_1x128_kernel<true>, grid_for_warps(warps), 256, 0, as_stream(stream), x, M,
+                    K / 128, ldx, q, ldq, s, s_ld, e8);
+}
+
+extern "C" float moe_ue8m0_scale(float amax, uint8_t* byte_out) {
+  uint8_t byte = 0;
+  const float s = block_scale_ue8m0(amax, &byte);
+  if (byte_out != nullptr) *byte_out = byte;
+  return s;
 }
 
 extern "C" int moe_quant_weight_fp8(const uint16_t* w, int64_t E, int64_t N, int64_t K, uint8_t* q,

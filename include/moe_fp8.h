@@ -113,6 +113,25 @@ int moe_quant_fp8(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
                   int32_t *err, void *stream);
 
 /*
+ * a1 with power-of-two (UE8M0) block scales -- the alternative reading of the
+ * DeepGEMM bullet's "packing of the input scales" ("Deploying DeepSeek on
+ * GB200 NVL72 with PD and Large Scale EP (Part I)", Implementation details),
+ * the scale format of the hardware block-scaled MMA.  Per row m and block kb:
+ *   s = 2^e, e the smallest integer with max(amax, 1e-4) / 2^e <= 448
+ *   q = e4m3_rne_satfinite( x / s )                  (exact: s is a power of two)
+ * x, q, s, s_ld as moe_quant_fp8 (s holds the float value 2^e);
+ * e8 : device uint8 (may be NULL), e8[kb * s_ld + m] = e + 127.
+ */
+int moe_quant_fp8_ue8m0(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                        uint8_t *q, int64_t ldq, float *s, uint8_t *e8, int64_t s_ld,
+                        int32_t *err, void *stream);
+
+/* The UE8M0 block-scale rule above for one block maximum, on the host:
+ * returns s = 2^e and stores e + 127 in *byte_out (may be NULL).  An
+ * infinite maximum gives s = inf and byte 0xFF. */
+float moe_ue8m0_scale(float amax, uint8_t *byte_out);
+
+/*
  * a3 -- 128x128 block weight quantisation (set-up, not on the timed path).
  * The a1 rule with amax taken over each 128x128 tile.
  * w : device bf16 [E, N, K] (K-major: the GEMM's B operand, out x in).

@@ -144,3 +144,24 @@ def test_masked_gemm_dispatch_is_host_logic(so):
     assert v(1024, 200, moe.MOE_GEMM_FORCE_WEIGHTS_M) == 256
     assert v(1000, 200, moe.MOE_GEMM_FORCE_WEIGHTS_M) == moe.MOE_ERR_UNSUPPORTED   # max_m % 16
     assert v(1000, 2) == 0                                 # weights-as-M needs max_m % 16 == 0
+
+
+def test_ue8m0_scale_rule_matches_the_oracle(so):
+    # the library's power-of-two block-scale rule (the code the UE8M0 quant
+    # kernel runs, compiled for the host here) against the oracle's, bit for
+    # bit: exact boundaries 448 * 2^j, their float32 neighbours, random maxima,
+    # the floor and below it, the bf16 maximum
+    import numpy as np
+    import fp8_grouped_expert_x128_gb300 as moe
+    from oracle.ffn import _block_scale_ue8m0
+    rng = np.random.default_rng(7)
+    edges = (448.0 * np.exp2(np.arange(-30, 120))).astype(np.float32)
+    amax = np.concatenate([edges, np.nextafter(edges, np.float32(np.inf)), np.nextafter(edges, np.float32(0)),
+                           np.exp2(rng.uniform(-40, 127, 2000)).astype(np.float32),
+                           np.float32([0.0, 1e-30, 1e-4, 2e-4, 3.3895314e38])])
+    amax = amax[np.isfinite(amax)]
+    ref_s, ref_b = _block_scale_ue8m0(amax)
+    for a, rs, rb in zip(amax, ref_s, ref_b):
+        s, b = moe.moe_ue8m0_scale(float(a))
+        assert np.float32(s) == rs and b == int(rb), (a, s, b, rs, rb)
+    assert moe.moe_ue8m0_scale(float("inf")) == (float("inf"), 0xFF)

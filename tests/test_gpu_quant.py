@@ -151,3 +151,68 @@ def test_weight_quant_full_size_expert(lib):
     rq, rs = oracle_weights("c2", "w2", (1,))
     assert np.array_equal(s.cpu().numpy(), rs)
     assert np.array_equal(u8(q), rq)
+
+
+def _gpu_quant_ue8m0(lib, xbits, s_ld=None):
+    M, K = xbits.shape
+    x = from_bits(xbits)
+    s_ld = s_ld or max(4, (M + 3) // 4 * 4)
+    q = torch.full((M, K), SENTINEL_U8, dtype=torch.uint8, device="cuda")
+    s = torch.full((K // 128, s_ld), SENTINEL_F32, dtype=torch.float32, device="cuda")
+    e8 = torch.full((K // 128, s_ld), 0xA5, dtype=torch.uint8, device="cuda")
+    lib.moe_quant_fp8_ue8m0(x, q, s, e8, s_ld)
+    torch.cuda.synchronize()
+    return u8(q), s.cpu().numpy(), e8.cpu().numpy()
+
+
+def _assert_ue8m0_equal(lib, xbits):
+    q, s, e8 = _gpu_quant_ue8m0(lib, xbits)
+    rq, rs, rb = oracle.quant_1x128_ue8m0(oracle.bf16_decode(xbits).astype(np.float32))
+    M = xbits.shape[0]
+    assert np.array_equal(s[:, :M], rs), "scales differ"
+    assert np.array_equal(e8[:, :M], rb), "scale bytes differ"
+    assert (s[:, M:] == SENTINEL_F32).all() and (e8[:, M:] == 0xA5).all(), "padding columns written"
+    mism = np.nonzero(q != rq)
+    assert mism[0].size == 0, f"{mism[0].size} codes differ, first at {mism[0][0]},{mism[1][0]}"
+
+
+def test_quant_ue8m0_configs_bitexact(lib):
+    # power-of-two (UE8M0) block scales: codes, scales and exponent bytes equal
+    # the oracle's on the tiny config and a prefill sample with 20x outliers
+    _assert_ue8m0_equal(lib, activations_bits("c1", 64))
+    _assert_ue8m0_equal(lib, activations_bits("c3", 600))
+
+
+def test_quant_ue8m0_every_bf16_value_under_three_scales(lib):
+    # blocks whose maximum is 448 * 2^j hold every finite bf16 magnitude <= 448
+    # scaled by 2^j (both signs): s = 2^j and q = e4m3(x / 2^j) exactly
+    allv = oracle.bf16_decode(np.arange(65536, dtype=np.uint32).astype(np.uint16))
+    vals = allv[np.isfinite(allv) & (np.abs(allv) <= 448.0)]
+    for j in (-9, 0, 5):
+        v = oracle.bf16_encode(vals * 2.0 ** j)
+        nb = -(-v.size // 127)
+        blocks = np.zeros((nb + (-nb) % 4, 128), np.uint16)
+        blocks[:nb, 0] = oracle.bf16_encode(np.array([448.0 * 2.0 ** j]))[0]
+        flat = np.zeros(nb * 127, np.uint16)
+        flat[:v.size] = v
+        blocks[:nb, 1:] = flat.reshape(nb, 127)
+        _assert_ue8m0_equal(lib, blocks.reshape(-1, 512))
+
+
+def test_quant_ue8m0_edge_cases(lib):
+    rng = np.random.default_rng(8)
+    M, K = 21, 384
+    x = rng.standard_normal((M, K))
+    x[0] = 0.0                          # all zero: floor scale 2^-22, zero codes
+    x[1, :128] = -0.0
+    x[2] *= 1e-30                       # below the floor
+    x[3] *= 1e4
+    x[4, 5] = 3.0e38                    # near the bf16 maximum: s = 2^120
+    x[5, :] = 2.0 ** -20
+    x[6, 130] = -7.0
+    x[7, 256:] = 448.0                  # exactly 448: s = 1
+    x[8, 256:] = 448.0 * (1 + 2 ** -7)  # just above: s = 2
+    _assert_ue8m0_equal(lib, oracle.bf16_encode(x))
+    q, s, e8 = _gpu_quant_ue8m0(lib, oracle.bf16_encode(x))
+    assert s[0, 0] == np.float32(2.0 ** -22) and e8[0, 0] == 105
+    assert s[2, 7] == 1.0 and s[2, 8] == 2.0
