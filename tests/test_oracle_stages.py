@@ -138,6 +138,30 @@ def test_ue8m0_against_fp32_scales():
         assert (err <= np.abs(x) * 2.0 ** -4 + sc * 2.0 ** -10 + 1e-30).all()
 
 
+def test_ue8m0_gemm_within_tolerance_of_the_fp32_scale_gemm():
+    # tolerance-only parity between the two readings of the input scales: the
+    # block-scaled GEMM with UE8M0 activation scales stays as close to the exact
+    # float64 product as the fp32-scale one, up to the factor the coarser
+    # scale grid allows (a power of two wastes under one bit of E4M3 range)
+    rng = np.random.default_rng(99)
+    x = (rng.standard_normal((96, 512)) * np.exp2(rng.integers(-3, 4, (96, 4))).repeat(128, 1)).astype(np.float32)
+    x = bf16_decode(bf16_encode(x)).astype(np.float32)
+    w = bf16_decode(bf16_encode(rng.standard_normal((256, 512)) / np.sqrt(512))).astype(np.float32)
+    exact = x.astype(np.float64) @ w.astype(np.float64).T
+    qb, sb = quant_128x128(w)
+    qa32, sa32 = quant_1x128(x)
+    qa8, sa8, _ = oracle.quant_1x128_ue8m0(x)
+    rel = lambda y: np.sqrt(np.mean((y - exact) ** 2) / np.mean(exact ** 2))
+    e32 = rel(gemm_block_scaled(qa32, sa32, qb, sb))
+    e8 = rel(gemm_block_scaled(qa8, sa8, qb, sb))
+    assert 0 < e32 < 0.05 and 0 < e8 < 0.05
+    assert e8 < 2.0 * e32
+    # the two readings differ by quantisation noise, far beyond the bf16-level
+    # GEMM tolerance: parity between them is at this level only
+    d8, d32 = gemm_block_scaled(qa8, sa8, qb, sb), gemm_block_scaled(qa32, sa32, qb, sb)
+    assert 0 < np.sqrt(np.mean((d8 - d32) ** 2) / np.mean(d32 ** 2)) < e8 + e32
+
+
 def test_quant_128x128_tiles_are_independent():
     w = _bf16(RNG.standard_normal((256, 384)) * 0.05)
     q, s = quant_128x128(w)
