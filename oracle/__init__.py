@@ -29,13 +29,15 @@ Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 """
 from .fp8 import (bf16_decode, bf16_encode, e4m3_decode, e4m3_encode,
                   e4m3_encode_bruteforce, E4M3_MAX)
-from .ffn import (quant_1x128, quant_1x128_ue8m0, quant_128x128, permute, gemm_block_scaled,
+from .ffn import (quant_1x128, quant_1x128_ue8m0, quant_128x128, quant_128x128_ue8m0, permute,
+                  gemm_block_scaled,
                   gemm_masked, gemm_contig, swiglu, swiglu_quant, combine,
                   ffn_chain, SCALE_FLOOR)
 
 __all__ = [
     "bf16_decode", "bf16_encode", "e4m3_decode", "e4m3_encode", "e4m3_encode_bruteforce",
-    "E4M3_MAX", "quant_1x128", "quant_1x128_ue8m0", "quant_128x128", "permute", "gemm_block_scaled",
+    "E4M3_MAX", "quant_1x128", "quant_1x128_ue8m0", "quant_128x128", "quant_128x128_ue8m0", "permute",
+    "gemm_block_scaled",
     "gemm_masked", "gemm_contig", "swiglu", "swiglu_quant", "combine", "ffn_chain",
     "SCALE_FLOOR",
 ]

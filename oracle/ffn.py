@@ -104,6 +104,22 @@ def quant_128x128(w) -> tuple[np.ndarray, np.ndarray]:
     return q, s
 
 
+def quant_128x128_ue8m0(w) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """128x128 block E4M3 quantisation of a K-major weight [N, K] with power-of-two
+    (UE8M0) tile scales: the rule of ``quant_1x128_ue8m0`` with amax over the
+    whole tile.  Returns q [N, K] uint8, s [N/128, K/128] float32 (2^e) and the
+    bytes e + 127 [N/128, K/128] uint8."""
+    w = np.asarray(w, dtype=np.float32)
+    N, K = w.shape
+    assert N % BLOCK == 0 and K % BLOCK == 0
+    tiles = w.reshape(N // BLOCK, BLOCK, K // BLOCK, BLOCK)
+    amax = np.abs(tiles).max(axis=(1, 3))                   # [NB, KB]
+    s, byte = _block_scale_ue8m0(amax)
+    y = tiles.astype(np.float64) / s[:, None, :, None].astype(np.float64)   # exact
+    q = e4m3_encode(y).reshape(N, K)
+    return q, s, byte
+
+
 def permute(topk_ids, expert_begin: int, E: int, layout: str, max_m: int = 0,
             align: int = BLOCK, q=None, s=None) -> dict:
     """Route token-order assignments into the grouped layout of the local experts.

@@ -138,6 +138,22 @@ def test_ue8m0_against_fp32_scales():
         assert (err <= np.abs(x) * 2.0 ** -4 + sc * 2.0 ** -10 + 1e-30).all()
 
 
+def test_ue8m0_weight_tiles():
+    # 128x128 tiles with UE8M0 scales: each tile's scale is the smallest power
+    # of two for its own maximum (brute force), tiles are independent, and the
+    # codes are the brute-force encoding of w / s
+    w = (RNG.standard_normal((256, 384)) * np.exp2(RNG.integers(-8, 8, (2, 1, 3, 1)))
+         .repeat(128, 1).reshape(2, 128, 3, 1).repeat(128, 3).reshape(256, 384)).astype(np.float32)
+    q, s, byte = oracle.quant_128x128_ue8m0(w)
+    for nb in range(2):
+        for kb in range(3):
+            tile = w[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128]
+            e = _smallest_pow2_exponent(max(float(np.abs(tile).max()), float(np.float32(1e-4))))
+            assert s[nb, kb] == np.float32(2.0 ** e) and int(byte[nb, kb]) == e + 127
+            ref = oracle.e4m3_encode_bruteforce(tile.astype(np.float64) / 2.0 ** e)
+            assert np.array_equal(q[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128], ref)
+
+
 def test_ue8m0_gemm_within_tolerance_of_the_fp32_scale_gemm():
     # tolerance-only parity between the two readings of the input scales: the
     # block-scaled GEMM with UE8M0 activation scales stays as close to the exact
