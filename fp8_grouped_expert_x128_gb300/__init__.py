@@ -42,6 +42,8 @@ MOE_GEMM_FORCE_WEIGHTS_M = 0x2
 MOE_FFN_FUSE_SWIGLU = 0x4
 MOE_GEMM_CTA_PAIR = 0x8
 MOE_GEMM_DEBUG_STALL = 0x100
+MOE_QUANT_UE8M0 = 0x1
+MOE_COMBINE_ACCUMULATE = 0x1
 
 EXPORTED = [
     "moe_status_string", "moe_version", "moe_read_device_status", "moe_quant_fp8",
@@ -76,7 +78,7 @@ _sig("moe_status_string", ctypes.c_char_p, [ctypes.c_int])
 _sig("moe_version", ctypes.c_int, [])
 _sig("moe_read_device_status", ctypes.c_int,
      [_P, _P, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(_I32)])
-_sig("moe_quant_fp8", ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P])
+_sig("moe_quant_fp8", ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _I32, _P, _P])
 _sig("moe_quant_fp8_ue8m0", ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _I64, _P, _P])
 _sig("moe_ue8m0_scale", ctypes.c_float, [ctypes.c_float, ctypes.POINTER(ctypes.c_uint8)])
 _sig("moe_quant_weight_fp8", ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P])
@@ -90,7 +92,7 @@ _sig("moe_gemm_fp8_masked", ctypes.c_int,
      [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I32, _P, _P])
 _sig("moe_gemm_fp8_masked_variant", ctypes.c_int, [_I32, _I32, _I32])
 _sig("moe_swiglu_quant", ctypes.c_int, [_P, _I64, _I32, _P, _I32, _P, _P, _P, _I64, _P, _P])
-_sig("moe_combine", ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I32, _I32, _P, _I64, _P, _P])
+_sig("moe_combine", ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I32, _I32, _P, _I64, _I32, _P, _I64, _P, _P])
 _sig("moe_ffn_workspace_size", ctypes.c_size_t, [ctypes.POINTER(moe_ffn_desc)])
 _sig("moe_ffn_kernel_count", ctypes.c_int, [ctypes.POINTER(moe_ffn_desc)])
 _sig("moe_ffn", ctypes.c_int, [ctypes.POINTER(moe_ffn_desc), _P, ctypes.c_size_t, _P])
@@ -160,13 +162,14 @@ def moe_contig_rows_bound(assignments: int, E: int) -> int:
     return int(_lib.moe_contig_rows_bound(assignments, E))
 
 
-def moe_quant_fp8(x, q, s, s_ld=None, err=None, stream=None):
-    """a1: x bf16 [M, K] -> q uint8 [M, K], s fp32 [K/128, s_ld] (s[kb, m])."""
+def moe_quant_fp8(x, q, s, s_ld=None, flags=0, err=None, stream=None):
+    """a1: x bf16 [M, K] -> q uint8 [M, K], s fp32 [K/128, s_ld] (s[kb, m]);
+    flags = MOE_QUANT_UE8M0 for power-of-two scales."""
     _dev(x, torch.bfloat16, "x"); _dev(q, _U8, "q"); _dev(s, torch.float32, "s")
     M, K = x.shape
     s_ld = s.shape[-1] if s_ld is None else s_ld
     _check(_lib.moe_quant_fp8(_ptr(x), M, K, x.stride(0), _ptr(_u8(q)), q.stride(0), _ptr(s), s_ld,
-                              _ptr(err), _stream(stream)), "moe_quant_fp8")
+                              flags, _ptr(err), _stream(stream)), "moe_quant_fp8")
     return q, s
 
 
@@ -252,12 +255,15 @@ def moe_swiglu_quant(Y1, q, s, counts=None, max_m=0, m_indices=None, s_ld=0, err
            "moe_swiglu_quant")
 
 
-def moe_combine(Y2, dst_row, topk_w, out, err=None, stream=None):
-    """a7: out[t] = bf16(sum_j w[t,j] * Y2[dst_row[t*k+j]]); Y2 viewed as [rows, H]."""
+def moe_combine(Y2, dst_row, topk_w, out, shared=None, flags=0, err=None, stream=None):
+    """a7: out[t] = bf16((out[t] if ACCUMULATE) + sum_j w[t,j] * Y2[dst_row[t*k+j]] + shared[t]);
+    Y2 viewed as [rows, H]; shared (optional) bf16 [T, H]."""
     H = Y2.shape[-1]
     rows = Y2.numel() // H
     T, k = topk_w.shape
-    _check(_lib.moe_combine(_ptr(Y2), H, rows, _ptr(dst_row), _ptr(topk_w), T, k, H, _ptr(out),
+    _dev(shared, torch.bfloat16, "shared")
+    _check(_lib.moe_combine(_ptr(Y2), H, rows, _ptr(dst_row), _ptr(topk_w), T, k, H, _ptr(shared),
+                            shared.stride(0) if shared is not None else 0, flags, _ptr(out),
                             out.stride(0), _ptr(err), _stream(stream)), "moe_combine")
     return out
 

@@ -145,7 +145,7 @@ extern "C" const char* moe_status_string(int status) {
   }
 }
 
-extern "C" int moe_version(void) { return 100; }
+extern "C" int moe_version(void) { return 200; }
 
 extern "C" int moe_read_device_status(int32_t* err, void* stream, int* status_out,
                                       int32_t* raw_bits_out) {
@@ -342,7 +342,8 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
   if (rc) return rc;
   if ((rc = mark(5))) return rc;
   if (!fuse_combine &&
-      (rc = moe_combine(y2, d->H, p.rows, dst, d->topk_w, d->T, d->k, d->H, d->out, d->H, d->err, stream)))
+      (rc = moe_combine(y2, d->H, p.rows, dst, d->topk_w, d->T, d->k, d->H, nullptr, 0, 0, d->out, d->H, d->err,
+                        stream)))
     return rc;
   return mark(6);
 }

@@ -102,6 +102,7 @@ struct GemmArgs {
   const int32_t* counts;     // masked
   const int32_t* offsets;    // contiguous
   const int32_t* m_indices;  // contiguous
+  int64_t M_capacity;        // contiguous: rows of A / D / m_indices
   uint16_t* D;
   int64_t ldd;
   int32_t E, N, K, max_m, layout;
@@ -153,7 +154,14 @@ __device__ void build_schedule(const GemmArgs& p, const Sched& s, int n_tiles) {
     } else {
       rb = p.offsets[e];
       rx = p.offsets[e + 1] - rb;
-      if ((rb % BM) != 0 || rx < 0 || (rx % BM) != 0) { bad = true; rx = 0; }
+      // a segment must start on a 128-row boundary and lie inside the
+      // M_capacity rows of A, D and m_indices; otherwise it is skipped
+      if (rb < 0 || (rb % BM) != 0 || rx < 0 || (rx % BM) != 0 ||
+          static_cast<int64_t>(rb) + rx > p.M_capacity) {
+        bad = true;
+        rb = 0;
+        rx = 0;
+      }
     }
     s.rbase[e] = rb;
     s.rext[e] = rx;
@@ -1313,6 +1321,7 @@ int gemm_contig_swiglu(const uint8_t* A, int64_t lda, const float* sA, int64_t s
   a.sB = sB;
   a.offsets = offsets;
   a.m_indices = m_indices;
+  a.M_capacity = M_capacity;
   a.E = E;
   a.N = N;
   a.K = K;
@@ -1373,6 +1382,7 @@ int gemm_contig_combine1(const uint8_t* A, int64_t lda, const float* sA, int64_t
   a.sB = sB;
   a.offsets = offsets;
   a.m_indices = m_indices;
+  a.M_capacity = M_capacity;
   a.E = E;
   a.N = N;
   a.K = K;
@@ -1410,6 +1420,7 @@ extern "C" int moe_gemm_fp8_contig(const uint8_t* A, int64_t lda, const float* s
   a.sB = sB;
   a.offsets = offsets;
   a.m_indices = m_indices;
+  a.M_capacity = M_capacity;
   a.D = D;
   a.ldd = ldd;
   a.E = E;

@@ -15,7 +15,8 @@
 // and a per-warp table in shared memory; a second kernel copies the 1-byte
 // rows (16-byte vectors, one warp per row) and gathers their fp32 scales, or --
 // inside moe_ffn -- quantises the bf16 token rows straight into their slots.
-// combine: one CTA per token, fp32 accumulation over the k choices in order.
+// combine: a resident wave of CTAs over the tokens, fp32 accumulation over the
+// k choices in order (then the optional shared-expert row).
 #include "common.cuh"
 
 namespace moe {
@@ -321,10 +322,23 @@ __global__ void __launch_bounds__(32 * kQsWarps, kQsWarps == 4 ? 6 : 4) quant_sc
 constexpr int kCombThreads = 128;
 constexpr int kCombVec = 8;
 
+// Optional terms (both default off): with `accumulate` the sum starts from the
+// output row's current value, and `shared` (a bf16 [T, H] row per token, row
+// stride lds) is added with weight 1 after the slots -- the same fp32 steps as
+// one more routing slot of weight 1, so the bits equal that formulation.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+  const uint32_t x[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    f[2 * h] = __uint_as_float(x[h] << 16);
+    f[2 * h + 1] = __uint_as_float(x[h] & 0xFFFF0000u);
+  }
+}
+
 __global__ void __launch_bounds__(kCombThreads) combine_kernel(
     const uint16_t* __restrict__ y2, int64_t ldy, int64_t y_rows, const int32_t* __restrict__ dst_row,
-    const float* __restrict__ topk_w, int32_t k, int64_t H, uint16_t* __restrict__ out, int64_t ldo,
-    int64_t T, int32_t* err) {
+    const float* __restrict__ topk_w, int32_t k, int64_t H, const uint16_t* __restrict__ shared, int64_t lds,
+    int accumulate, uint16_t* __restrict__ out, int64_t ldo, int64_t T, int32_t* err) {
   grid_dependency_wait();
   grid_launch_dependents();
   __shared__ int32_t s_dst[32];
@@ -366,9 +380,15 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(
     for (int64_t base = 0; base < H; base += static_cast<int64_t>(kCombThreads) * 8 * kCombVec) {
       float acc[kCombVec][8];
 #pragma unroll
-      for (int v = 0; v < kCombVec; ++v)
+      for (int v = 0; v < kCombVec; ++v) {
+        const int64_t c = base + (static_cast<int64_t>(v) * kCombThreads + tid) * 8;
+        if (accumulate && c < H) {
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(out + t * ldo + c), acc[v]);
+        } else {
 #pragma unroll
-        for (int h = 0; h < 8; ++h) acc[v][h] = 0.f;
+          for (int h = 0; h < 8; ++h) acc[v][h] = 0.f;
+        }
+      }
       for (int jj = 0; jj < n; ++jj) {
         const uint16_t* row = y2 + static_cast<int64_t>(s_dst[jj]) * ldy;
         const float w = s_w[jj];
@@ -386,6 +406,17 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(
             acc[v][2 * h] = fmaf(w, __uint_as_float(x[h] << 16), acc[v][2 * h]);
             acc[v][2 * h + 1] = fmaf(w, __uint_as_float(x[h] & 0xFFFF0000u), acc[v][2 * h + 1]);
           }
+        }
+      }
+      if (shared != nullptr) {
+#pragma unroll
+        for (int v = 0; v < kCombVec; ++v) {
+          const int64_t c = base + (static_cast<int64_t>(v) * kCombThreads + tid) * 8;
+          if (c >= H) continue;
+          float f[8];
+          bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(shared + t * lds + c)), f);
+#pragma unroll
+          for (int h = 0; h < 8; ++h) acc[v][h] = fmaf(1.0f, f[h], acc[v][h]);
         }
       }
 #pragma unroll
@@ -416,8 +447,8 @@ constexpr int kCombLatSlots = 4;
 
 __global__ void __launch_bounds__(kCombLatThreads) combine_latency_kernel(
     const uint16_t* __restrict__ y2, int64_t ldy, int64_t y_rows, const int32_t* __restrict__ dst_row,
-    const float* __restrict__ topk_w, int32_t k, int64_t H, uint16_t* __restrict__ out, int64_t ldo,
-    int32_t* err) {
+    const float* __restrict__ topk_w, int32_t k, int64_t H, const uint16_t* __restrict__ shared, int64_t lds,
+    int accumulate, uint16_t* __restrict__ out, int64_t ldo, int32_t* err) {
   grid_dependency_wait();
   grid_launch_dependents();
   __shared__ int32_t s_dst[32];
@@ -449,9 +480,15 @@ __global__ void __launch_bounds__(kCombLatThreads) combine_latency_kernel(
   for (int64_t base = 0; base < H; base += static_cast<int64_t>(kCombLatThreads) * 8 * kCombLatVec) {
     float acc[kCombLatVec][8];
 #pragma unroll
-    for (int v = 0; v < kCombLatVec; ++v)
+    for (int v = 0; v < kCombLatVec; ++v) {
+      const int64_t c = base + (static_cast<int64_t>(v) * kCombLatThreads + tid) * 8;
+      if (accumulate && c < H) {
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(out + t * ldo + c), acc[v]);
+      } else {
 #pragma unroll
-      for (int h = 0; h < 8; ++h) acc[v][h] = 0.f;
+        for (int h = 0; h < 8; ++h) acc[v][h] = 0.f;
+      }
+    }
     for (int j0 = 0; j0 < n; j0 += kCombLatSlots) {
       uint4 u[kCombLatSlots][kCombLatVec];
 #pragma unroll
@@ -476,6 +513,17 @@ __global__ void __launch_bounds__(kCombLatThreads) combine_latency_kernel(
             acc[v][2 * h + 1] = fmaf(w, __uint_as_float(x[h] & 0xFFFF0000u), acc[v][2 * h + 1]);
           }
         }
+      }
+    }
+    if (shared != nullptr) {
+#pragma unroll
+      for (int v = 0; v < kCombLatVec; ++v) {
+        const int64_t c = base + (static_cast<int64_t>(v) * kCombLatThreads + tid) * 8;
+        if (c >= H) continue;
+        float f[8];
+        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(shared + t * lds + c)), f);
+#pragma unroll
+        for (int h = 0; h < 8; ++h) acc[v][h] = fmaf(1.0f, f[h], acc[v][h]);
       }
     }
 #pragma unroll
@@ -587,18 +635,22 @@ extern "C" int moe_permute(const uint8_t* q, const float* s, int64_t s_ld, const
 }
 
 extern "C" int moe_combine(const uint16_t* Y2, int64_t ldy, int64_t y_rows, const int32_t* dst_row,
-                           const float* topk_w, int64_t T, int32_t k, int32_t H, uint16_t* out,
-                           int64_t ldo, int32_t* err, void* stream) {
+                           const float* topk_w, int64_t T, int32_t k, int32_t H, const uint16_t* shared_or_null,
+                           int64_t lds, int32_t flags, uint16_t* out, int64_t ldo, int32_t* err, void* stream) {
   MOE_CHECK_ARG(T >= 0 && k >= 1 && k <= 32 && H > 0 && H % 8 == 0);
+  MOE_CHECK_ARG((flags & ~MOE_COMBINE_ACCUMULATE) == 0);
   if (T == 0) return MOE_OK;
   MOE_CHECK_ARG(Y2 && dst_row && topk_w && out && aligned16(Y2) && aligned16(out));
   MOE_CHECK_ARG(ldy >= H && ldy % 8 == 0 && ldo >= H && ldo % 8 == 0 && y_rows >= 0);
+  if (shared_or_null != nullptr) MOE_CHECK_ARG(aligned16(shared_or_null) && lds >= H && lds % 8 == 0);
   MOE_CHECK_ARG(T < (1ll << 31));
   if (int st = check_device()) return st;
+  const int acc = (flags & MOE_COMBINE_ACCUMULATE) ? 1 : 0;
   // a few tokens (up to one per SM): one wide CTA per token, slots' loads in flight together
   if (T <= num_sms())
     return launch_pdl(combine_latency_kernel, static_cast<unsigned>(T), kCombLatThreads, 0, as_stream(stream), Y2,
-                      ldy, y_rows, dst_row, topk_w, k, static_cast<int64_t>(H), out, ldo, err);
+                      ldy, y_rows, dst_row, topk_w, k, static_cast<int64_t>(H), shared_or_null, lds, acc, out, ldo,
+                      err);
   static int per_sm[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
@@ -608,6 +660,6 @@ extern "C" int moe_combine(const uint16_t* Y2, int64_t ldy, int64_t y_rows, cons
     return MOE_ERR_CUDA;
   const int64_t wave = static_cast<int64_t>(num_sms()) * per_sm[dev];
   return launch_pdl(combine_kernel, static_cast<unsigned>(T < wave ? T : wave), kCombThreads, 0,
-                    as_stream(stream), Y2, ldy, y_rows, dst_row, topk_w, k, static_cast<int64_t>(H), out, ldo, T,
-                    err);
+                    as_stream(stream), Y2, ldy, y_rows, dst_row, topk_w, k, static_cast<int64_t>(H), shared_or_null,
+                    lds, acc, out, ldo, T, err);
 }

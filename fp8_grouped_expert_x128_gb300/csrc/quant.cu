@@ -215,8 +215,10 @@ inline unsigned grid_for_warps(int64_t warps) {
 using namespace moe;
 
 extern "C" int moe_quant_fp8(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
-                             int64_t ldq, float* s, int64_t s_ld, int32_t* err, void* stream) {
+                             int64_t ldq, float* s, int64_t s_ld, int32_t flags, int32_t* err, void* stream) {
   (void)err;
+  MOE_CHECK_ARG((flags & ~MOE_QUANT_UE8M0) == 0);
+  if (flags & MOE_QUANT_UE8M0) return moe_quant_fp8_ue8m0(x, M, K, ldx, q, ldq, s, nullptr, s_ld, err, stream);
   MOE_CHECK_ARG(M >= 0 && K > 0 && K % 128 == 0);
   if (M == 0) return MOE_OK;
   MOE_CHECK_ARG(x && q && s && aligned16(x) && aligned16(q) && aligned16(s));

@@ -83,6 +83,12 @@ extern "C" {
                                          consumer's bounded wait expires and the call
                                          reports MOE_DEV_TIMEOUT (no hang, no trap)      */
 
+/* moe_quant_fp8 flags */
+#define MOE_QUANT_UE8M0 0x1           /* power-of-two block scales (the rule of
+                                         moe_quant_fp8_ue8m0), written as fp32 2^e     */
+/* moe_combine flags */
+#define MOE_COMBINE_ACCUMULATE 0x1    /* add to the output's current values            */
+
 /* Human-readable name of a status code. Never NULL. */
 const char *moe_status_string(int status);
 
@@ -106,10 +112,15 @@ int moe_read_device_status(int32_t *err, void *stream, int *status_out, int32_t 
  * x  : device bf16 [M, K], row stride ldx (elements).
  * q  : device uint8 [M, K], row stride ldq (bytes).
  * s  : device fp32, one group: s[kb * s_ld + m], s_ld >= M.
+ * flags: 0, or MOE_QUANT_UE8M0 for power-of-two scales (the rule of
+ *   moe_quant_fp8_ue8m0 below; s then holds 2^e).  Unknown bits are refused.
+ * Non-finite inputs: NaN elements take no part in amax (maxNum) and encode to
+ * 0x7F; an infinite element makes s = inf, so the block's finite elements
+ * encode to signed zeros and the infinite one to 0x7F.
  * M may be 0 (nothing is launched).
  */
 int moe_quant_fp8(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
-                  uint8_t *q, int64_t ldq, float *s, int64_t s_ld,
+                  uint8_t *q, int64_t ldq, float *s, int64_t s_ld, int32_t flags,
                   int32_t *err, void *stream);
 
 /*
@@ -195,7 +206,10 @@ int moe_permute(const uint8_t *q, const float *s, int64_t s_ld,
  * moe_gemm_fp8_contig -- contiguous (prefill) layout, as moe_permute writes it:
  *   A [M_capacity, K] (row stride lda), sA[kb * sA_ld + r], offsets [E+1],
  *   m_indices [M_capacity]; D row stride ldd.  Rows with m_indices == -1 and
- *   rows >= offsets[E] are not written.  Segments must start at multiples of 128.
+ *   rows >= offsets[E] are not written.  Segments must start at multiples of 128
+ *   and lie inside [0, M_capacity): a segment that does not (offsets[e] < 0, not
+ *   a multiple of 128, decreasing, or offsets[e+1] > M_capacity) is skipped --
+ *   none of its rows is read or written -- and MOE_DEV_BAD_INDEX is set.
  */
 int moe_gemm_fp8_contig(const uint8_t *A, int64_t lda, const float *sA, int64_t sA_ld,
                         const uint8_t *B, const float *sB,
@@ -246,15 +260,22 @@ int moe_swiglu_quant(const uint16_t *Y1, int64_t rows, int32_t I,
 
 /*
  * a7 -- top-k-weighted combine back to token order (moe_combine).
- *   out[t, :] = bf16_rne( sum_j  w[t, j] * Y2[dst_row[t*k + j], :] )
- * fp32 accumulation in j order; entries with dst_row == -1 are skipped (a token
- * with none gets zeros).  Y2: device bf16 rows of H (row stride ldy),
- * dst_row: device int32 [T*k], topk_w: device fp32 [T, k], out: device bf16
- * [T, H] (row stride ldo).  dst_row values must be < y_rows (else
- * MOE_DEV_BAD_INDEX and the entry is skipped).
+ *   out[t, :] = bf16_rne( a[t, :] + sum_j  w[t, j] * Y2[dst_row[t*k + j], :] + shared[t, :] )
+ * with a = the current out row under MOE_COMBINE_ACCUMULATE (else 0) and the
+ * shared term only when shared_or_null is given (a shared expert's output,
+ * weight 1).  fp32 accumulation: a, then the slots in j order, then the shared
+ * row -- the same steps as routing the shared expert as one more slot of
+ * weight 1, so the bits equal that formulation.  Entries with dst_row == -1 are
+ * skipped (a token with none and no other term gets zeros).
+ * Y2: device bf16 rows of H (row stride ldy); dst_row: device int32 [T*k];
+ * topk_w: device fp32 [T, k]; shared_or_null: device bf16 [T, H] (row stride
+ * lds) or NULL; out: device bf16 [T, H] (row stride ldo).  flags: 0 or
+ * MOE_COMBINE_ACCUMULATE; unknown bits are refused.  dst_row values must be <
+ * y_rows (else MOE_DEV_BAD_INDEX and the entry is skipped).
  */
 int moe_combine(const uint16_t *Y2, int64_t ldy, int64_t y_rows,
                 const int32_t *dst_row, const float *topk_w, int64_t T, int32_t k, int32_t H,
+                const uint16_t *shared_or_null, int64_t lds, int32_t flags,
                 uint16_t *out, int64_t ldo, int32_t *err, void *stream);
 
 /*

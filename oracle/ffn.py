@@ -32,9 +32,20 @@ BLOCK = 128
 SCALE_FLOOR = np.float32(1e-4)
 
 
+def _block_amax(blocks: np.ndarray, axis) -> np.ndarray:
+    """max |x| over a block (exact in float32).  A reading for non-finite inputs,
+    which the pages never mention: NaN elements take no part in the maximum
+    (IEEE maxNum, what a hardware fmax reduction does), so a block whose
+    elements are all NaN has maximum 0; an infinite element makes it inf."""
+    with np.errstate(invalid="ignore"):
+        a = np.fmax.reduce(np.abs(blocks), axis=axis)
+    return np.where(np.isnan(a), np.float32(0.0), a).astype(np.float32)
+
+
 def _block_scale(amax_f32: np.ndarray) -> np.ndarray:
-    """s = float32(max(amax, 1e-4) / 448): one correctly rounded float32 division."""
-    a = np.maximum(amax_f32.astype(np.float32), SCALE_FLOOR)
+    """s = float32(max(amax, 1e-4) / 448): one correctly rounded float32 division
+    (an infinite maximum gives s = inf, and then x / s is 0 or NaN)."""
+    a = np.fmax(amax_f32.astype(np.float32), SCALE_FLOOR)
     return (a / np.float32(E4M3_MAX)).astype(np.float32)
 
 
@@ -51,9 +62,10 @@ def quant_1x128(x) -> tuple[np.ndarray, np.ndarray]:
     M, K = x.shape
     assert K % BLOCK == 0
     blocks = x.reshape(M, K // BLOCK, BLOCK)
-    amax = np.abs(blocks).max(axis=2)                       # [M, KB]
+    amax = _block_amax(blocks, 2)                            # [M, KB]
     s = _block_scale(amax)                                   # [M, KB]
-    y = (blocks / s[:, :, None]).astype(np.float32)          # float32 IEEE division
+    with np.errstate(invalid="ignore"):
+        y = (blocks / s[:, :, None]).astype(np.float32)      # float32 IEEE division
     q = e4m3_encode(y.astype(np.float64)).reshape(M, K)
     return q, np.ascontiguousarray(s.T)
 
@@ -63,12 +75,18 @@ def _block_scale_ue8m0(amax_f32: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     an unsigned 8-bit exponent, s = 2^(byte - 127)): the smallest power of two
     s with max(amax, 1e-4) / s <= 448, i.e. s = 2^ceil(log2(max(amax, 1e-4) / 448)).
     The exponent is found by exact comparisons of a against 448 * 2^e (both
-    exact in float64), not by a rounded logarithm.  Returns (s float32, byte uint8)."""
-    a = np.maximum(amax_f32.astype(np.float32), SCALE_FLOOR).astype(np.float64)
+    exact in float64), not by a rounded logarithm.  An infinite maximum has no
+    such power of two: it gives s = inf and the byte 0xFF (the all-ones UE8M0
+    exponent), so that x / s is 0 or NaN as with the float32 scale.
+    Returns (s float32, byte uint8)."""
+    a = np.fmax(amax_f32.astype(np.float32), SCALE_FLOOR).astype(np.float64)
+    inf = np.isinf(a)
+    a = np.where(inf, 1.0, a)
     e = np.ceil(np.log2(a / E4M3_MAX)).astype(np.int64)          # estimate, then make exact
     e = np.where(a > E4M3_MAX * np.exp2(e.astype(np.float64)), e + 1, e)
     e = np.where(a <= E4M3_MAX * np.exp2((e - 1).astype(np.float64)), e - 1, e)
-    return np.exp2(e.astype(np.float64)).astype(np.float32), (e + 127).astype(np.uint8)
+    s = np.where(inf, np.inf, np.exp2(e.astype(np.float64))).astype(np.float32)
+    return s, np.where(inf, 255, e + 127).astype(np.uint8)
 
 
 def quant_1x128_ue8m0(x) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
@@ -82,9 +100,10 @@ def quant_1x128_ue8m0(x) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
     M, K = x.shape
     assert K % BLOCK == 0
     blocks = x.reshape(M, K // BLOCK, BLOCK)
-    amax = np.abs(blocks).max(axis=2)
+    amax = _block_amax(blocks, 2)
     s, byte = _block_scale_ue8m0(amax)
-    y = blocks.astype(np.float64) / s[:, :, None].astype(np.float64)   # exact
+    with np.errstate(invalid="ignore"):
+        y = blocks.astype(np.float64) / s[:, :, None].astype(np.float64)   # exact
     q = e4m3_encode(y).reshape(M, K)
     return q, np.ascontiguousarray(s.T), np.ascontiguousarray(byte.T)
 
@@ -97,9 +116,10 @@ def quant_128x128(w) -> tuple[np.ndarray, np.ndarray]:
     N, K = w.shape
     assert N % BLOCK == 0 and K % BLOCK == 0
     tiles = w.reshape(N // BLOCK, BLOCK, K // BLOCK, BLOCK)
-    amax = np.abs(tiles).max(axis=(1, 3))                   # [NB, KB]
+    amax = _block_amax(tiles, (1, 3))                       # [NB, KB]
     s = _block_scale(amax)
-    y = (tiles / s[:, None, :, None]).astype(np.float32)
+    with np.errstate(invalid="ignore"):
+        y = (tiles / s[:, None, :, None]).astype(np.float32)
     q = e4m3_encode(y.astype(np.float64)).reshape(N, K)
     return q, s
 
@@ -113,9 +133,10 @@ def quant_128x128_ue8m0(w) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
     N, K = w.shape
     assert N % BLOCK == 0 and K % BLOCK == 0
     tiles = w.reshape(N // BLOCK, BLOCK, K // BLOCK, BLOCK)
-    amax = np.abs(tiles).max(axis=(1, 3))                   # [NB, KB]
+    amax = _block_amax(tiles, (1, 3))                       # [NB, KB]
     s, byte = _block_scale_ue8m0(amax)
-    y = tiles.astype(np.float64) / s[:, None, :, None].astype(np.float64)   # exact
+    with np.errstate(invalid="ignore"):
+        y = tiles.astype(np.float64) / s[:, None, :, None].astype(np.float64)   # exact
     q = e4m3_encode(y).reshape(N, K)
     return q, s, byte
 
@@ -260,32 +281,47 @@ def swiglu(y1_bits) -> np.ndarray:
     return h.astype(np.float32)
 
 
-def swiglu_quant(y1_bits) -> tuple[np.ndarray, np.ndarray]:
-    """SwiGLU followed by the 1x128 E4M3 quantisation of ``quant_1x128``."""
+def swiglu_quant(y1_bits, ue8m0: bool = False) -> tuple[np.ndarray, np.ndarray]:
+    """SwiGLU followed by the 1x128 E4M3 quantisation of ``quant_1x128`` (or, with
+    ``ue8m0``, of ``quant_1x128_ue8m0``: power-of-two scales, returned as floats)."""
+    if ue8m0:
+        q, s, _ = quant_1x128_ue8m0(swiglu(y1_bits))
+        return q, s
     return quant_1x128(swiglu(y1_bits))
 
 
-def combine(y2_bits, dst_row, topk_w) -> np.ndarray:
-    """out[t] = bf16( sum_j w[t, j] * Y2[dst_row[t*k + j]] ), float64 accumulation,
-    assignments with dst_row == -1 skipped.  y2_bits [rows, H] -> [T, H] bf16 bits."""
+def combine(y2_bits, dst_row, topk_w, shared_bits=None, out_bits=None) -> np.ndarray:
+    """out[t] = bf16( a[t] + sum_j w[t, j] * Y2[dst_row[t*k + j]] + shared[t] ), float64
+    accumulation, assignments with dst_row == -1 skipped.  y2_bits [rows, H] -> [T, H]
+    bf16 bits.  Optional terms: ``shared_bits`` [T, H], the output of a shared
+    expert every token uses at weight 1 (added, not renormalised with the top-k
+    weights -- a reading); ``out_bits`` [T, H], the current output to add to
+    (a = 0 without it)."""
     w = np.asarray(topk_w, dtype=np.float64)
     T, k = w.shape
     y = bf16_decode(y2_bits)
     out = np.zeros((T, y.shape[1]), dtype=np.float64)
+    if out_bits is not None:
+        out += bf16_decode(out_bits)
     dst = np.asarray(dst_row).reshape(T, k)
     for j in range(k):
         ok = dst[:, j] >= 0
         out[ok] += w[ok, j][:, None] * y[dst[ok, j]]
+    if shared_bits is not None:
+        out += bf16_decode(shared_bits)
     return bf16_encode(out)
 
 
 def ffn_chain(x_bits, topk_ids, topk_w, expert_begin, E, layout, max_m,
-              w13_q, w13_s, w2_q, w2_s, align: int = BLOCK) -> dict:
+              w13_q, w13_s, w2_q, w2_s, align: int = BLOCK, ue8m0: bool = False) -> dict:
     """The whole path: quant -> permute -> GEMM1 (W13) -> SwiGLU+quant -> GEMM2 (W2)
     -> combine.  Weights are pre-quantised: w13_q [E, 2I, H], w13_s [E, 2I/128, H/128],
-    w2_q [E, H, I], w2_s [E, H/128, I/128].  Returns every intermediate."""
+    w2_q [E, H, I], w2_s [E, H/128, I/128].  With ``ue8m0`` both activation
+    quantisations take power-of-two scales (the other reading of the packed
+    input scales; the weights are then expected from quant_128x128_ue8m0, their
+    scales as floats 2^e).  Returns every intermediate."""
     x = bf16_decode(x_bits).astype(np.float32)
-    q, s = quant_1x128(x)
+    q, s = quant_1x128_ue8m0(x)[:2] if ue8m0 else quant_1x128(x)
     p = permute(topk_ids, expert_begin, E, layout, max_m, align, q=q, s=s)
     if layout == "masked":
         A1 = p["q"].reshape(E, max_m, -1)
@@ -294,7 +330,7 @@ def ffn_chain(x_bits, topk_ids, topk_w, expert_begin, E, layout, max_m,
         vflat = valid.reshape(-1)
         q2 = np.zeros((E * max_m, y1f.shape[1] // 2), dtype=np.uint8)
         s2 = np.zeros((y1f.shape[1] // 2 // BLOCK, E * max_m), dtype=np.float32)
-        qq, ss = swiglu_quant(y1f[vflat])
+        qq, ss = swiglu_quant(y1f[vflat], ue8m0)
         q2[vflat], s2[:, vflat] = qq, ss
         s2m = np.ascontiguousarray(s2.reshape(-1, E, max_m).transpose(1, 0, 2))
         y2, _ = gemm_masked(q2.reshape(E, max_m, -1), s2m, w2_q, w2_s, p["counts"])
@@ -303,7 +339,7 @@ def ffn_chain(x_bits, topk_ids, topk_w, expert_begin, E, layout, max_m,
         y1f, vflat = gemm_contig(p["q"], p["s"], w13_q, w13_s, p["offsets"], p["m_indices"])
         q2 = np.zeros((p["rows"], y1f.shape[1] // 2), dtype=np.uint8)
         s2 = np.zeros((y1f.shape[1] // 2 // BLOCK, p["rows"]), dtype=np.float32)
-        qq, ss = swiglu_quant(y1f[vflat])
+        qq, ss = swiglu_quant(y1f[vflat], ue8m0)
         q2[vflat], s2[:, vflat] = qq, ss
         s2m = s2
         y2f, _ = gemm_contig(q2, s2, w2_q, w2_s, p["offsets"], p["m_indices"])

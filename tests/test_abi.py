@@ -50,7 +50,7 @@ def test_status_strings_and_version(so):
     assert moe.moe_status_string(0) == "MOE_OK"
     assert moe.moe_status_string(-5) == "MOE_ERR_TIMEOUT"
     assert moe.moe_status_string(12345) == "MOE_ERR_UNKNOWN"
-    assert moe.moe_version() >= 100
+    assert moe.moe_version() >= 200
 
 
 def test_host_side_argument_validation(so):
@@ -58,19 +58,30 @@ def test_host_side_argument_validation(so):
     lib.moe_quant_fp8.restype = ctypes.c_int
     i64, p = ctypes.c_int64, ctypes.c_void_p
     # K not a multiple of 128 -> rejected before any CUDA call
-    rc = lib.moe_quant_fp8(p(16), i64(4), i64(100), i64(100), p(16), i64(100), p(16), i64(4), None, None)
+    i32 = ctypes.c_int32
+    rc = lib.moe_quant_fp8(p(16), i64(4), i64(100), i64(100), p(16), i64(100), p(16), i64(4), i32(0), None, None)
     assert rc == -1
     # null pointers
-    rc = lib.moe_quant_fp8(None, i64(4), i64(128), i64(128), None, i64(128), None, i64(4), None, None)
+    rc = lib.moe_quant_fp8(None, i64(4), i64(128), i64(128), None, i64(128), None, i64(4), i32(0), None, None)
     assert rc == -1
     # misaligned pointer
-    rc = lib.moe_quant_fp8(p(18), i64(4), i64(128), i64(128), p(16), i64(128), p(16), i64(4), None, None)
+    rc = lib.moe_quant_fp8(p(18), i64(4), i64(128), i64(128), p(16), i64(128), p(16), i64(4), i32(0), None, None)
+    assert rc == -1
+    # unknown flag bits
+    rc = lib.moe_quant_fp8(p(16), i64(4), i64(128), i64(128), p(16), i64(128), p(16), i64(4), i32(0x6), None, None)
     assert rc == -1
     # empty input is a no-op
-    rc = lib.moe_quant_fp8(None, i64(0), i64(128), i64(128), None, i64(128), None, i64(0), None, None)
+    rc = lib.moe_quant_fp8(None, i64(0), i64(128), i64(128), None, i64(128), None, i64(0), i32(0), None, None)
     assert rc == 0
+    lib.moe_combine.restype = ctypes.c_int
+    # unknown combine flag bits; a misaligned shared row pointer
+    rc = lib.moe_combine(p(16), i64(256), i64(8), p(16), p(16), i64(4), i32(2), i32(256), None, i64(0), i32(2),
+                         p(16), i64(256), None, None)
+    assert rc == -1
+    rc = lib.moe_combine(p(16), i64(256), i64(8), p(16), p(16), i64(4), i32(2), i32(256), p(18), i64(256), i32(0),
+                         p(16), i64(256), None, None)
+    assert rc == -1
     lib.moe_gemm_fp8_masked.restype = ctypes.c_int
-    i32 = ctypes.c_int32
     rc = lib.moe_gemm_fp8_masked(p(16), p(16), p(16), p(16), p(16), i32(4), i32(128), i32(200),
                                  i32(256), i32(0), p(16), i32(0), None, None)
     assert rc == -1                                   # N % 128 != 0
@@ -159,7 +170,7 @@ def test_ue8m0_scale_rule_matches_the_oracle(so):
     amax = np.concatenate([edges, np.nextafter(edges, np.float32(np.inf)), np.nextafter(edges, np.float32(0)),
                            np.exp2(rng.uniform(-40, 127, 2000)).astype(np.float32),
                            np.float32([0.0, 1e-30, 1e-4, 2e-4, 3.3895314e38])])
-    amax = amax[np.isfinite(amax)]
+    amax = np.concatenate([amax[np.isfinite(amax)], np.float32([np.inf, np.nan])])
     ref_s, ref_b = _block_scale_ue8m0(amax)
     for a, rs, rb in zip(amax, ref_s, ref_b):
         s, b = moe.moe_ue8m0_scale(float(a))

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 import synth
-from tests.gpu_common import (SENTINEL_BF16, activations_bits, bits, check_tol, from_bits,
+from tests.gpu_common import (SENTINEL_BF16, Guarded, activations_bits, bits, check_tol, from_bits,
                               oracle_weights, rand_codes, routing, to_dev, u8)
 
 pytestmark = pytest.mark.gpu
@@ -24,25 +24,27 @@ pytestmark = pytest.mark.gpu
 def _masked(lib, A, sA, B, sB, counts, flags=0, expected_m=0):
     E, max_m, K = A.shape
     N = B.shape[1]
-    D = torch.full((E, max_m, N), SENTINEL_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    g = Guarded((E, max_m, N), torch.bfloat16, SENTINEL_BF16)
     err = lib.new_error_word()
     lib.moe_gemm_fp8_masked(to_dev(A), to_dev(sA), to_dev(B), to_dev(sB),
-                            to_dev(np.asarray(counts, np.int32)), D, expected_m=expected_m,
+                            to_dev(np.asarray(counts, np.int32)), g.t, expected_m=expected_m,
                             flags=flags, err=err)
     status, _ = lib.moe_read_device_status(err)
-    return bits(D), status
+    assert g.intact(), "a store landed past the end of D"
+    return bits(g.t), status
 
 
 def _contig(lib, A, sA, B, sB, offsets, m_indices, flags=0):
     M_cap, K = A.shape
     N = B.shape[1]
-    D = torch.full((M_cap, N), SENTINEL_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    g = Guarded((M_cap, N), torch.bfloat16, SENTINEL_BF16)
     err = lib.new_error_word()
     lib.moe_gemm_fp8_contig(to_dev(A), to_dev(sA), to_dev(B), to_dev(sB),
                             to_dev(np.asarray(offsets, np.int32)), to_dev(np.asarray(m_indices, np.int32)),
-                            D, flags=flags, err=err)
+                            g.t, flags=flags, err=err)
     status, _ = lib.moe_read_device_status(err)
-    return bits(D), status
+    assert g.intact(), "a store landed past the end of D"
+    return bits(g.t), status
 
 
 def _check_masked(got, ref, valid, what):
@@ -222,6 +224,35 @@ def test_gemm_contig_prefill_sampled_rows(lib, flags):
         ref = oracle.bf16_encode(oracle.gemm_block_scaled(xq, xs, Bq[e], Bs[e]))
         check_tol(got[sel], ref, f"c3 expert {e}")
     assert (got[mi_h < 0] == SENTINEL_BF16).all()
+
+
+@pytest.mark.parametrize("case", ["past_capacity", "negative", "unaligned", "decreasing"])
+@pytest.mark.parametrize("flags", [0, 0x8], ids=["single", "pair"])
+def test_gemm_contig_segment_outside_capacity_is_skipped(lib, case, flags):
+    # offsets that put a segment outside [0, M_capacity) (or off the 128-row grid)
+    # must not be read or written: the segment is skipped, MOE_DEV_BAD_INDEX is
+    # set, the good segments are still computed, and nothing lands past D
+    rng = np.random.default_rng(17)
+    N, K, M_cap = 256, 256, 384
+    offsets = {"past_capacity": [0, 128, M_cap + 128], "negative": [-128, 128, 384],
+               "unaligned": [0, 64, 384], "decreasing": [0, 128, 0]}[case]
+    good = {"past_capacity": [0], "negative": [1], "unaligned": [], "decreasing": [0]}[case]
+    mi = -np.ones(M_cap, np.int64)
+    mi[0:100] = 0
+    mi[128:384] = 1
+    A, B = rand_codes(rng, (M_cap, K)), rand_codes(rng, (2, N, K))
+    sA = np.exp(rng.uniform(-4, 1, (K // 128, M_cap))).astype(np.float32)
+    sB = np.exp(rng.uniform(-4, 1, (2, N // 128, K // 128))).astype(np.float32)
+    got, st = _contig(lib, A, sA, B, sB, offsets, mi, flags=flags)
+    assert st == lib.MOE_ERR_BAD_INDEX
+    written = np.zeros(M_cap, bool)
+    for e in good:
+        lo = offsets[e]
+        rows = np.nonzero(mi[lo:offsets[e + 1]] == e)[0] + lo
+        ref = oracle.bf16_encode(oracle.gemm_block_scaled(A[rows], sA[:, rows], B[e], sB[e]))
+        check_tol(got[rows], ref, f"{case} expert {e}")
+        written[rows] = True
+    assert (got[~written] == SENTINEL_BF16).all(), "a skipped segment was written"
 
 
 def test_gemm_stall_reports_timeout_and_recovers(lib):

@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import synth
-from tests.gpu_common import SENTINEL_F32, SENTINEL_U8, to_dev, u8
+from tests.gpu_common import SENTINEL_F32, SENTINEL_U8, Guarded, f32_bits, to_dev, u8
 
 pytestmark = pytest.mark.gpu
 
@@ -19,25 +19,25 @@ def _run(lib, ids, expert_begin, E, layout, max_m, H=256, seed=0):
     s = np.full((H // 128, T_pad), -1.0, np.float32)
     s[:, :T] = rng.random((H // 128, T)).astype(np.float32)
     dev = "cuda"
+    # every output carries a guard band: nothing may be written past its end
     if layout == lib.MOE_LAYOUT_MASKED:
         rows = E * max_m
-        s_out = torch.full((E, H // 128, max_m), SENTINEL_F32, device=dev)
+        gs = Guarded((E, H // 128, max_m), torch.float32, f32_bits(SENTINEL_F32))
         cap = 0
     else:
         cap = lib.moe_contig_rows_bound(T * k, E) + 128
         rows = cap
-        s_out = torch.full((H // 128, cap), SENTINEL_F32, device=dev)
-    q_out = torch.full((rows, H), SENTINEL_U8, dtype=torch.uint8, device=dev)
-    counts = torch.full((E,), -7, dtype=torch.int32, device=dev)
-    offsets = torch.full((E + 1,), -7, dtype=torch.int32, device=dev)
-    m_ind = torch.full((max(rows, 1),), -7, dtype=torch.int32, device=dev)
-    row_src = torch.full((rows,), -7, dtype=torch.int32, device=dev)
-    dst = torch.full((T * k,), -7, dtype=torch.int32, device=dev)
+        gs = Guarded((H // 128, cap), torch.float32, f32_bits(SENTINEL_F32))
+    gq = Guarded((rows, H), torch.uint8, SENTINEL_U8)
+    outs = [Guarded((n,), torch.int32, -7) for n in (E, E + 1, max(rows, 1), rows, T * k)]
+    counts, offsets, m_ind, row_src, dst = [g.t for g in outs]
+    s_out, q_out = gs.t, gq.t
     err = lib.new_error_word()
     lib.moe_permute(to_dev(q), to_dev(s), to_dev(ids.astype(np.int32)), expert_begin, E, layout,
                     max_m, q_out, s_out, counts, offsets, m_ind, row_src, dst, rows_capacity=cap,
                     err=err)
     status, raw = lib.moe_read_device_status(err)
+    assert all(g.intact() for g in [gs, gq] + outs), "permute wrote past the end of an output"
     ref = oracle.permute(ids, expert_begin, E, "masked" if layout == 0 else "contig", max_m,
                          q=q, s=s[:, :T])
     got = dict(counts=counts.cpu().numpy(), offsets=offsets.cpu().numpy(),

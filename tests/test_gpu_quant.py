@@ -216,3 +216,39 @@ def test_quant_ue8m0_edge_cases(lib):
     q, s, e8 = _gpu_quant_ue8m0(lib, oracle.bf16_encode(x))
     assert s[0, 0] == np.float32(2.0 ** -22) and e8[0, 0] == 105
     assert s[2, 7] == 1.0 and s[2, 8] == 2.0
+
+
+def test_quant_non_finite_inputs(lib):
+    # NaN elements are left out of the block maximum and encode to 0x7F; a block
+    # of NaNs takes the floor scale; an infinite element makes the block's scale
+    # inf (UE8M0 byte 0xFF): finite elements become signed zeros, the infinite
+    # one NaN.  Both scale readings, bit for bit against the oracle.
+    rng = np.random.default_rng(9)
+    M, K = 9, 384
+    x = rng.standard_normal((M, K))
+    x[0, 7] = np.nan
+    x[1, :128] = np.nan
+    x[2, 5] = np.inf
+    x[3, 200] = -np.inf
+    x[4, 130:140] = np.nan
+    x[4, 300] = np.inf
+    x[5, 256:] = -np.inf
+    xb = oracle.bf16_encode(x)
+    _assert_quant_equal(lib, xb)
+    _assert_ue8m0_equal(lib, xb)
+    q, s = _gpu_quant(lib, xb)
+    assert q[0, 7] == 0x7F and (q[1, :128] == 0x7F).all() and np.isinf(s[0, 2])
+    _, _, e8 = _gpu_quant_ue8m0(lib, xb)
+    assert e8[0, 2] == 255 and e8[1, 3] == 255 and e8[2, 5] == 255
+
+
+def test_quant_flag_selects_power_of_two_scales(lib):
+    # moe_quant_fp8 with MOE_QUANT_UE8M0 writes what moe_quant_fp8_ue8m0 writes
+    xb = activations_bits("c3", 64)
+    x = from_bits(xb)
+    q = torch.full((64, xb.shape[1]), SENTINEL_U8, dtype=torch.uint8, device="cuda")
+    s = torch.full((xb.shape[1] // 128, 64), SENTINEL_F32, dtype=torch.float32, device="cuda")
+    lib.moe_quant_fp8(x, q, s, flags=lib.MOE_QUANT_UE8M0)
+    torch.cuda.synchronize()
+    rq, rs, _ = oracle.quant_1x128_ue8m0(oracle.bf16_decode(xb).astype(np.float32))
+    assert np.array_equal(u8(q), rq) and np.array_equal(s.cpu().numpy(), rs)

@@ -100,6 +100,45 @@ def test_ue8m0_scale_is_the_smallest_power_of_two():
     assert (top <= 448.0).all() and (top >= 224.0).all()
 
 
+def test_quant_non_finite_inputs():
+    # A reading for inputs the pages never mention: NaN elements take no part in
+    # the block maximum (IEEE maxNum, as a hardware fmax reduction) and encode to
+    # the NaN code 0x7F; a block of NaNs has maximum 0 (floor scale); an infinite
+    # element gives s = inf (UE8M0 byte 0xFF), so the finite elements of its block
+    # become signed zeros and the infinite one NaN (inf / inf).
+    x = np.zeros((4, 256), np.float32)
+    x[0, :128] = _bf16(RNG.standard_normal(128))
+    x[0, 7] = np.nan
+    x[1, :128] = np.nan
+    x[2, :128] = _bf16(RNG.standard_normal(128))
+    x[2, 5], x[2, 6], x[2, 8] = np.inf, -3.0, 2.5
+    x[3, 200], x[3, 201], x[3, 202] = -np.inf, 1.0, -1.0
+    clean = x[0].copy()
+    clean[7] = 0.0
+    floors = {quant_1x128: FLOOR_SCALE, oracle.quant_1x128_ue8m0: np.float32(2.0 ** -22)}
+    for fn, floor in floors.items():
+        res = fn(x)
+        q, s = res[0], res[1]
+        qc, sc = fn(clean[None])[:2]
+        assert s[0, 0] == sc[0, 0] and np.isfinite(s[0, 0])
+        assert q[0, 7] == 0x7F and np.array_equal(np.delete(q[0, :128], 7), np.delete(qc[0, :128], 7))
+        assert s[0, 1] == floor and (q[1, :128] == 0x7F).all()
+        assert np.isinf(s[0, 2]) and q[2, 5] == 0x7F and q[2, 6] == 0x80 and q[2, 8] == 0x00
+        assert np.isinf(s[1, 3]) and q[3, 200] == 0x7F and q[3, 201] == 0x00 and q[3, 202] == 0x80
+        assert np.isfinite(s[1, 2]) and np.isfinite(s[0, 3])   # the other blocks are unaffected
+    byte = oracle.quant_1x128_ue8m0(x)[2]
+    assert byte[0, 2] == 255 and byte[1, 3] == 255 and byte[0, 1] == 127 - 22
+    # a 128x128 weight tile: the same rules over the tile
+    w = np.zeros((128, 256), np.float32)
+    w[3, 3], w[9, 10] = np.nan, -2.0
+    w[100, 200] = np.inf
+    qw, sw = quant_128x128(w)
+    assert sw[0, 0] == np.float32(np.float32(2.0) / np.float32(448.0)) and qw[3, 3] == 0x7F
+    assert qw[9, 10] == 0xFE and np.isinf(sw[0, 1]) and qw[100, 200] == 0x7F
+    _, swe, bwe = oracle.quant_128x128_ue8m0(w)
+    assert swe[0, 0] == np.float32(2.0 ** -7) and bwe[0, 1] == 255
+
+
 def test_ue8m0_codes_are_the_bruteforce_encoding_of_x_over_s():
     # blocks whose maximum is 448 * 2^j: s = 2^j exactly and every element's code
     # is the brute-force nearest E4M3 of x / 2^j
@@ -390,3 +429,33 @@ def test_combine_bruteforce():
             if dst[t * k + j] >= 0:
                 ref += float(w[t, j]) * Y[dst[t * k + j]]
         assert np.array_equal(out[t], bf16_decode(bf16_encode(ref)))
+
+
+def test_combine_shared_row_and_accumulate():
+    # the shared expert's row at weight 1 equals one more routing slot of weight
+    # 1 (same float64 steps); accumulating into an output adds its values; with
+    # no slot and no shared row, accumulation leaves the output as it was; brute
+    # force on a small case
+    T, k, H, rows = 6, 3, 16, 10
+    y = bf16_encode(RNG.standard_normal((rows, H)))
+    sh = bf16_encode(RNG.standard_normal((T, H)))
+    old = bf16_encode(RNG.standard_normal((T, H)))
+    dst = RNG.integers(-1, rows, (T, k))
+    w = RNG.uniform(0, 1, (T, k)).astype(np.float32)
+    y_ext = np.concatenate([y, sh])
+    dst_ext = np.concatenate([dst, rows + np.arange(T)[:, None]], axis=1)
+    w_ext = np.concatenate([w, np.ones((T, 1), np.float32)], axis=1)
+    assert np.array_equal(combine(y, dst.reshape(-1), w, shared_bits=sh),
+                          combine(y_ext, dst_ext.reshape(-1), w_ext))
+    none = -np.ones((T, k), np.int64)
+    assert np.array_equal(combine(y, none.reshape(-1), w, out_bits=old), old)
+    got = bf16_decode(combine(y, dst.reshape(-1), w, shared_bits=sh, out_bits=old))
+    yd, sd, od = bf16_decode(y), bf16_decode(sh), bf16_decode(old)
+    for t in range(T):
+        for h in range(H):
+            acc = od[t, h]
+            for j in range(k):
+                if dst[t, j] >= 0:
+                    acc += float(w[t, j]) * yd[dst[t, j], h]
+            acc += sd[t, h]
+            assert got[t, h] == bf16_decode(bf16_encode(np.array([acc])))[0]
