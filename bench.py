@@ -40,15 +40,18 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # ----------------------------------------------------------------------------- workload
-def build_workload(cfg_name: str, device="cuda", quantise_on_gpu=True):
+def build_workload(cfg_name: str, device="cuda", gen_device=None):
     """Seeded inputs of one config resident on `device`; expert weights quantised
-    to E4M3 128x128 blocks by the library's weight-quant kernel."""
+    to E4M3 128x128 blocks by the library's weight-quant kernel.  The inputs are
+    drawn on `gen_device` (default: `device`) and copied over; the generator is
+    device independent, so the values are the same either way."""
     import torch
     import fp8_grouped_expert_x128_gb300 as moe
+    gen = device if gen_device is None else gen_device
     cfg = synth.get_config(cfg_name)
     r = synth.make_routing(cfg)
     T, k = r["T"], r["k"]
-    x = synth.make_activations(cfg, T, device=device)
+    x = synth.make_activations(cfg, T, device=gen).to(device)
     ids = torch.from_numpy(r["topk_ids"].astype(np.int32)).to(device)
     w = torch.from_numpy(r["topk_w"].astype(np.float32)).to(device)
     E, H, I = cfg.E, cfg.H, cfg.I
@@ -57,9 +60,9 @@ def build_workload(cfg_name: str, device="cuda", quantise_on_gpu=True):
     w2 = torch.empty((E, H, I), dtype=torch.uint8, device=device)
     w2_s = torch.empty((E, H // 128, I // 128), dtype=torch.float32, device=device)
     for e in range(E):
-        b13 = synth.make_expert_weights(cfg, "w13", e, device=device)
+        b13 = synth.make_expert_weights(cfg, "w13", e, device=gen).to(device)
         moe.moe_quant_weight_fp8(b13[None], w13[e:e + 1], w13_s[e:e + 1])
-        b2 = synth.make_expert_weights(cfg, "w2", e, device=device)
+        b2 = synth.make_expert_weights(cfg, "w2", e, device=gen).to(device)
         moe.moe_quant_weight_fp8(b2[None], w2[e:e + 1], w2_s[e:e + 1])
         del b13, b2
     torch.cuda.synchronize()
@@ -100,20 +103,78 @@ def gemm1_fused(wl):
     return gemm1_variant(wl).endswith("<swiglu>")
 
 
+def gemm2_variant(wl):
+    """The GEMM2 kernel moe_ffn runs for this workload."""
+    import fp8_grouped_expert_x128_gb300 as moe
+    if wl["layout"] == moe.MOE_LAYOUT_MASKED:
+        v = moe.moe_gemm_fp8_masked_variant(wl["cfg"].max_m, wl["expected_m"], wl.get("gemm_flags", 0))
+        if v != 0:
+            return f"gemm_fp8_weights_m_kernel<{v}>"
+    if combine_fused(wl):
+        return "gemm_fp8_tokens_m_kernel<combine1>"
+    return "gemm_fp8_tokens_m_kernel"
+
+
+def combine_fused(wl):
+    """moe_ffn folds the combine into GEMM2's epilogue for one routing slot per
+    token (device output; the tokens-as-M kernel serving GEMM2)."""
+    import fp8_grouped_expert_x128_gb300 as moe
+    if wl["k"] != 1:
+        return False
+    if wl["layout"] == moe.MOE_LAYOUT_MASKED:
+        return moe.moe_gemm_fp8_masked_variant(wl["cfg"].max_m, wl["expected_m"], wl.get("gemm_flags", 0)) == 0
+    return True
+
+
+def units_per_step(wl):
+    """The metric's unit per step: routed (token, local expert) rows for the
+    post-dispatch workloads (EP72 decode, EP32 prefill), tokens otherwise."""
+    return wl["rows"] if wl["cfg"].name.startswith(("c2", "c3")) else wl["T"]
+
+
+def unit_name(wl):
+    return "routed (token, local expert) rows" if wl["cfg"].name.startswith(("c2", "c3")) else "tokens"
+
+
 def algorithmic_counts(wl):
-    """Algorithmic FLOPs and bytes per step and per GEMM1 launch."""
+    """Algorithmic FLOPs and HBM bytes per step and per GEMM launch (padding
+    rows and idle experts excluded): weights once per active expert, each
+    activation tensor once in and once out."""
     cfg = wl["cfg"]
     H, I = cfg.H, cfg.I
-    rows, act = wl["rows"], wl["active_experts"]
+    rows, act, T, k = wl["rows"], wl["active_experts"], wl["T"], wl["k"]
     fused = gemm1_fused(wl)
     flops_g1 = 2.0 * rows * H * 2 * I
     flops_g2 = 2.0 * rows * I * H
     w13_bytes = act * (2 * I * H + 4 * (2 * I // 128) * (H // 128))
     w2_bytes = act * (H * I + 4 * (H // 128) * (I // 128))
-    g1_out = rows * (I + 4 * I / 128) if fused else rows * 2 * I * 2   # FP8 h + scales, or bf16 Y1
-    g1_bytes = w13_bytes + rows * (H + 4 * H / 128) + g1_out
-    return dict(flops=flops_g1 + flops_g2, flops_g1=flops_g1, g1_bytes=g1_bytes,
-                weight_bytes=w13_bytes + w2_bytes)
+    a1 = rows * (H + 4 * H / 128)                    # FP8 rows + fp32 scales into GEMM1
+    a2 = rows * (I + 4 * I / 128)                    # FP8 h + scales into GEMM2
+    y1 = rows * 2 * I * 2                            # bf16 Y1
+    y2 = rows * H * 2                                # bf16 Y2
+    out = T * H * 2
+    g1_bytes = w13_bytes + a1 + (a2 if fused else y1)
+    g2_bytes = w2_bytes + a2 + (out if combine_fused(wl) else y2)
+    # the whole step: x in, the routed rows through both GEMMs, out
+    step_bytes = (T * H * 2 + T * k * 4 * 2 + a1 + w13_bytes + w2_bytes + a2 +
+                  (0 if fused else 2 * y1) + (out if combine_fused(wl) else 2 * y2 + out))
+    return dict(flops=flops_g1 + flops_g2, flops_g1=flops_g1, flops_g2=flops_g2, g1_bytes=g1_bytes,
+                g2_bytes=g2_bytes, weight_bytes=w13_bytes + w2_bytes, step_bytes=step_bytes)
+
+
+def roofline(flops, nbytes, seconds, peaks):
+    """Bound = whichever of bytes / HBM peak and FLOPs / FP8 peak is larger;
+    achieved and frac against that peak; both fractions alongside."""
+    hbm, fp8 = peaks["hbm_gbs"], peaks["fp8_tflops"]
+    t_mem, t_cmp = nbytes / (hbm * 1e9), flops / (fp8 * 1e12)
+    gbs, tfs = nbytes / seconds / 1e9, flops / seconds / 1e12
+    if t_mem >= t_cmp:
+        r = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm}
+    else:
+        r = {"bound": "tensor", "achieved": tfs, "peak": fp8, "unit": "TFLOP/s", "frac": tfs / fp8}
+    r.update({"hbm_frac": gbs / hbm, "fp8_frac": tfs / fp8, "t_min_ms": 1e3 * max(t_mem, t_cmp),
+              "algorithmic": {"bytes": nbytes, "flops": flops}})
+    return r
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -173,30 +234,30 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- oracle leg
-def _oracle_token_rows(wl, oracle_w, tokens):
-    """The oracle chain restricted to `tokens` (rows are independent): quant,
-    each local assignment's GEMM1 -> SwiGLU+quant -> GEMM2, combine.  Returns
-    the number of routed rows processed."""
+def _oracle_rows(wl, oracle_w, assignments):
+    """The oracle chain on a sample of routed rows (rows are independent): each
+    sampled assignment (t, j) quantises token t, runs GEMM1 -> SwiGLU+quant ->
+    GEMM2 against its expert, and the sampled rows of each token are combined
+    with their weights.  Returns the number of routed rows processed."""
     import oracle
     cfg = wl["cfg"]
     r = wl["routing"]
-    x = wl["x_host_bits"][tokens]
-    q, s = oracle.quant_1x128(oracle.bf16_decode(x).astype(np.float32))
+    by_token = {}
+    for t, j in assignments:
+        by_token.setdefault(t, []).append(j)
     n_rows = 0
-    for i, t in enumerate(tokens):
+    for t, slots in by_token.items():
+        q, s = oracle.quant_1x128(oracle.bf16_decode(wl["x_host_bits"][t:t + 1]).astype(np.float32))
         y2_rows, ws = [], []
-        for j in range(r["k"]):
+        for j in slots:
             e = int(r["topk_ids"][t, j]) - r["expert_begin"]
-            if not 0 <= e < cfg.E:
-                continue
             w13q, w13s, w2q, w2s = oracle_w[e]
-            y1 = oracle.bf16_encode(oracle.gemm_block_scaled(q[i:i + 1], s[:, i:i + 1], w13q, w13s))
+            y1 = oracle.bf16_encode(oracle.gemm_block_scaled(q, s, w13q, w13s))
             q2, s2 = oracle.swiglu_quant(y1)
             y2_rows.append(oracle.bf16_encode(oracle.gemm_block_scaled(q2, s2, w2q, w2s))[0])
             ws.append(float(r["topk_w"][t, j]))
             n_rows += 1
-        if y2_rows:
-            oracle.combine(np.stack(y2_rows), np.arange(len(ws)), np.array([ws], np.float32))
+        oracle.combine(np.stack(y2_rows), np.arange(len(ws)), np.array([ws], np.float32))
     return n_rows
 
 
@@ -227,31 +288,49 @@ class OracleWeights:
         return self.cache[e]
 
 
-def _local_experts(wl, tokens):
+def local_assignments(wl):
+    """The routed (token, slot) pairs the FFN processes, in assignment order
+    (masked layouts: the ones kept under max_m)."""
     r = wl["routing"]
-    ids = r["topk_ids"][tokens].reshape(-1) - r["expert_begin"]
-    return [int(e) for e in ids if 0 <= e < wl["cfg"].E]
+    cfg = wl["cfg"]
+    e = r["topk_ids"] - r["expert_begin"]
+    out = []
+    seen = np.zeros(cfg.E, np.int64)
+    for t in range(r["T"]):
+        for j in range(r["k"]):
+            ee = int(e[t, j])
+            if 0 <= ee < cfg.E and (cfg.layout != "masked" or seen[ee] < cfg.max_m):
+                seen[ee] += 1
+                out.append((t, j))
+    return out
 
 
 def time_oracle(wl, oracle_w, budget_s=15.0, start=0):
-    """Time the oracle on a bounded sample of whole local tokens taken in order
-    from `start`: one token first to estimate the cost, then as many as fit in
-    about `budget_s`.  Weight preparation happens before each timed region.
-    Returns (rows/s, seconds timed, tokens, rows)."""
-    T = wl["T"]
-    first = [start % T]
-    oracle_w.prepare(_local_experts(wl, first))
+    """Time the oracle on a bounded sample of the workload's routed rows, taken
+    in assignment order from `start`: one row first to estimate the cost, then
+    as many as fit in about `budget_s`.  Weight preparation happens before each
+    timed region.  Returns (value in the metric's unit per second, seconds
+    timed, rows): rows/s for row-unit workloads, rows/s x tokens per routed row
+    for token-unit workloads."""
+    rows_all = wl.get("_assign")
+    if rows_all is None:
+        rows_all = wl["_assign"] = local_assignments(wl)
+    n = len(rows_all)
+    e_of = lambda a: int(wl["routing"]["topk_ids"][a]) - wl["routing"]["expert_begin"]
+    first = [rows_all[start % n]]
+    oracle_w.prepare([e_of(a) for a in first])
     t0 = time.perf_counter()
-    rows = _oracle_token_rows(wl, oracle_w, first)
+    rows = _oracle_rows(wl, oracle_w, first)
     dt = time.perf_counter() - t0
     n_more = int(max(0.0, budget_s - dt) / max(dt, 1e-3))
-    more = [(start + 1 + i) % T for i in range(min(n_more, T - 1))]
+    more = [rows_all[(start + 1 + i) % n] for i in range(min(n_more, n - 1))]
     if more:
-        oracle_w.prepare(_local_experts(wl, more))
+        oracle_w.prepare([e_of(a) for a in more])
         t1 = time.perf_counter()
-        rows += _oracle_token_rows(wl, oracle_w, more)
+        rows += _oracle_rows(wl, oracle_w, more)
         dt += time.perf_counter() - t1
-    return rows / dt, dt, 1 + len(more), rows
+    per_unit = units_per_step(wl) / wl["rows"]           # metric units per routed row
+    return rows / dt * per_unit, dt, rows
 
 
 def cpu_cores():
@@ -305,10 +384,12 @@ def _sum_over_ranks(world, v):
     return float(t.item())
 
 
-def recorded_traffic(kernel_label: str, workload: str):
-    """DRAM bytes (read + write) per launch of this kernel on this workload from
-    the ncu capture recorded in profiles/traffic.json, or None when there is no
-    capture or gemm.cu has changed since it was taken."""
+def recorded_traffic(kernel_label: str, workload: str, which: str = "gemm1"):
+    """DRAM bytes (read + write) per launch of this kernel (as GEMM1 or GEMM2) on
+    this workload from the ncu capture recorded in profiles/traffic.json, or
+    None when there is no capture or gemm.cu has changed since it was taken.
+    A record may hold a capture of a cut-down case scaled to the full launch
+    (its "scaled_from" field says how)."""
     import hashlib
     path = os.path.join(HERE, "profiles", "traffic.json")
     src = os.path.join(HERE, "fp8_grouped_expert_x128_gb300", "csrc", "gemm.cu")
@@ -318,7 +399,8 @@ def recorded_traffic(kernel_label: str, workload: str):
         sha = hashlib.sha256(f.read()).hexdigest()
     with open(path) as f:
         rec = json.load(f)
-    r = rec.get(f"{kernel_label}@{workload}")
+    r = rec.get(f"{kernel_label}@{workload}:{which}") or (rec.get(f"{kernel_label}@{workload}")
+                                                          if which == "gemm1" else None)
     if not r or r.get("gemm_cu_sha256") != sha:
         return None
     return r["dram_read_bytes"] + r["dram_write_bytes"]
@@ -333,47 +415,312 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def config_dict(wl, world):
+    """The workload the line is quoted on (the same dict for both arms)."""
+    cfg = wl["cfg"]
+    return {"workload": f"{cfg.name}: {cfg.description}", "tokens": unit_name(wl),
+            "units_per_step": units_per_step(wl), "rows_per_step": wl["rows"], "local_tokens": wl["T"],
+            "counts": [int(c) for c in wl["counts"]], "max_m": cfg.max_m,
+            "active_experts": wl["active_experts"], "hidden": cfg.H, "intermediate": cfg.I,
+            "l2": "flushed (256 MiB write) before every timed step", "parallelism": f"replicas x{world}"}
+
+
+def routing_summary(cfg_name):
+    """Host-side facts of a workload (no GPU): routing, counts, rows."""
+    cfg = synth.get_config(cfg_name)
+    r = synth.make_routing(cfg)
+    E = cfg.E
+    counts = np.array([(r["topk_ids"] == r["expert_begin"] + e).sum() for e in range(E)])
+    rows = int(np.minimum(counts, cfg.max_m).sum()) if cfg.layout == "masked" else int(counts.sum())
+    return dict(cfg=cfg, routing=r, T=r["T"], k=r["k"], counts=counts, rows=rows,
+                active_experts=int((counts > 0).sum()))
+
+
 def run_reference(args, world, rank):
     """The reference arm: the CPU oracle, as it stands, on a bounded sample per step."""
     if rank != 0:
         return
     import torch
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    wl = reference_workload(args.workload, dev)
+    wl = routing_summary(args.workload)
+    x = synth.make_activations(wl["cfg"], wl["T"], device=dev)
+    wl["x_host_bits"] = x.cpu().view(torch.int16).numpy().view(np.uint16)
     oracle_w = OracleWeights(wl, dev)
     per_step = []
     for i in range(args.warmup + args.steps):
-        rate, dt, ntok, nrows = time_oracle(wl, oracle_w, budget_s=args.ref_step_s, start=i)
+        rate, dt, nrows = time_oracle(wl, oracle_w, budget_s=args.ref_step_s, start=i * 7)
         if i >= args.warmup:
-            per_step.append((rate, dt, ntok, nrows))
-    rows = sum(p[3] for p in per_step)
+            per_step.append((rate, dt, nrows))
+    per_unit = units_per_step(wl) / wl["rows"]
+    units = sum(p[2] for p in per_step) * per_unit
     secs = sum(p[1] for p in per_step)
-    value = rows / secs
-    cfg = wl["cfg"]
+    value = units / secs
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, len(per_step)),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)", "impl": "reference",
-        "config": {"workload": f"{cfg.name}: {cfg.description}", "tokens": "routed (token, local expert) rows",
-                   "l2": "n/a (CPU)"},
+        "config": config_dict(wl, 1),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                         "sample": f"each step: whole local tokens in order, ~{args.ref_step_s:.0f}s "
-                                   f"of CPU work (~{per_step[0][2]} tokens, {per_step[0][3]} rows); "
-                                   "numpy float64, BLAS threads = all affinity cores"},
+                         "sample": f"each step: routed rows in assignment order, ~{args.ref_step_s:.0f}s of "
+                                   f"CPU work (~{per_step[0][2]} rows), scaled to {unit_name(wl)} at "
+                                   f"{per_unit:.4g} per routed row; numpy float64, BLAS threads = all "
+                                   "affinity cores"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def reference_workload(cfg_name, dev):
+class Step:
+    """One moe_ffn step of a workload, captured once in a CUDA graph (as the
+    decode path runs in serving) and replayed; a second graph of the same call
+    records the seven stage events between the kernels (used for the per-stage
+    split and the GEMM launch times only, never for the value)."""
+
+    def __init__(self, wl, dev, eager=False):
+        import torch
+        import fp8_grouped_expert_x128_gb300 as moe
+        self.moe, self.dev, self.wl = moe, dev, wl
+        cfg = wl["cfg"]
+        self.out = torch.empty((wl["T"], cfg.H), dtype=torch.bfloat16, device=dev)
+        self.err = moe.new_error_word(dev)
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+        self.desc = make_desc(wl, self.out, err=self.err)
+        self.desc_ev = make_desc(wl, self.out, err=self.err, stage_events=self.events)
+        self.ws = moe.alloc_workspace(self.desc, dev)
+        self.run = lambda: moe.moe_ffn(self.desc, self.ws)
+        self.run_ev = lambda: moe.moe_ffn(self.desc_ev, self.ws)
+        self.graph = None
+        self.eager = eager
+
+    def capture(self, warmup):
+        import torch
+        dev = self.dev
+        for _ in range(warmup):
+            self.run()
+        torch.cuda.synchronize(dev)
+        self.check("warm-up")
+        if self.eager:
+            return
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            self.run()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run()
+        g_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_ev):
+            self.run_ev()
+        for _ in range(warmup):
+            g.replay()
+            g_ev.replay()
+        torch.cuda.synchronize(dev)
+        try:                                       # the graph's stage events must be timeable
+            self.events[0].elapsed_time(self.events[6])
+            self.graph = g
+            self.run, self.run_ev = g.replay, g_ev.replay
+        except RuntimeError as exc:
+            print(f"graph stage events not timeable ({exc}); timing eager calls", file=sys.stderr)
+
+    def check(self, where):
+        st, _ = self.moe.moe_read_device_status(self.err)
+        if st not in (self.moe.MOE_OK, self.moe.MOE_ERR_OVERFLOW):
+            raise SystemExit(f"device status {self.moe.moe_status_string(st)} in {where}")
+        return st
+
+    def time(self, n, l2_flush, stream):
+        """Device time of n steps, each preceded by an L2-evicting write, with two
+        CUDA events on the launching stream around each step."""
+        import torch
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ms = []
+        for _ in range(n):
+            l2_flush.fill_(1)
+            t0.record(stream)
+            self.run()
+            t1.record(stream)
+            torch.cuda.synchronize(self.dev)
+            ms.append(t0.elapsed_time(t1))
+        return ms
+
+    def soak(self, seconds, l2_flush):
+        """Untimed steps for about `seconds` (the clock sampler sees the load)."""
+        import torch
+        t_end = time.perf_counter() + seconds
+        while time.perf_counter() < t_end:
+            for _ in range(16):
+                l2_flush.fill_(1)
+                self.run()
+            torch.cuda.synchronize(self.dev)
+
+    def split(self, n, l2_flush):
+        """Per-stage times (mean over n instrumented replays) and the GEMM1 and
+        GEMM2 launch times of each replay."""
+        import torch
+        stage = [0.0] * 6
+        g1, g2 = [], []
+        for _ in range(n):
+            l2_flush.fill_(1)
+            self.run_ev()
+            torch.cuda.synchronize(self.dev)
+            for i in range(6):
+                stage[i] += self.events[i].elapsed_time(self.events[i + 1]) / n
+            g1.append(self.events[2].elapsed_time(self.events[3]))
+            g2.append(self.events[4].elapsed_time(self.events[5]))
+        return stage, g1, g2
+
+
+STAGES = ["quant (fused into permute)", "quant+permute", "gemm1", "swiglu_quant (fused into gemm1 when 0)",
+          "gemm2", "combine (fused into gemm2 when 0)"]
+
+
+def kernel_rooflines(wl, name, g1_s, g2_s, peaks, peak_src):
+    alg = algorithmic_counts(wl)
+    out = {}
+    for which, kname, sec, flops, nbytes in (
+            ("gemm1", gemm1_variant(wl), g1_s, alg["flops_g1"], alg["g1_bytes"]),
+            ("gemm2", gemm2_variant(wl), g2_s, alg["flops_g2"], alg["g2_bytes"])):
+        r = roofline(flops, nbytes, sec, peaks)
+        what = {"gemm1": "GEMM1 (W13)" + (" + SwiGLU + FP8 requant" if gemm1_fused(wl) else ""),
+                "gemm2": "GEMM2 (W2)" + (" + single-slot combine" if combine_fused(wl) else "")}[which]
+        r.update({"kernel": f"{kname} ({what})", "launch_ms": 1e3 * sec,
+                  "traffic": recorded_traffic(kname.split(" ")[0], name, which),
+                  "peak_source": peak_src + ("" if r["bound"] == "hbm" else " bf16 burst x2 (nominal FP8:BF16)")})
+        out[which] = r
+    return out
+
+
+def measure(name, args, dev, world, l2_flush, stream, peaks, peak_src, clk_seconds=0.0):
+    """Build a workload, time K steps, and report its line fields."""
+    wl = build_workload(name, dev)
+    if args.expected_m is not None:
+        wl["expected_m"] = args.expected_m
+    wl["gemm_flags"] = args.gemm_flags
+    st = Step(wl, dev, eager=args.eager)
+    st.capture(args.warmup)
+    clk = ClockSampler(dev.index if dev.index is not None else 0) if clk_seconds > 0 else None
+    _barrier(world)
     import torch
-    cfg = synth.get_config(cfg_name)
-    r = synth.make_routing(cfg)
-    x = synth.make_activations(cfg, r["T"], device=dev)
-    counts = np.array([(r["topk_ids"] == r["expert_begin"] + e).sum() for e in range(cfg.E)])
-    return dict(cfg=cfg, routing=r, T=r["T"], counts=counts,
-                x_host_bits=x.cpu().view(torch.int16).numpy().view(np.uint16))
+    torch.cuda.synchronize(dev)
+    if clk is not None:
+        clk.__enter__()
+        st.soak(clk_seconds, l2_flush)
+    t_wall = time.perf_counter()
+    step_ms = st.time(args.steps, l2_flush, stream)
+    t_wall = time.perf_counter() - t_wall
+    if clk is not None:
+        clk.__exit__(None, None, None)
+    _barrier(world)
+    status = st.check("the timed region")
+    stage_ms, g1, g2 = st.split(max(3, min(args.steps, 10)), l2_flush)
+    total_s = _max_over_ranks(world, sum(step_ms) / 1e3)
+    units = _sum_over_ranks(world, units_per_step(wl) * args.steps)
+    ms_per_step = 1e3 * total_s / args.steps
+    alg = algorithmic_counts(wl)
+    g1_s, g2_s = statistics.mean(g1) / 1e3, statistics.mean(g2) / 1e3
+    rep = {
+        "value": units / total_s, "ms_per_step": ms_per_step,
+        "stage_ms": {n: round(v, 4) for n, v in zip(STAGES, stage_ms)},
+        "kernels": kernel_rooflines(wl, name, g1_s, g2_s, peaks, peak_src),
+        "step_roofline": roofline(alg["flops"], alg["step_bytes"], ms_per_step / 1e3, peaks),
+        "tflops": alg["flops"] / (ms_per_step / 1e3) / 1e12,
+        "weight_gbs": alg["weight_bytes"] / (ms_per_step / 1e3) / 1e9,
+        "gpu_launches": moe_kernel_count(st) * args.steps,
+        "device_status": st.moe.moe_status_string(status),
+        "tuning": {"expected_m_hint": wl["expected_m"], "gemm_flags": args.gemm_flags,
+                   "launch": "eager moe_ffn" if st.graph is None else
+                             "moe_ffn captured once in a CUDA graph, replayed per step",
+                   "gemm1": gemm1_variant(wl), "gemm2": gemm2_variant(wl)},
+        "wall_s_timed": t_wall,
+    }
+    return wl, st, rep, clk
+
+
+def moe_kernel_count(st):
+    return st.moe.moe_ffn_kernel_count(st.desc)
+
+
+def e2e_leg(wl, st, args, dev, world, l2_flush, stream):
+    """The same metric through the public call with the step's inputs and output
+    crossing the host link inside every timed step (pinned host buffers)."""
+    import torch
+    moe = st.moe
+    T, H = wl["T"], wl["cfg"].H
+    x_h = wl["x"].cpu().pin_memory()
+    ids_h = wl["topk_ids"].cpu().pin_memory()
+    w_h = wl["topk_w"].cpu().pin_memory()
+    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(wl["x"])
+    ids_d = torch.empty_like(wl["topk_ids"])
+    w_d = torch.empty_like(wl["topk_w"])
+    d2 = make_desc(wl, st.out, err=st.err, x=x_d, ids=ids_d, w=w_d)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def host_step():
+        x_d.copy_(x_h, non_blocking=True); ids_d.copy_(ids_h, non_blocking=True)
+        w_d.copy_(w_h, non_blocking=True)
+        moe.moe_ffn(d2, st.ws)
+        out_h.copy_(st.out, non_blocking=True)
+
+    def time_e2e(run):
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize(dev)
+        ms = []
+        for _ in range(args.steps):
+            l2_flush.fill_(1)
+            e0.record(stream)
+            run()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms.append(e0.elapsed_time(e1))
+        return _max_over_ranks(world, sum(ms) / 1e3)
+
+    def graphed(fn):
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            fn()
+        return gr
+
+    # Three ways from host buffers, every byte crossing the host link inside the
+    # timed region of each step:
+    #  host I/O  moe_ffn given the pinned host x / routing / out directly: the
+    #            kernels read and write them in place, overlapped with the
+    #            compute (the library's host-buffer path; the value);
+    #  copies    explicit copies in, moe_ffn, copy out;
+    #  eager     the copies path with eager calls instead of a graph.
+    use_graph = st.graph is not None
+    eager_s = time_e2e(host_step)
+    copies_s = time_e2e(graphed(host_step).replay) if use_graph else eager_s
+    d_host = make_desc(wl, out_h, err=st.err, x=x_h, ids=ids_h, w=w_h)
+    host_io = lambda: moe.moe_ffn(d_host, st.ws)
+    try:
+        host_io()
+        torch.cuda.synchronize(dev)
+        host_s = time_e2e(graphed(host_io).replay if use_graph else host_io)
+    except moe.MoeError as exc:
+        print(f"host-buffer moe_ffn refused ({exc}); e2e = the copies path", file=sys.stderr)
+        host_s = None
+    e2e_s = host_s if host_s is not None else copies_s
+    units = _sum_over_ranks(world, units_per_step(wl) * args.steps)
+    h2d = x_h.numel() * 2 + ids_h.numel() * 4 + w_h.numel() * 4
+    return {"value": units / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(out_h.numel() * 2),
+            "ms_per_step": 1e3 * e2e_s / args.steps,
+            "copies": {"value": units / copies_s, "ms_per_step": 1e3 * copies_s / args.steps},
+            "eager": {"value": units / eager_s, "ms_per_step": 1e3 * eager_s / args.steps},
+            "how": ("moe_ffn on pinned host x, topk_ids, topk_w and out (read and written in place "
+                    "by the kernels across the host link)" if host_s is not None else
+                    "pinned-host x, topk_ids, topk_w -> device, moe_ffn, out -> pinned host")
+                   + ("; one CUDA graph replay per step" if use_graph else "; eager calls")
+                   + "; 'copies' = explicit copies in and out around moe_ffn; 'eager' = copies, eager calls"}
 
 
 def main():
@@ -382,10 +729,17 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="c2")
+    ap.add_argument("--workload", default="c5",
+                    help="the headline workload (default: the all-experts decode layer, the largest "
+                         "configuration that fits one GPU)")
+    ap.add_argument("--extra", default="c2,c3,c4",
+                    help="comma-separated workloads also measured in the same run, reported under "
+                         "'workloads' (not part of the value); empty for none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--ref-step-s", type=float, default=2.0)
+    ap.add_argument("--clock-soak-s", type=float, default=1.0,
+                    help="untimed steps run under the clock sampler right before the timed region")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager moe_ffn calls instead of a CUDA graph")
     ap.add_argument("--expected-m", type=int, default=None,
@@ -400,237 +754,65 @@ def main():
         raise SystemExit("--warmup must be >= 3")
 
     import torch
-    import fp8_grouped_expert_x128_gb300 as moe
-
     dev = torch.device("cuda", local if world > 1 else 0)
-    wl = build_workload(args.workload, dev)
-    if args.expected_m is not None:
-        wl["expected_m"] = args.expected_m
-    wl["gemm_flags"] = args.gemm_flags
-    cfg = wl["cfg"]
-    T, H = wl["T"], cfg.H
-    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    err = moe.new_error_word(dev)
-    events = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
-    desc = make_desc(wl, out, err=err)                           # the timed step
-    desc_ev = make_desc(wl, out, err=err, stage_events=events)   # the per-stage split
-    ws = moe.alloc_workspace(desc, dev)
+    peaks_raw, peak_src = load_peaks()
+    peaks = {"hbm_gbs": peaks_raw.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]),
+             "fp8_tflops": FP8_PER_BF16 * peaks_raw.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])}
     l2_flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    for _ in range(args.warmup):
-        moe.moe_ffn(desc, ws)
-    torch.cuda.synchronize(dev)
-    status, bits = moe.moe_read_device_status(err)
-    if status not in (moe.MOE_OK, moe.MOE_ERR_OVERFLOW):
-        raise SystemExit(f"device status {moe.moe_status_string(status)} during warm-up")
+    # other workloads first (each freed before the next), the headline last
+    extra = {}
+    for name in [n for n in args.extra.split(",") if n and n != args.workload]:
+        wl_x, st_x, rep_x, _ = measure(name, args, dev, world, l2_flush, stream, peaks, peak_src)
+        rep_x.update({"workload": f"{wl_x['cfg'].name}: {wl_x['cfg'].description}", "tokens": unit_name(wl_x)})
+        extra[name] = rep_x
+        del wl_x, st_x
+        torch.cuda.empty_cache()
 
-    # One step = one moe_ffn.  By default it is captured once in a CUDA graph
-    # (as the decode path runs in serving) and replayed.  The timed step is
-    # bracketed by two events on the stream around the replay; the per-stage
-    # split comes from a second graph of the same call with the stage events
-    # as event-record nodes (they sit between the kernels, so that graph is
-    # used for the split only).
-    step = lambda: moe.moe_ffn(desc, ws)
-    step_ev = lambda: moe.moe_ffn(desc_ev, ws)
-    graph = None
-    if not args.eager:
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(torch.cuda.current_stream(dev))
-        with torch.cuda.stream(side):
-            moe.moe_ffn(desc, ws)
-        torch.cuda.current_stream(dev).wait_stream(side)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            moe.moe_ffn(desc, ws)
-        graph_ev = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph_ev):
-            moe.moe_ffn(desc_ev, ws)
-        for _ in range(args.warmup):
-            graph.replay()
-            graph_ev.replay()
-        torch.cuda.synchronize(dev)
-        try:                                       # the graph's stage events must be timeable
-            events[0].elapsed_time(events[6])
-            step, step_ev = graph.replay, graph_ev.replay
-        except RuntimeError as exc:
-            print(f"graph stage events not timeable ({exc}); timing eager calls", file=sys.stderr)
-            graph = None
+    wl, st, rep, clk = measure(args.workload, args, dev, world, l2_flush, stream, peaks, peak_src,
+                               clk_seconds=args.clock_soak_s)
+    e2e = None if args.no_e2e else e2e_leg(wl, st, args, dev, world, l2_flush, stream)
 
-    step_ms = []
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    _barrier(world)
-    torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        t_wall = time.perf_counter()
-        for _ in range(args.steps):
-            l2_flush.fill_(1)                       # evict the previous step from L2
-            t0.record(stream)
-            step()
-            t1.record(stream)
-            torch.cuda.synchronize(dev)
-            step_ms.append(t0.elapsed_time(t1))
-        t_wall = time.perf_counter() - t_wall
-    _barrier(world)
-    torch.cuda.synchronize(dev)
-    status, bits = moe.moe_read_device_status(err)
-    if status not in (moe.MOE_OK, moe.MOE_ERR_OVERFLOW):
-        raise SystemExit(f"device status {moe.moe_status_string(status)} in the timed region")
-    stage_ms = [0.0] * 6
-    g1_ms = []
-    # instrumented passes for the per-stage split and the GEMM1 launch time
-    # (not part of the value)
-    n_split = max(3, min(args.steps, 10))
-    for _ in range(n_split):
-        l2_flush.fill_(1)
-        step_ev()
-        torch.cuda.synchronize(dev)
-        for i in range(6):
-            stage_ms[i] += events[i].elapsed_time(events[i + 1]) / n_split
-        g1_ms.append(events[2].elapsed_time(events[3]))
-
-    total_s = sum(step_ms) / 1e3
-    total_s = _max_over_ranks(world, total_s)
-    rows_all = _sum_over_ranks(world, wl["rows"] * args.steps)
-    value = rows_all / total_s
-    ms_per_step = 1e3 * total_s / args.steps
-
-    # ------------------------------------------------------------------ e2e (host buffers)
-    e2e = None
-    if not args.no_e2e:
-        x_h = wl["x"].cpu().pin_memory()
-        ids_h = wl["topk_ids"].cpu().pin_memory()
-        w_h = wl["topk_w"].cpu().pin_memory()
-        out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-        x_d = torch.empty_like(wl["x"])
-        ids_d = torch.empty_like(wl["topk_ids"])
-        w_d = torch.empty_like(wl["topk_w"])
-        d2 = make_desc(wl, out, err=err, x=x_d, ids=ids_d, w=w_d)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-
-        def host_step():
-            x_d.copy_(x_h, non_blocking=True); ids_d.copy_(ids_h, non_blocking=True)
-            w_d.copy_(w_h, non_blocking=True)
-            moe.moe_ffn(d2, ws)
-            out_h.copy_(out, non_blocking=True)
-
-        def time_e2e(run):
-            for _ in range(3):
-                run()
-            torch.cuda.synchronize(dev)
-            ms = []
-            for _ in range(args.steps):
-                l2_flush.fill_(1)
-                e0.record(stream)
-                run()
-                e1.record(stream)
-                torch.cuda.synchronize(dev)
-                ms.append(e0.elapsed_time(e1))
-            return _max_over_ranks(world, sum(ms) / 1e3)
-
-        def graphed(fn):
-            side = torch.cuda.Stream(dev)
-            side.wait_stream(torch.cuda.current_stream(dev))
-            with torch.cuda.stream(side):
-                fn()
-            torch.cuda.current_stream(dev).wait_stream(side)
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr):
-                fn()
-            return gr
-
-        # Three ways from host buffers, every byte crossing the host link inside
-        # the timed region of each step:
-        #  host I/O  moe_ffn given the pinned host x / routing / out directly:
-        #            the kernels read and write them in place, overlapped with
-        #            the compute (the library's host-buffer path; the value);
-        #  copies    explicit copies in, moe_ffn, copy out;
-        #  eager     the copies path with eager calls instead of a graph.
-        # The graph variants are captured once and replayed (as the decode
-        # path runs in serving); without graphs (--eager) all are eager.
-        eager_s = time_e2e(host_step)
-        copies_s = time_e2e(graphed(host_step).replay) if graph is not None else eager_s
-        d_host = make_desc(wl, out_h, err=err, x=x_h, ids=ids_h, w=w_h)
-        host_io = lambda: moe.moe_ffn(d_host, ws)
-        try:
-            host_io()
-            torch.cuda.synchronize(dev)
-            host_s = time_e2e(graphed(host_io).replay if graph is not None else host_io)
-        except moe.MoeError as exc:
-            print(f"host-buffer moe_ffn refused ({exc}); e2e = the copies path", file=sys.stderr)
-            host_s = None
-        e2e_s = host_s if host_s is not None else copies_s
-        h2d = x_h.numel() * 2 + ids_h.numel() * 4 + w_h.numel() * 4
-        e2e = {"value": rows_all / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(out_h.numel() * 2),
-               "ms_per_step": 1e3 * e2e_s / args.steps,
-               "copies": {"value": rows_all / copies_s, "ms_per_step": 1e3 * copies_s / args.steps},
-               "eager": {"value": rows_all / eager_s, "ms_per_step": 1e3 * eager_s / args.steps},
-               "how": ("moe_ffn on pinned host x, topk_ids, topk_w and out (read and written in place "
-                       "by the kernels across the host link)" if host_s is not None else
-                       "pinned-host x, topk_ids, topk_w -> device, moe_ffn, out -> pinned host")
-                      + ("; one CUDA graph replay per step" if graph is not None else "; eager calls")
-                      + "; 'copies' = explicit copies in and out around moe_ffn; 'eager' = copies, eager calls"}
-
-    # ------------------------------------------------------------------ roofline (GEMM1)
-    peaks, peak_src = load_peaks()
-    alg = algorithmic_counts(wl)
-    g1_s = statistics.mean(g1_ms) / 1e3
-    hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    fp8_peak = FP8_PER_BF16 * peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    t_mem = alg["g1_bytes"] / (hbm_peak * 1e9)
-    t_cmp = alg["flops_g1"] / (fp8_peak * 1e12)
-    if t_mem >= t_cmp:
-        achieved = alg["g1_bytes"] / g1_s / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak}
-    else:
-        achieved = alg["flops_g1"] / g1_s / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                "frac": achieved / fp8_peak}
-    kname = gemm1_variant(wl)
-    what = "GEMM1 (W13) + SwiGLU + FP8 requant" if gemm1_fused(wl) else "GEMM1 (W13)"
-    roof.update({"traffic": recorded_traffic(kname, args.workload), "kernel": f"{kname} ({what})",
-                 "launch_ms": 1e3 * g1_s, "peak_source": f"{peak_src}" +
-                 ("" if roof["bound"] == "hbm" else " bf16 burst x2 (nominal FP8:BF16)"),
-                 "algorithmic": {"bytes": alg["g1_bytes"], "flops": alg["flops_g1"]}})
-
-    # ------------------------------------------------------------------ CPU oracle baseline
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ref_wl = dict(wl, x_host_bits=wl["x"].cpu().view(torch.int16).numpy().view(np.uint16))
         oracle_w = OracleWeights(ref_wl, dev)
-        rate, dt, ntok, nrows = time_oracle(ref_wl, oracle_w, budget_s=args.cpu_budget_s)
+        rate, dt, nrows = time_oracle(ref_wl, oracle_w, budget_s=args.cpu_budget_s)
         cpu = {"value": rate, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"first {ntok} local tokens ({nrows} routed rows) through the whole "
-                         f"chain, {dt:.1f}s; numpy float64, BLAS threads = all affinity cores"}
+               "sample": f"the first {nrows} routed rows in assignment order through the whole chain "
+                         f"(quant, GEMM1, SwiGLU+quant, GEMM2, combine), {dt:.1f}s, scaled to "
+                         f"{unit_name(wl)} at {units_per_step(wl) / wl['rows']:.4g} per routed row; "
+                         "numpy float64, BLAS threads = all affinity cores"}
 
     if rank == 0:
+        k = rep["kernels"]
+        dominant = max(("gemm1", "gemm2"), key=lambda w: k[w]["launch_ms"])
+        roof = dict(k[dominant])
+        clocks = clk.summary() if clk is not None else {"sm_mhz": None, "reasons": ["unsampled"]}
+        clocks["window"] = (f"{args.clock_soak_s:.1f}s of untimed steps immediately before the timed region, "
+                            "and the timed region")
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "metric": METRIC, "value": rep["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": rep["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate, bf16 out)",
             "data": "synthetic (seeded)",
-            "config": {"workload": f"{cfg.name}: {cfg.description}",
-                       "tokens": "routed (token, local expert) rows", "rows_per_step": wl["rows"],
-                       "local_tokens": T, "counts": [int(c) for c in wl["counts"]],
-                       "max_m": cfg.max_m, "active_experts": wl["active_experts"],
-                       "expected_m_hint": wl["expected_m"], "gemm_flags": args.gemm_flags,
-                       "l2": "flushed (256 MiB write) before every timed step",
-                       "launch": "eager moe_ffn" if graph is None else "moe_ffn captured once in a CUDA graph, replayed per step",
-                       "timing": "CUDA events on the launching stream around each step; stage split from a separate instrumented replay",
-                       "parallelism": f"replicas x{world}"},
-            "stage_ms": {n: round(v, 4) for n, v in zip(
-                ["quant (fused into permute)", "quant+permute", "gemm1", "swiglu_quant (fused into gemm1 when 0)", "gemm2", "combine (fused into gemm2 when 0)"], stage_ms)},
-            "tflops": alg["flops"] / (ms_per_step / 1e3) / 1e12,
-            "weight_gbs": alg["weight_bytes"] / (ms_per_step / 1e3) / 1e9,
+            "config": config_dict(wl, world),
+            "stage_ms": rep["stage_ms"],
+            "tflops": rep["tflops"], "weight_gbs": rep["weight_gbs"],
             "roofline": roof,
+            "kernels": k,
+            "step_roofline": rep["step_roofline"],
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": moe.moe_ffn_kernel_count(desc) * args.steps,
-            "clocks": clk.summary(),
-            "device_status": moe.moe_status_string(status),
-            "wall_s_timed": t_wall,
+            "gpu_launches": rep["gpu_launches"],
+            "clocks": clocks,
+            "device_status": rep["device_status"],
+            "tuning": rep["tuning"],
+            "timing": "CUDA events on the launching stream around each step (graph replay); stage split "
+                      "and GEMM launch times from a separate instrumented replay",
+            "wall_s_timed": rep["wall_s_timed"],
+            "workloads": extra,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
