@@ -40,16 +40,28 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # ----------------------------------------------------------------------------- workload
-def build_workload(cfg_name: str, device="cuda", gen_device=None):
+def build_workload(cfg_name: str, device="cuda", gen_device=None, ue8m0=False, local_experts=None):
     """Seeded inputs of one config resident on `device`; expert weights quantised
-    to E4M3 128x128 blocks by the library's weight-quant kernel.  The inputs are
-    drawn on `gen_device` (default: `device`) and copied over; the generator is
-    device independent, so the values are the same either way."""
+    to E4M3 128x128 blocks by the library's weight-quant kernel (with `ue8m0`:
+    power-of-two tile scales, also packed for the block-scaled GEMMs, and the
+    FFN run with MOE_FFN_UE8M0).  The inputs are drawn on `gen_device`
+    (default: `device`) and copied over; the generator is device independent,
+    so the values are the same either way.  `local_experts` keeps the routing
+    and keeps only the first that many local experts resident (the others act
+    as another rank's: their routing slots are skipped) -- a cut-down case of
+    the same workload for profiling."""
+    import dataclasses
     import torch
     import fp8_grouped_expert_x128_gb300 as moe
     gen = device if gen_device is None else gen_device
     cfg = synth.get_config(cfg_name)
     r = synth.make_routing(cfg)
+    cut = local_experts is not None and local_experts < cfg.E
+    if cut:
+        cfg = dataclasses.replace(cfg, E=local_experts,
+                                  description=cfg.description + f" [cut down to the first {local_experts} "
+                                                                "local experts, for profiling]")
+        r = dict(r, E=cfg.E)
     T, k = r["T"], r["k"]
     x = synth.make_activations(cfg, T, device=gen).to(device)
     ids = torch.from_numpy(r["topk_ids"].astype(np.int32)).to(device)
@@ -59,12 +71,20 @@ def build_workload(cfg_name: str, device="cuda", gen_device=None):
     w13_s = torch.empty((E, 2 * I // 128, H // 128), dtype=torch.float32, device=device)
     w2 = torch.empty((E, H, I), dtype=torch.uint8, device=device)
     w2_s = torch.empty((E, H // 128, I // 128), dtype=torch.float32, device=device)
+    wquant = moe.moe_quant_weight_fp8_ue8m0 if ue8m0 else moe.moe_quant_weight_fp8
     for e in range(E):
         b13 = synth.make_expert_weights(cfg, "w13", e, device=gen).to(device)
-        moe.moe_quant_weight_fp8(b13[None], w13[e:e + 1], w13_s[e:e + 1])
+        wquant(b13[None], w13[e:e + 1], w13_s[e:e + 1])
         b2 = synth.make_expert_weights(cfg, "w2", e, device=gen).to(device)
-        moe.moe_quant_weight_fp8(b2[None], w2[e:e + 1], w2_s[e:e + 1])
+        wquant(b2[None], w2[e:e + 1], w2_s[e:e + 1])
         del b13, b2
+    extra = {}
+    if ue8m0:
+        w13_sf = torch.empty(moe.moe_ue8m0_weight_words(E, 2 * I, H), dtype=torch.int32, device=device)
+        w2_sf = torch.empty(moe.moe_ue8m0_weight_words(E, H, I), dtype=torch.int32, device=device)
+        moe.moe_pack_ue8m0_weight(w13_s, w13_sf, H)
+        moe.moe_pack_ue8m0_weight(w2_s, w2_sf, I)
+        extra = dict(w13_sf=w13_sf, w2_sf=w2_sf, gemm_flags=moe.MOE_FFN_UE8M0, ue8m0=True)
     torch.cuda.synchronize()
     layout = moe.MOE_LAYOUT_MASKED if cfg.layout == "masked" else moe.MOE_LAYOUT_CONTIG
     local = (r["topk_ids"] >= r["expert_begin"]) & (r["topk_ids"] < r["expert_begin"] + E)
@@ -74,7 +94,7 @@ def build_workload(cfg_name: str, device="cuda", gen_device=None):
     expected_m = int(math.ceil(rows / max(1, int((counts > 0).sum()))))
     return dict(cfg=cfg, routing=r, T=T, k=k, x=x, topk_ids=ids, topk_w=w, w13=w13, w13_s=w13_s,
                 w2=w2, w2_s=w2_s, layout=layout, rows=rows, counts=counts,
-                active_experts=int((counts > 0).sum()), expected_m=expected_m)
+                active_experts=int((counts > 0).sum()), expected_m=expected_m, **extra)
 
 
 def make_desc(wl, out, err=None, stage_events=None, x=None, ids=None, w=None):
@@ -84,12 +104,29 @@ def make_desc(wl, out, err=None, stage_events=None, x=None, ids=None, w=None):
                              w if w is not None else wl["topk_w"], wl["w13"], wl["w13_s"], wl["w2"],
                              wl["w2_s"], out, wl["routing"]["expert_begin"], cfg.E, wl["layout"],
                              max_m=cfg.max_m, expected_m=wl["expected_m"],
-                             gemm_flags=wl.get("gemm_flags", 0), err=err, stage_events=stage_events)
+                             gemm_flags=wl.get("gemm_flags", 0), err=err, stage_events=stage_events,
+                             w13_sf=wl.get("w13_sf"), w2_sf=wl.get("w2_sf"))
+
+
+def is_ue8m0(wl):
+    import fp8_grouped_expert_x128_gb300 as moe
+    return bool(wl.get("gemm_flags", 0) & moe.MOE_FFN_UE8M0)
+
+
+def _ue8m0_variant(wl):
+    import fp8_grouped_expert_x128_gb300 as moe
+    if wl["layout"] == moe.MOE_LAYOUT_MASKED:
+        v = moe.moe_gemm_fp8_masked_variant(wl["cfg"].max_m, wl["expected_m"], wl.get("gemm_flags", 0))
+        if v != 0:
+            return f"gemm_fp8_ue8m0_weights_m_kernel<{min(v, 128)}>"
+    return "gemm_fp8_ue8m0_kernel"
 
 
 def gemm1_variant(wl):
     """The GEMM1 kernel moe_ffn runs for this workload."""
     import fp8_grouped_expert_x128_gb300 as moe
+    if is_ue8m0(wl):
+        return _ue8m0_variant(wl)
     if wl["layout"] == moe.MOE_LAYOUT_MASKED:
         v = moe.moe_gemm_fp8_masked_variant(wl["cfg"].max_m, wl["expected_m"], wl.get("gemm_flags", 0))
         if v != 0:
@@ -106,6 +143,8 @@ def gemm1_fused(wl):
 def gemm2_variant(wl):
     """The GEMM2 kernel moe_ffn runs for this workload."""
     import fp8_grouped_expert_x128_gb300 as moe
+    if is_ue8m0(wl):
+        return _ue8m0_variant(wl)
     if wl["layout"] == moe.MOE_LAYOUT_MASKED:
         v = moe.moe_gemm_fp8_masked_variant(wl["cfg"].max_m, wl["expected_m"], wl.get("gemm_flags", 0))
         if v != 0:
@@ -119,7 +158,7 @@ def combine_fused(wl):
     """moe_ffn folds the combine into GEMM2's epilogue for one routing slot per
     token (device output; the tokens-as-M kernel serving GEMM2)."""
     import fp8_grouped_expert_x128_gb300 as moe
-    if wl["k"] != 1:
+    if wl["k"] != 1 or is_ue8m0(wl):
         return False
     if wl["layout"] == moe.MOE_LAYOUT_MASKED:
         return moe.moe_gemm_fp8_masked_variant(wl["cfg"].max_m, wl["expected_m"], wl.get("gemm_flags", 0)) == 0
@@ -144,12 +183,13 @@ def algorithmic_counts(wl):
     H, I = cfg.H, cfg.I
     rows, act, T, k = wl["rows"], wl["active_experts"], wl["T"], wl["k"]
     fused = gemm1_fused(wl)
+    sb = 1 if is_ue8m0(wl) else 4                    # bytes per block scale: exponent byte or fp32
     flops_g1 = 2.0 * rows * H * 2 * I
     flops_g2 = 2.0 * rows * I * H
-    w13_bytes = act * (2 * I * H + 4 * (2 * I // 128) * (H // 128))
-    w2_bytes = act * (H * I + 4 * (H // 128) * (I // 128))
-    a1 = rows * (H + 4 * H / 128)                    # FP8 rows + fp32 scales into GEMM1
-    a2 = rows * (I + 4 * I / 128)                    # FP8 h + scales into GEMM2
+    w13_bytes = act * (2 * I * H + sb * (2 * I // 128) * (H // 128))
+    w2_bytes = act * (H * I + sb * (H // 128) * (I // 128))
+    a1 = rows * (H + sb * H / 128)                   # FP8 rows + their scales into GEMM1
+    a2 = rows * (I + sb * I / 128)                   # FP8 h + scales into GEMM2
     y1 = rows * 2 * I * 2                            # bf16 Y1
     y2 = rows * H * 2                                # bf16 Y2
     out = T * H * 2
@@ -593,11 +633,13 @@ def kernel_rooflines(wl, name, g1_s, g2_s, peaks, peak_src):
 
 
 def measure(name, args, dev, world, l2_flush, stream, peaks, peak_src, clk_seconds=0.0):
-    """Build a workload, time K steps, and report its line fields."""
-    wl = build_workload(name, dev)
+    """Build a workload ('<config>' or '<config>:ue8m0' for the power-of-two
+    reading of the scales end to end), time K steps, and report its line fields."""
+    cfg_name, _, variant = name.partition(":")
+    wl = build_workload(cfg_name, dev, ue8m0=variant == "ue8m0", local_experts=args.local_experts)
     if args.expected_m is not None:
         wl["expected_m"] = args.expected_m
-    wl["gemm_flags"] = args.gemm_flags
+    wl["gemm_flags"] = wl.get("gemm_flags", 0) | args.gemm_flags
     st = Step(wl, dev, eager=args.eager)
     st.capture(args.warmup)
     clk = ClockSampler(dev.index if dev.index is not None else 0) if clk_seconds > 0 else None
@@ -623,13 +665,13 @@ def measure(name, args, dev, world, l2_flush, stream, peaks, peak_src, clk_secon
     rep = {
         "value": units / total_s, "ms_per_step": ms_per_step,
         "stage_ms": {n: round(v, 4) for n, v in zip(STAGES, stage_ms)},
-        "kernels": kernel_rooflines(wl, name, g1_s, g2_s, peaks, peak_src),
+        "kernels": kernel_rooflines(wl, name.replace(":", "-"), g1_s, g2_s, peaks, peak_src),
         "step_roofline": roofline(alg["flops"], alg["step_bytes"], ms_per_step / 1e3, peaks),
         "tflops": alg["flops"] / (ms_per_step / 1e3) / 1e12,
         "weight_gbs": alg["weight_bytes"] / (ms_per_step / 1e3) / 1e9,
         "gpu_launches": moe_kernel_count(st) * args.steps,
         "device_status": st.moe.moe_status_string(status),
-        "tuning": {"expected_m_hint": wl["expected_m"], "gemm_flags": args.gemm_flags,
+        "tuning": {"expected_m_hint": wl["expected_m"], "gemm_flags": wl["gemm_flags"],
                    "launch": "eager moe_ffn" if st.graph is None else
                              "moe_ffn captured once in a CUDA graph, replayed per step",
                    "gemm1": gemm1_variant(wl), "gemm2": gemm2_variant(wl)},
@@ -732,15 +774,19 @@ def main():
     ap.add_argument("--workload", default="c5",
                     help="the headline workload (default: the all-experts decode layer, the largest "
                          "configuration that fits one GPU)")
-    ap.add_argument("--extra", default="c2,c3,c4",
+    ap.add_argument("--extra", default="c2,c3,c4,c3:ue8m0,c4:ue8m0,c2:ue8m0,c5:ue8m0",
                     help="comma-separated workloads also measured in the same run, reported under "
-                         "'workloads' (not part of the value); empty for none")
+                         "'workloads' (not part of the value); '<config>:ue8m0' runs the power-of-two "
+                         "reading of the scales end to end (block-scaled GEMMs); empty for none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--ref-step-s", type=float, default=2.0)
     ap.add_argument("--clock-soak-s", type=float, default=1.0,
                     help="untimed steps run under the clock sampler right before the timed region")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--local-experts", type=int, default=None,
+                    help="keep only the first N local experts resident (the rest act as another rank's); "
+                         "a cut-down case of the workload for profiling, not a bench line")
     ap.add_argument("--eager", action="store_true", help="time eager moe_ffn calls instead of a CUDA graph")
     ap.add_argument("--expected-m", type=int, default=None,
                     help="override the per-expert count hint given to the masked GEMMs (tuning)")
@@ -765,7 +811,9 @@ def main():
     extra = {}
     for name in [n for n in args.extra.split(",") if n and n != args.workload]:
         wl_x, st_x, rep_x, _ = measure(name, args, dev, world, l2_flush, stream, peaks, peak_src)
-        rep_x.update({"workload": f"{wl_x['cfg'].name}: {wl_x['cfg'].description}", "tokens": unit_name(wl_x)})
+        rep_x.update({"workload": f"{wl_x['cfg'].name}: {wl_x['cfg'].description}", "tokens": unit_name(wl_x),
+                      "scales": "UE8M0 (power-of-two, packed; block-scaled MMA)" if is_ue8m0(wl_x)
+                                else "fp32 (per-k-block promotion)"})
         extra[name] = rep_x
         del wl_x, st_x
         torch.cuda.empty_cache()

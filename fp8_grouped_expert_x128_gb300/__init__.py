@@ -41,6 +41,7 @@ MOE_GEMM_FORCE_TOKENS_M = 0x1
 MOE_GEMM_FORCE_WEIGHTS_M = 0x2
 MOE_FFN_FUSE_SWIGLU = 0x4
 MOE_GEMM_CTA_PAIR = 0x8
+MOE_FFN_UE8M0 = 0x10
 MOE_GEMM_DEBUG_STALL = 0x100
 MOE_QUANT_UE8M0 = 0x1
 MOE_COMBINE_ACCUMULATE = 0x1
@@ -50,7 +51,8 @@ EXPORTED = [
     "moe_quant_weight_fp8", "moe_contig_rows_bound", "moe_permute", "moe_gemm_fp8_contig",
     "moe_gemm_fp8_masked", "moe_gemm_fp8_masked_variant", "moe_swiglu_quant", "moe_combine", "moe_ffn_workspace_size", "moe_ffn",
     "moe_ffn_noalloc", "moe_ffn_noalloc_capacity", "moe_ffn_kernel_count", "moe_quant_fp8_ue8m0",
-    "moe_ue8m0_scale",
+    "moe_ue8m0_scale", "moe_quant_weight_fp8_ue8m0", "moe_ue8m0_act_words", "moe_ue8m0_weight_words",
+    "moe_pack_ue8m0_act", "moe_pack_ue8m0_weight", "moe_gemm_fp8_contig_ue8m0", "moe_gemm_fp8_masked_ue8m0",
 ]
 
 _P = ctypes.c_void_p
@@ -63,7 +65,7 @@ class moe_ffn_desc(ctypes.Structure):
         ("T", _I64), ("H", _I32), ("I", _I32), ("k", _I32), ("expert_begin", _I32), ("E", _I32),
         ("layout", _I32), ("max_m", _I32), ("expected_m", _I32), ("gemm_flags", _I32),
         ("x", _P), ("topk_ids", _P), ("topk_w", _P), ("w13", _P), ("w13_s", _P), ("w2", _P),
-        ("w2_s", _P), ("out", _P), ("err", _P), ("stage_events", _P),
+        ("w2_s", _P), ("out", _P), ("err", _P), ("stage_events", _P), ("w13_sf", _P), ("w2_sf", _P),
     ]
 
 
@@ -82,6 +84,7 @@ _sig("moe_quant_fp8", ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _
 _sig("moe_quant_fp8_ue8m0", ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _I64, _P, _P])
 _sig("moe_ue8m0_scale", ctypes.c_float, [ctypes.c_float, ctypes.POINTER(ctypes.c_uint8)])
 _sig("moe_quant_weight_fp8", ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P])
+_sig("moe_quant_weight_fp8_ue8m0", ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _P])
 _sig("moe_contig_rows_bound", _I64, [_I64, _I32])
 _sig("moe_permute", ctypes.c_int,
      [_P, _P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _I64, _P, _P, _P, _P,
@@ -91,8 +94,16 @@ _sig("moe_gemm_fp8_contig", ctypes.c_int,
 _sig("moe_gemm_fp8_masked", ctypes.c_int,
      [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I32, _P, _P])
 _sig("moe_gemm_fp8_masked_variant", ctypes.c_int, [_I32, _I32, _I32])
-_sig("moe_swiglu_quant", ctypes.c_int, [_P, _I64, _I32, _P, _I32, _P, _P, _P, _I64, _P, _P])
+_sig("moe_swiglu_quant", ctypes.c_int, [_P, _I64, _I32, _P, _I32, _P, _P, _P, _I64, _I32, _P, _P])
 _sig("moe_combine", ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I32, _I32, _P, _I64, _I32, _P, _I64, _P, _P])
+_sig("moe_ue8m0_act_words", _I64, [_I64, _I64, _I64])
+_sig("moe_ue8m0_weight_words", _I64, [_I64, _I64, _I64])
+_sig("moe_pack_ue8m0_act", ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P])
+_sig("moe_pack_ue8m0_weight", ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P])
+_sig("moe_gemm_fp8_contig_ue8m0", ctypes.c_int,
+     [_P, _I64, _P, _I64, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _P, _I64, _I32, _P, _P])
+_sig("moe_gemm_fp8_masked_ue8m0", ctypes.c_int,
+     [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I32, _P, _P])
 _sig("moe_ffn_workspace_size", ctypes.c_size_t, [ctypes.POINTER(moe_ffn_desc)])
 _sig("moe_ffn_kernel_count", ctypes.c_int, [ctypes.POINTER(moe_ffn_desc)])
 _sig("moe_ffn", ctypes.c_int, [ctypes.POINTER(moe_ffn_desc), _P, ctypes.c_size_t, _P])
@@ -201,6 +212,17 @@ def moe_quant_weight_fp8(w, q, s, stream=None):
     return q, s
 
 
+def moe_quant_weight_fp8_ue8m0(w, q, s, e8=None, stream=None):
+    """a3 with power-of-two tile scales: s fp32 [E, N/128, K/128] holds 2^e, e8
+    uint8 (optional, same shape) holds e + 127."""
+    _dev(w, torch.bfloat16, "w"); _dev(q, _U8, "q"); _dev(s, torch.float32, "s"); _dev(e8, _U8, "e8")
+    E, N, K = w.shape
+    assert w.is_contiguous() and q.is_contiguous() and s.is_contiguous()
+    _check(_lib.moe_quant_weight_fp8_ue8m0(_ptr(w), E, N, K, _ptr(_u8(q)), _ptr(s), _ptr(e8), _stream(stream)),
+           "moe_quant_weight_fp8_ue8m0")
+    return q, s
+
+
 def moe_permute(q, s, topk_ids, expert_begin, E, layout, max_m, q_out, s_out, counts, offsets,
                 m_indices, row_src, dst_row, rows_capacity=0, s_ld=None, s_out_ld=None, err=None,
                 stream=None):
@@ -244,14 +266,58 @@ def moe_gemm_fp8_masked_variant(max_m: int, expected_m: int = 0, flags: int = 0)
     return int(_lib.moe_gemm_fp8_masked_variant(max_m, expected_m, flags))
 
 
-def moe_swiglu_quant(Y1, q, s, counts=None, max_m=0, m_indices=None, s_ld=0, err=None,
+def moe_ue8m0_act_words(groups: int, G: int, K: int) -> int:
+    return int(_lib.moe_ue8m0_act_words(groups, G, K))
+
+
+def moe_ue8m0_weight_words(E: int, N: int, K: int) -> int:
+    return int(_lib.moe_ue8m0_weight_words(E, N, K))
+
+
+def moe_pack_ue8m0_act(s, groups, G, rows, K, sfA, stream=None):
+    """Power-of-two fp32 scales in the grouped layout (groups of G rows) -> packed
+    UE8M0 words sfA (int32 tensor of moe_ue8m0_act_words(groups, G, K) words)."""
+    _dev(s, torch.float32, "s"); _dev(sfA, torch.int32, "sfA")
+    _check(_lib.moe_pack_ue8m0_act(_ptr(s), groups, G, rows, K, _ptr(sfA), _stream(stream)), "moe_pack_ue8m0_act")
+    return sfA
+
+
+def moe_pack_ue8m0_weight(s, sfB, K, stream=None):
+    """Power-of-two fp32 weight scales [E, N/128, K/128] -> packed records sfB."""
+    _dev(s, torch.float32, "s"); _dev(sfB, torch.int32, "sfB")
+    E, NB, _ = s.shape
+    _check(_lib.moe_pack_ue8m0_weight(_ptr(s), E, NB * 128, K, _ptr(sfB), _stream(stream)), "moe_pack_ue8m0_weight")
+    return sfB
+
+
+def moe_gemm_fp8_contig_ue8m0(A, sfA, sfA_ld, B, sfB, offsets, m_indices, D, flags=0, err=None, stream=None):
+    """a4/a6 with packed UE8M0 scales, contiguous layout."""
+    E, N, K = B.shape
+    _check(_lib.moe_gemm_fp8_contig_ue8m0(_ptr(_u8(A)), A.stride(0), _ptr(sfA), sfA_ld, _ptr(_u8(B)), _ptr(sfB),
+                                          _ptr(offsets), _ptr(m_indices), A.shape[0], E, N, K, _ptr(D),
+                                          D.stride(0), flags, _ptr(err), _stream(stream)), "moe_gemm_fp8_contig_ue8m0")
+    return D
+
+
+def moe_gemm_fp8_masked_ue8m0(A, sfA, B, sfB, counts, D, expected_m=0, flags=0, err=None, stream=None):
+    """a4/a6 with packed UE8M0 scales, masked layout: A [E, max_m, K], D [E, max_m, N]."""
+    E, max_m, K = A.shape
+    N = B.shape[1]
+    _check(_lib.moe_gemm_fp8_masked_ue8m0(_ptr(_u8(A)), _ptr(sfA), _ptr(_u8(B)), _ptr(sfB), _ptr(counts), E, max_m,
+                                          N, K, expected_m, _ptr(D), flags, _ptr(err), _stream(stream)),
+           "moe_gemm_fp8_masked_ue8m0")
+    return D
+
+
+def moe_swiglu_quant(Y1, q, s, counts=None, max_m=0, m_indices=None, s_ld=0, flags=0, err=None,
                      stream=None):
     """a5: Y1 bf16 [rows, 2I] -> q uint8 [rows, I] + scales (groups of max_m rows when
-    ``counts`` is given, else one group of ``s_ld`` rows selected by ``m_indices``)."""
+    ``counts`` is given, else one group of ``s_ld`` rows selected by ``m_indices``);
+    flags = MOE_QUANT_UE8M0 for power-of-two scales."""
     two_i = Y1.shape[-1]
     rows = Y1.numel() // two_i
     _check(_lib.moe_swiglu_quant(_ptr(Y1), rows, two_i // 2, _ptr(counts), max_m, _ptr(m_indices),
-                                 _ptr(_u8(q)), _ptr(s), s_ld, _ptr(err), _stream(stream)),
+                                 _ptr(_u8(q)), _ptr(s), s_ld, flags, _ptr(err), _stream(stream)),
            "moe_swiglu_quant")
 
 
@@ -269,15 +335,18 @@ def moe_combine(Y2, dst_row, topk_w, out, shared=None, flags=0, err=None, stream
 
 
 def make_ffn_desc(x, topk_ids, topk_w, w13, w13_s, w2, w2_s, out, expert_begin, E, layout,
-                  max_m=0, expected_m=0, gemm_flags=0, err=None, stage_events=None):
+                  max_m=0, expected_m=0, gemm_flags=0, err=None, stage_events=None, w13_sf=None, w2_sf=None):
     T, H = x.shape
     I = w2.shape[2]
     d = moe_ffn_desc(T=T, H=H, I=I, k=topk_ids.shape[1], expert_begin=expert_begin, E=E,
                      layout=layout, max_m=max_m, expected_m=expected_m, gemm_flags=gemm_flags,
                      x=x.data_ptr(), topk_ids=topk_ids.data_ptr(), topk_w=topk_w.data_ptr(),
-                     w13=_u8(w13).data_ptr(), w13_s=w13_s.data_ptr(), w2=_u8(w2).data_ptr(),
-                     w2_s=w2_s.data_ptr(), out=out.data_ptr(),
-                     err=err.data_ptr() if err is not None else None, stage_events=None)
+                     w13=_u8(w13).data_ptr(), w13_s=w13_s.data_ptr() if w13_s is not None else None,
+                     w2=_u8(w2).data_ptr(),
+                     w2_s=w2_s.data_ptr() if w2_s is not None else None, out=out.data_ptr(),
+                     err=err.data_ptr() if err is not None else None, stage_events=None,
+                     w13_sf=w13_sf.data_ptr() if w13_sf is not None else None,
+                     w2_sf=w2_sf.data_ptr() if w2_sf is not None else None)
     if stage_events is not None:
         if len(stage_events) != 7:
             raise ValueError("stage_events needs 7 events")

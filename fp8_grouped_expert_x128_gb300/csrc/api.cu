@@ -84,6 +84,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 
 struct FfnPlan {
   int64_t T_pad, rows, s_ld1, s_ld2;
+  bool ue8m0;   // packed power-of-two activation scales (off_sa1 / off_sa2 hold words)
   size_t off_counts, off_offsets, off_mind, off_rowsrc, off_dst, off_a1, off_sa1,
       off_y1, off_a2, off_sa2, off_y2, total;
 };
@@ -117,11 +118,20 @@ int plan_ffn(const moe_ffn_desc* d, FfnPlan* p) {
   p->off_mind = take(sizeof(int32_t) * p->rows);
   p->off_rowsrc = take(sizeof(int32_t) * p->rows);
   p->off_dst = take(sizeof(int32_t) * d->T * d->k);
+  p->ue8m0 = (d->gemm_flags & MOE_FFN_UE8M0) != 0;
+  // packed UE8M0 scales: masked -> one group of max_m rows per expert;
+  // contiguous -> one group of `rows` rows (a multiple of 128)
+  const int64_t groups = d->layout == MOE_LAYOUT_MASKED ? E : 1;
+  const int64_t G = d->layout == MOE_LAYOUT_MASKED ? d->max_m : p->rows;
+  auto scale_bytes = [&](int64_t K) {
+    return p->ue8m0 ? sizeof(uint32_t) * static_cast<size_t>(moe_ue8m0_act_words(groups, G, K))
+                    : sizeof(float) * (K / 128) * p->rows;
+  };
   p->off_a1 = take(static_cast<size_t>(p->rows) * H);
-  p->off_sa1 = take(sizeof(float) * (H / 128) * p->rows);
+  p->off_sa1 = take(scale_bytes(H));
   p->off_y1 = take(sizeof(uint16_t) * p->rows * 2 * I);
   p->off_a2 = take(static_cast<size_t>(p->rows) * I);
-  p->off_sa2 = take(sizeof(float) * (I / 128) * p->rows);
+  p->off_sa2 = take(scale_bytes(I));
   p->off_y2 = take(sizeof(uint16_t) * p->rows * H);
   p->total = o;
   return MOE_OK;
@@ -204,6 +214,10 @@ FfnFusion ffn_fusion(const moe_ffn_desc* d, bool out_on_host) {
   const bool masked = d->layout == MOE_LAYOUT_MASKED;
   const int32_t gflags = d->gemm_flags & ~MOE_FFN_FUSE_SWIGLU;
   FfnFusion f;
+  if (d->gemm_flags & MOE_FFN_UE8M0) {   // the block-scaled GEMMs have no fused epilogues
+    f.swiglu = f.combine = false;
+    return f;
+  }
   // stages 3+4: on request (MOE_FFN_FUSE_SWIGLU) and where the tokens-as-M
   // kernel serves GEMM1, SwiGLU and the FP8 requantisation run in its
   // epilogue (no bf16 Y1 round trip); otherwise GEMM1 writes Y1 and the
@@ -250,14 +264,20 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
   if (int st = plan_ffn(d, &p)) return st;
   MOE_CHECK_ARG(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255) == 0);
   MOE_CHECK_ARG(workspace_bytes >= p.total);
-  MOE_CHECK_ARG(d->x && d->topk_ids && d->topk_w && d->w13 && d->w13_s && d->w2 && d->w2_s && d->out);
+  const bool ue8m0 = p.ue8m0;
+  MOE_CHECK_ARG(d->x && d->topk_ids && d->topk_w && d->w13 && d->w2 && d->out);
+  if (ue8m0)
+    MOE_CHECK_ARG(d->w13_sf && d->w2_sf && aligned16(d->w13_sf) && aligned16(d->w2_sf));
+  else
+    MOE_CHECK_ARG(d->w13_s && d->w2_s);
   if (int st = check_device()) return st;
   const void* io[3] = {d->x, d->topk_ids, d->topk_w};
   for (const void* ptr : io)
     if (int rc = check_placement(ptr, true)) return rc;
   bool out_on_host = false;
   if (int rc = check_placement(d->out, true, &out_on_host)) return rc;
-  const void* on_device[5] = {d->w13, d->w13_s, d->w2, d->w2_s, workspace};
+  const void* on_device[5] = {d->w13, ue8m0 ? static_cast<const void*>(d->w13_sf) : d->w13_s, d->w2,
+                              ue8m0 ? static_cast<const void*>(d->w2_sf) : d->w2_s, workspace};
   for (const void* ptr : on_device)
     if (int rc = check_placement(ptr, false)) return rc;
   cudaStream_t st = as_stream(stream);
@@ -289,7 +309,7 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
     return MOE_OK;
   };
   int rc;
-  const int32_t gflags = d->gemm_flags & ~MOE_FFN_FUSE_SWIGLU;
+  const int32_t gflags = d->gemm_flags & ~(MOE_FFN_FUSE_SWIGLU | MOE_FFN_UE8M0);
   const FfnFusion fusion = ffn_fusion(d, out_on_host);
   const bool fuse_combine = fusion.combine;
   // stages 1+2: routing index pass, then each routed token row is quantised
@@ -297,11 +317,37 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
   if ((rc = mark(0))) return rc;
   if ((rc = mark(1))) return rc;
   if ((rc = permute_launch(nullptr, nullptr, 0, d->x, d->H, d->topk_ids, d->T, d->H, d->k,
-                           d->expert_begin, d->E, d->layout, d->max_m, a1, sa1, p.s_ld1, counts,
+                           d->expert_begin, d->E, d->layout, d->max_m, a1, ue8m0 ? nullptr : sa1, p.s_ld1, counts,
                            offsets, mind, rowsrc, dst, p.rows, d->err, st, fuse_combine ? d->out : nullptr,
-                           d->H)))
+                           d->H, ue8m0 ? reinterpret_cast<uint8_t*>(sa1) : nullptr)))
     return rc;
   if ((rc = mark(2))) return rc;
+  if (ue8m0) {
+    // the power-of-two reading end to end: block-scaled GEMMs on packed scales
+    const uint32_t* sf1 = reinterpret_cast<const uint32_t*>(sa1);
+    const uint32_t* sf2 = reinterpret_cast<const uint32_t*>(sa2);
+    rc = masked ? moe_gemm_fp8_masked_ue8m0(a1, sf1, d->w13, d->w13_sf, counts, d->E, d->max_m, 2 * d->I, d->H,
+                                            d->expected_m, y1, gflags, d->err, stream)
+                : moe_gemm_fp8_contig_ue8m0(a1, d->H, sf1, p.rows, d->w13, d->w13_sf, offsets, mind, p.rows, d->E,
+                                            2 * d->I, d->H, y1, 2 * d->I, gflags, d->err, stream);
+    if (rc) return rc;
+    if ((rc = mark(3))) return rc;
+    if ((rc = swiglu_launch(y1, p.rows, d->I, masked ? counts : nullptr, masked ? d->max_m : 0,
+                            masked ? nullptr : mind, a2, nullptr, p.s_ld2, true, reinterpret_cast<uint8_t*>(sa2),
+                            st)))
+      return rc;
+    if ((rc = mark(4))) return rc;
+    rc = masked ? moe_gemm_fp8_masked_ue8m0(a2, sf2, d->w2, d->w2_sf, counts, d->E, d->max_m, d->H, d->I,
+                                            d->expected_m, y2, gflags, d->err, stream)
+                : moe_gemm_fp8_contig_ue8m0(a2, d->I, sf2, p.rows, d->w2, d->w2_sf, offsets, mind, p.rows, d->E,
+                                            d->H, d->I, y2, d->H, gflags, d->err, stream);
+    if (rc) return rc;
+    if ((rc = mark(5))) return rc;
+    if ((rc = moe_combine(y2, d->H, p.rows, dst, d->topk_w, d->T, d->k, d->H, nullptr, 0, 0, d->out, d->H, d->err,
+                          stream)))
+      return rc;
+    return mark(6);
+  }
   const bool fuse_swiglu = fusion.swiglu;
   if (fuse_swiglu) {
     if (masked)
@@ -323,7 +369,7 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
     if (rc) return rc;
     if ((rc = mark(3))) return rc;
     if ((rc = moe_swiglu_quant(y1, p.rows, d->I, masked ? counts : nullptr, masked ? d->max_m : 0,
-                               masked ? nullptr : mind, a2, sa2, p.s_ld2, d->err, stream)))
+                               masked ? nullptr : mind, a2, sa2, p.s_ld2, 0, d->err, stream)))
       return rc;
     if ((rc = mark(4))) return rc;
   }

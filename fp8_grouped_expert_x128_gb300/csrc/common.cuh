@@ -68,7 +68,13 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
                    uint8_t* q_out, float* s_out, int64_t s_out_ld, int32_t* counts,
                    int32_t* offsets, int32_t* m_indices, int32_t* row_src, int32_t* dst_row,
                    int64_t rows_capacity, int32_t* err, cudaStream_t st,
-                   uint16_t* zero_out = nullptr, int64_t ldo = 0);
+                   uint16_t* zero_out = nullptr, int64_t ldo = 0, uint8_t* sf8_out = nullptr);
+
+// SwiGLU + 1x128 requantisation (moe_swiglu_quant and moe_ffn): fp32 scales
+// in groups of G rows, or (sf8) exponent bytes in the packed UE8M0 layout.
+int swiglu_launch(const uint16_t* Y1, int64_t rows, int32_t I, const int32_t* counts, int32_t max_m,
+                  const int32_t* m_indices, uint8_t* q, float* s, int64_t s_ld, bool ue8m0, uint8_t* sf8,
+                  cudaStream_t st);
 
 // GEMM1 with SwiGLU + 1x128 requantisation fused into the tokens-as-M
 // epilogue (bytes equal GEMM1 -> moe_swiglu_quant); used inside moe_ffn.
@@ -476,6 +482,33 @@ __host__ __device__ inline float block_scale_ue8m0(float amax, uint8_t* byte) {
   memcpy(&s, &sbits, sizeof(s));
   return s;
 }
+
+// Byte offset of (row r of its scale group grp, k-block kb) in the packed
+// UE8M0 activation scales (moe_fp8.h): groups of G rows, k-groups of four
+// k-blocks, 128-row chunks; row i of a chunk owns word 4 * (i % 32) + i / 32,
+// k-block kb its byte kb % 4.
+__host__ __device__ __forceinline__ int64_t ue8m0_act_byte(int64_t grp, int64_t r, int64_t kb, int64_t KG,
+                                                           int64_t NC) {
+  const int64_t i = r & 127;
+  return ((((grp * KG + (kb >> 2)) * NC + (r >> 7)) << 7) + 4 * (i & 31) + (i >> 5)) * 4 + (kb & 3);
+}
+
+// Where a quantising kernel puts a block scale: the fp32 value in the grouped
+// layout s[((row / G) * KB + kb) * G + row % G], or -- with sf8 given -- the
+// power-of-two scale's exponent byte in the packed UE8M0 layout.
+struct ScaleOut {
+  float* s;
+  uint8_t* sf8;
+  int64_t G;
+  int32_t KG, NC;
+  __device__ __forceinline__ void put(int64_t row, int64_t kb, int64_t KB, float sc, uint8_t byte) const {
+    const int64_t grp = row / G, pos = row - grp * G;
+    if (sf8 != nullptr)
+      sf8[ue8m0_act_byte(grp, pos, kb, KG, NC)] = byte;
+    else
+      s[(grp * KB + kb) * G + pos] = sc;
+  }
+};
 
 // s = max(amax, 1e-4) / 448 rounded to nearest: the same one-step correction
 // of a product by the rounded reciprocal (of the constant 448); non-finite

@@ -24,76 +24,34 @@
 //    registers while the tensor cores fill the other buffer;
 //  * every wait is bounded (see common.cuh): a stalled pipeline flags
 //    MOE_DEV_TIMEOUT and the CTA unwinds, frees its TMEM and returns.
-#include <map>
-#include <mutex>
-#include <utility>
-
-#include "common.cuh"
+#include "gemm_common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 128;
 constexpr int kStages = 4;
-constexpr int kEpiWarps = 8;
-constexpr int kEpiWarp0 = 4;                         // epilogue = warps 4..11 (warpgroups 1, 2)
-constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);  // warps 2-3 only hold warpgroup 0 together
-// Register split between warpgroups (setmaxnreg): warpgroup 0 (TMA + MMA
-// issue) needs few registers, the epilogue holds 128 fp32 accumulators per
-// thread.  The launch allocates kLaunchRegs to all 384 threads; warpgroup 0
-// gives back down to kRegsLow and the two epilogue warpgroups take kRegsHigh:
-// 128 * 40 + 256 * 232 = 64512 = 384 * 168, exactly the launch allocation, so
-// the increase never waits on registers that do not exist.  The host refuses to
-// launch a split kernel whose compiled register count differs from kLaunchRegs.
 constexpr int kScaleAhead = 4;                       // scale prefetch distance (k-blocks)
-constexpr int kLaunchRegs = 168;
-constexpr int kRegsLow = 40;
-constexpr int kRegsHigh = 232;
-static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kLaunchRegs, "register split");
-static_assert(kThreads * kLaunchRegs <= 65536, "register file");
-
-__device__ __forceinline__ void regs_release_low() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+// Output staging of the tokens-as-M epilogue: per epilogue warp, 32 rows x
+// 32 bf16 columns (64 bytes per row), the row's 16-byte chunk c kept in slot
+// c ^ ((row >> 1) & 3): conflict-free both when a lane writes its own row's
+// chunks and when 8 lanes read two rows' four chunks.
+constexpr uint32_t kOutStageBytes = 32 * 64;
+__device__ __forceinline__ uint32_t out_stage_slot(int row, int chunk) {
+  return static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
 }
-__device__ __forceinline__ void regs_acquire_high() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
 }
-
-// Per-device, per-kernel launch set-up done once: the dynamic shared-memory
-// opt-in and, for kernels that split registers, the check that the launch
-// register count equals kLaunchRegs.  Keyed by (device, kernel address).
-template <typename F>
-int prepare_kernel(F kernel, size_t smem, bool split_regs) {
-  static std::mutex mu;
-  static std::map<std::pair<int, const void*>, size_t> prepared;  // -> smem opted in
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  const auto key = std::make_pair(dev, reinterpret_cast<const void*>(kernel));
-  std::lock_guard<std::mutex> lock(mu);
-  auto it = prepared.find(key);
-  if (it == prepared.end()) {
-    if (split_regs) {
-      cudaFuncAttributes attr;
-      if (cudaFuncGetAttributes(&attr, kernel) != cudaSuccess) return MOE_ERR_CUDA;
-      if (attr.numRegs != kLaunchRegs) return MOE_ERR_UNSUPPORTED;
-    }
-    it = prepared.emplace(key, 0).first;
-  }
-  if (smem > it->second) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    it->second = smem;
-  }
-  return MOE_OK;
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
 }
 constexpr uint32_t kATileBytes = BM * BK;
 constexpr uint32_t kBTileBytes = BN * BK;
 constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
-constexpr uint32_t kTmemCols = 512;
-constexpr int kMaxExperts = 1024;
 
 struct GemmArgs {
   const float* sA;
@@ -121,70 +79,6 @@ struct GemmArgs {
   int64_t ldo;
 };
 
-struct Sched {
-  int32_t* tile0;  // [E+1] first tile of each expert
-  int32_t* rbase;  // [E]   first A/D row of each expert
-  int32_t* rext;   // [E]   row extent (masked: kept count; contiguous: segment rows)
-};
-
-struct TileCursor {
-  int e = 0;
-  __device__ __forceinline__ void seek(const Sched& s, int t) {
-    while (t >= s.tile0[e + 1]) ++e;
-  }
-};
-
-// Warp 0 builds the tile schedule: each lane owns a contiguous chunk of experts;
-// an expert's rows are cut into blocks of kRows (128, or 256 for a CTA pair).
-template <int kRows = BM>
-__device__ void build_schedule(const GemmArgs& p, const Sched& s, int n_tiles) {
-  const int lane = threadIdx.x & 31;
-  const int per = (p.E + 31) / 32;
-  const int e0 = min(lane * per, p.E), e1 = min(e0 + per, p.E);
-  int local = 0;
-  bool overflow = false, bad = false;
-  for (int e = e0; e < e1; ++e) {
-    int rb, rx;
-    if (p.layout == MOE_LAYOUT_MASKED) {
-      int c = p.counts[e];
-      if (c > p.max_m) { overflow = true; c = p.max_m; }
-      if (c < 0) { bad = true; c = 0; }
-      rb = e * p.max_m;
-      rx = c;
-    } else {
-      rb = p.offsets[e];
-      rx = p.offsets[e + 1] - rb;
-      // a segment must start on a 128-row boundary and lie inside the
-      // M_capacity rows of A, D and m_indices; otherwise it is skipped
-      if (rb < 0 || (rb % BM) != 0 || rx < 0 || (rx % BM) != 0 ||
-          static_cast<int64_t>(rb) + rx > p.M_capacity) {
-        bad = true;
-        rb = 0;
-        rx = 0;
-      }
-    }
-    s.rbase[e] = rb;
-    s.rext[e] = rx;
-    local += (rx + kRows - 1) / kRows * n_tiles;
-  }
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  int run = incl - local;
-  for (int e = e0; e < e1; ++e) {
-    s.tile0[e] = run;
-    run += (s.rext[e] + kRows - 1) / kRows * n_tiles;
-  }
-  if (lane == 31) s.tile0[p.E] = incl;
-  if (blockIdx.x == 0) {
-    if (overflow) set_err(p.err, MOE_DEV_OVERFLOW);
-    if (bad) set_err(p.err, MOE_DEV_BAD_INDEX);
-  }
-}
-
 // kSwiGLU: the 256-wide B tile is 128 gate rows + the matching 128 up rows
 // (two 128-row TMA boxes), and the epilogue turns the tile into h = silu(g)*u
 // quantised 1x128 (bytes equal GEMM1 -> bf16 -> moe_swiglu_quant), writing
@@ -205,6 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Sched sched{sched_mem, sched_mem + p.E + 1, sched_mem + 2 * p.E + 1};
   // SwiGLU mode: per-row amax of each warpgroup's 64 columns, [tile parity][g][row]
   float* xch = reinterpret_cast<float*>(sched_mem + ((3 * p.E + 1 + 3) & ~3));
+  uint8_t* ostage = reinterpret_cast<uint8_t*>(xch + 2 * 256);   // kEpiWarps x kOutStageBytes
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars);
@@ -461,34 +356,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       if (!kSwiGLU) {
-        if (active && row_ok && p.out != nullptr) {
-          // the row's only routing slot: the combine's bf16(fmaf(w, bf16(y), 0))
-          // written straight to the token's output row
+        // bf16 results (with the single-slot combine: bf16(fmaf(w, bf16(y), 0)),
+        // the combine's arithmetic, written to the token's output row).  The
+        // warp's 32 rows x 128 columns go out through its 2 KB of shared
+        // staging in four 32-column quarters, so each store instruction writes
+        // 8 rows x 64 contiguous bytes instead of 32 rows x 16 bytes.
+        if (active) {
+          const bool to_out = p.out != nullptr;
+          uint16_t* row_base = to_out ? p.out + tok * p.ldo + n0 : p.D + gr * p.ldd + n0;
           const float w = wtok;
-          uint4* dst = reinterpret_cast<uint4*>(p.out + tok * p.ldo + n0);
           auto rb = [](float v) { return __bfloat162float(__float2bfloat16_rn(v)); };
+          const uint32_t stg = smem_u32(ostage + (warp - kEpiWarp0) * kOutStageBytes);
 #pragma unroll
-          for (int v = 0; v < 16; ++v) {
-            uint32_t o[4];
+          for (int qc = 0; qc < 4; ++qc) {
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const __nv_bfloat162 bb = __floats2bfloat162_rn(fmaf(w, rb(acc[v * 4 + h].x), 0.f),
-                                                              fmaf(w, rb(acc[v * 4 + h].y), 0.f));
-              o[h] = *reinterpret_cast<const uint32_t*>(&bb);
+            for (int c = 0; c < 4; ++c) {
+              const int v = qc * 4 + c;       // 16-byte chunk of the row: columns 8v .. 8v+7
+              uint32_t o[4];
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                const float2 a2 = acc[v * 4 + h];
+                const __nv_bfloat162 bb = to_out ? __floats2bfloat162_rn(fmaf(w, rb(a2.x), 0.f), fmaf(w, rb(a2.y), 0.f))
+                                                 : __floats2bfloat162_rn(a2.x, a2.y);
+                o[h] = *reinterpret_cast<const uint32_t*>(&bb);
+              }
+              st_shared_v4(stg + out_stage_slot(lane, c), make_uint4(o[0], o[1], o[2], o[3]));
             }
-            dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
-          }
-        } else if (active && row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(p.D + gr * p.ldd + n0);
+            __syncwarp();
 #pragma unroll
-          for (int v = 0; v < 16; ++v) {
-            uint32_t o[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const __nv_bfloat162 bb = __floats2bfloat162_rn(acc[v * 4 + h].x, acc[v * 4 + h].y);
-              o[h] = *reinterpret_cast<const uint32_t*>(&bb);
+            for (int j = 0; j < 4; ++j) {
+              const int r = 8 * j + (lane >> 2), c = lane & 3;   // row of the warp, chunk of the quarter
+              const uint4 val = ld_shared_v4(stg + out_stage_slot(r, c));
+              const bool ok_r = __shfl_sync(0xffffffffu, row_ok, r);
+              uint16_t* base_r = reinterpret_cast<uint16_t*>(
+                  __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(row_base), r));
+              if (ok_r) *reinterpret_cast<uint4*>(base_r + qc * 32 + c * 8) = val;
             }
-            dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+            __syncwarp();
           }
         }
       } else {
@@ -560,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t tokens_m_smem_bytes(int E) {
   return 1024 + static_cast<size_t>(kStages) * kStageBytes + (2 * kStages + 8) * 8 + 16 +
-         sizeof(int32_t) * (3 * E + 1 + 3) + sizeof(float) * 2 * 256;
+         sizeof(int32_t) * (3 * E + 1 + 3) + sizeof(float) * 2 * 256 + kEpiWarps * kOutStageBytes;
 }
 
 int launch_tokens_m(const uint8_t* A, int64_t a_rows, int64_t lda, const uint8_t* B,
@@ -969,12 +873,6 @@ __device__ void build_schedule_wm(const GemmArgs& p, const Sched& s, int nblk) {
   }
 }
 
-// Token-side tensor maps: the same [E*max_m, K] matrix with boxes of 16 << i
-// rows (a map whose box would exceed the matrix repeats the 16-row map; the
-// kernel never picks a box taller than the tile's rows).
-struct TokenMaps {
-  CUtensorMap box[4];
-};
 
 template <int BNT>
 __global__ void __launch_bounds__(kThreads, 1)

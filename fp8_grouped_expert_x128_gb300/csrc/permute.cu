@@ -244,11 +244,13 @@ __global__ void __launch_bounds__(128) permute_scatter_kernel(
 // many tokens (prefill) take 4-warp CTAs, 7 block pairs per warp, ~6 CTAs per
 // SM for the bytes in flight; a few hundred tokens (decode) take 8-warp CTAs,
 // 4 pairs per warp, so each row finishes sooner.
-template <int kQsWarps, int kQsPairs>
+// kUE8M0: power-of-two block scales, their exponent bytes written to the
+// packed layout of the block-scaled GEMM (ScaleOut with sf8).
+template <int kQsWarps, int kQsPairs, bool kUE8M0>
 __global__ void __launch_bounds__(32 * kQsWarps, kQsWarps == 4 ? 6 : 4) quant_scatter_kernel(
     const uint16_t* __restrict__ x, int64_t ldx, const int32_t* __restrict__ dst_row,
-    int64_t T, int32_t k, int64_t H, uint8_t* __restrict__ q_out, float* __restrict__ s_out,
-    int64_t G, uint16_t* __restrict__ zero_out, int64_t ldo) {
+    int64_t T, int32_t k, int64_t H, uint8_t* __restrict__ q_out, const ScaleOut so,
+    uint16_t* __restrict__ zero_out, int64_t ldo) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t KB = H / 128, NP = (KB + 1) / 2;
   bool waited = false;
@@ -271,6 +273,7 @@ __global__ void __launch_bounds__(32 * kQsWarps, kQsWarps == 4 ? 6 : 4) quant_sc
       }
       uint2 code[kQsPairs];
       float sc[kQsPairs];
+      uint8_t e8b[kQsPairs];
 #pragma unroll
       for (int j = 0; j < kQsPairs; ++j) {
         float f[8];
@@ -279,7 +282,8 @@ __global__ void __launch_bounds__(32 * kQsWarps, kQsWarps == 4 ? 6 : 4) quant_sc
 #pragma unroll
         for (int v = 0; v < 8; ++v) amax = fmaxf(amax, fabsf(f[v]));
         amax = half_warp_max(amax);
-        sc[j] = block_scale(amax);
+        e8b[j] = 0;
+        sc[j] = kUE8M0 ? block_scale_ue8m0(amax, &e8b[j]) : block_scale(amax);
         code[j] = quant8(f, sc[j]);
       }
       wait_index();
@@ -288,14 +292,13 @@ __global__ void __launch_bounds__(32 * kQsWarps, kQsWarps == 4 ? 6 : 4) quant_sc
       for (int j2 = 0; j2 < k; ++j2) {
         const int32_t dst = __shfl_sync(0xffffffffu, dl, j2);
         if (dst < 0) continue;
-        const int64_t grp = dst / G, pos = dst - grp * G;
         uint8_t* qr = q_out + static_cast<int64_t>(dst) * H;
 #pragma unroll
         for (int j = 0; j < kQsPairs; ++j) {
           const int64_t kb = (p0 + j * kQsWarps) * 2 + (lane >> 4);
           if (kb < KB) {
             *reinterpret_cast<uint2*>(qr + kb * 128 + (lane & 15) * 8) = code[j];
-            if ((lane & 15) == 0) s_out[(grp * KB + kb) * G + pos] = sc[j];
+            if ((lane & 15) == 0) so.put(dst, kb, KB, sc[j], e8b[j]);
           }
         }
       }
@@ -562,12 +565,12 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
                    uint8_t* q_out, float* s_out, int64_t s_out_ld, int32_t* counts,
                    int32_t* offsets, int32_t* m_indices, int32_t* row_src, int32_t* dst_row,
                    int64_t rows_capacity, int32_t* err, cudaStream_t st, uint16_t* zero_out,
-                   int64_t ldo) {
+                   int64_t ldo, uint8_t* sf8_out) {
   MOE_CHECK_ARG(T >= 0 && H > 0 && H % 128 == 0 && k >= 1 && k <= 32);
   MOE_CHECK_ARG(E >= 1 && E <= kMaxExperts);
   MOE_CHECK_ARG(layout == MOE_LAYOUT_MASKED || layout == MOE_LAYOUT_CONTIG);
-  MOE_CHECK_ARG(counts && row_src && q_out && s_out);
-  MOE_CHECK_ARG(aligned16(q_out) && aligned16(s_out));
+  MOE_CHECK_ARG(counts && row_src && q_out && (s_out || sf8_out));
+  MOE_CHECK_ARG(aligned16(q_out) && aligned16(s_out) && aligned16(sf8_out));
   int64_t G;
   if (layout == MOE_LAYOUT_MASKED) {
     MOE_CHECK_ARG(max_m > 0 && static_cast<int64_t>(E) * max_m < (1ll << 31));
@@ -605,17 +608,20 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
   if (x != nullptr) {
     // many rows: throughput shape; decode batches: latency shape
     const bool many = T >= 16384;
-    auto kern = many ? quant_scatter_kernel<4, 7> : quant_scatter_kernel<8, 4>;
+    const bool packed = sf8_out != nullptr;
+    auto kern = packed ? (many ? quant_scatter_kernel<4, 7, true> : quant_scatter_kernel<8, 4, true>)
+                       : (many ? quant_scatter_kernel<4, 7, false> : quant_scatter_kernel<8, 4, false>);
+    const ScaleOut so{s_out, sf8_out, G, static_cast<int32_t>((H / 128 + 3) / 4), static_cast<int32_t>((G + 127) / 128)};
     const int threads = many ? 128 : 256;
-    static int per_sm[2][64] = {{0}};
+    static int per_sm[4][64] = {{0}};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-    int& occ = per_sm[many ? 1 : 0][dev];
+    int& occ = per_sm[(many ? 1 : 0) + (packed ? 2 : 0)][dev];
     if (occ == 0 && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, 0) != cudaSuccess || occ < 1))
       return MOE_ERR_CUDA;
     const int64_t wave = static_cast<int64_t>(num_sms()) * occ;
     return launch_pdl(kern, static_cast<unsigned>(T < wave ? T : wave), threads, 0, st, x, ldx, dst_row, T, k,
-                      static_cast<int64_t>(H), q_out, s_out, G, k == 1 ? zero_out : nullptr, ldo);
+                      static_cast<int64_t>(H), q_out, so, k == 1 ? zero_out : nullptr, ldo);
   }
   return launch_pdl(permute_scatter_kernel, grid, 128, 0, st, q, s, s_ld, dst_row, n, k, H, q_out,
                     s_out, G);
@@ -631,7 +637,7 @@ extern "C" int moe_permute(const uint8_t* q, const float* s, int64_t s_ld, const
                            int64_t rows_capacity, int32_t* err, void* stream) {
   return permute_launch(q, s, s_ld, nullptr, 0, topk_ids, T, H, k, expert_begin, E, layout, max_m,
                         q_out, s_out, s_out_ld, counts, offsets, m_indices, row_src, dst_row,
-                        rows_capacity, err, as_stream(stream));
+                        rows_capacity, err, as_stream(stream), nullptr, 0, nullptr);
 }
 
 extern "C" int moe_combine(const uint16_t* Y2, int64_t ldy, int64_t y_rows, const int32_t* dst_row,

@@ -56,11 +56,14 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __rest
 
 // ---------------------------------------------------------------- a3
 // One CTA of 256 threads per 128x128 tile; thread t covers columns
-// (t % 16) * 8 .. +7 of rows t/16 + 16 i, i = 0..7.
+// (t % 16) * 8 .. +7 of rows t/16 + 16 i, i = 0..7.  kUE8M0: power-of-two
+// tile scales (block_scale_ue8m0), their exponent bytes also stored to e8.
+template <bool kUE8M0>
 __global__ void __launch_bounds__(256) quant_128x128_kernel(const uint16_t* __restrict__ w,
                                                             int64_t N, int64_t K,
                                                             uint8_t* __restrict__ q,
-                                                            float* __restrict__ s) {
+                                                            float* __restrict__ s,
+                                                            uint8_t* __restrict__ e8) {
   grid_dependency_wait();
   grid_launch_dependents();
   const int64_t NB = N / 128, KB = K / 128;
@@ -88,20 +91,26 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const uint16_t* __re
   amax = red[0];
 #pragma unroll
   for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
-  const float sc = block_scale(amax);
+  uint8_t byte = 0;
+  const float sc = kUE8M0 ? block_scale_ue8m0(amax, &byte) : block_scale(amax);
   uint8_t* qb = q + (e * N + nb * 128) * K + kb * 128 + c8 * 8;
 #pragma unroll
   for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(qb + (r0 + 16 * i) * K) = quant8(f[i], sc);
-  if (t == 0) s[(e * NB + nb) * KB + kb] = sc;
+  if (t == 0) {
+    s[(e * NB + nb) * KB + kb] = sc;
+    if (kUE8M0 && e8 != nullptr) e8[(e * NB + nb) * KB + kb] = byte;
+  }
 }
 
 // ---------------------------------------------------------------- a5
-// h = silu(g) * u in fp32, quantised by the a1 rule.  A warp covers blocks
-// 4w + h and 4w + h + 2 of one row (w = `part`, h = its half-warp), with all
-// four 16-byte loads (g and u of both blocks) issued before any use.
+// h = silu(g) * u in fp32, quantised by the a1 rule (kUE8M0: with power-of-two
+// scales).  A warp covers blocks 4w + h and 4w + h + 2 of one row (w = `part`,
+// h = its half-warp), with all four 16-byte loads (g and u of both blocks)
+// issued before any use.
+template <bool kUE8M0>
 __device__ __forceinline__ void swiglu_row_part(const uint16_t* __restrict__ y1, int64_t I, int64_t KB,
                                                 int64_t r, int64_t part, int lane, uint8_t* __restrict__ q,
-                                                float* __restrict__ s, int64_t G) {
+                                                const ScaleOut& so) {
   const int64_t kb0 = part * 4 + (lane >> 4);
   const uint16_t* row = y1 + r * 2 * I;
   uint4 gv[2], uv[2];
@@ -130,21 +139,20 @@ __device__ __forceinline__ void swiglu_row_part(const uint16_t* __restrict__ y1,
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(h[i]));
     amax = half_warp_max(amax);
     if (active) {
-      const float sc = block_scale(amax);
+      uint8_t byte = 0;
+      const float sc = kUE8M0 ? block_scale_ue8m0(amax, &byte) : block_scale(amax);
       *reinterpret_cast<uint2*>(q + r * I + col) = quant8(h, sc);
-      if ((lane & 15) == 0) {
-        const int64_t grp = r / G, pos = r - grp * G;
-        s[(grp * KB + kb) * G + pos] = sc;
-      }
+      if ((lane & 15) == 0) so.put(r, kb, KB, sc, byte);
     }
   }
 }
 
 // Contiguous layout (rows selected by m_indices, or all rows): one warp per
 // (row, part), the grid covering every row.
+template <bool kUE8M0>
 __global__ void __launch_bounds__(256) swiglu_quant_kernel(
     const uint16_t* __restrict__ y1, int64_t rows, int64_t I, const int32_t* __restrict__ m_indices,
-    uint8_t* __restrict__ q, float* __restrict__ s, int64_t G) {
+    uint8_t* __restrict__ q, const ScaleOut so) {
   grid_dependency_wait();
   grid_launch_dependents();
   const int64_t KB = I / 128;
@@ -153,7 +161,7 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(
   const int64_t r = gw / warps_per_row;
   if (r >= rows) return;
   if (m_indices != nullptr && __ldg(m_indices + r) < 0) return;
-  swiglu_row_part(y1, I, KB, r, gw % warps_per_row, threadIdx.x & 31, q, s, G);
+  swiglu_row_part<kUE8M0>(y1, I, KB, r, gw % warps_per_row, threadIdx.x & 31, q, so);
 }
 
 // Masked layout: only the rows below each expert's count hold tokens (a few
@@ -163,9 +171,10 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(
 // search over the prefix.
 constexpr int kSwMaxExperts = 1024;
 
+template <bool kUE8M0>
 __global__ void __launch_bounds__(256) swiglu_quant_masked_kernel(
     const uint16_t* __restrict__ y1, int64_t I, const int32_t* __restrict__ counts, int32_t E,
-    int64_t max_m, uint8_t* __restrict__ q, float* __restrict__ s) {
+    int64_t max_m, uint8_t* __restrict__ q, const ScaleOut so) {
   __shared__ int32_t pre[kSwMaxExperts + 1];   // pre[e] = valid rows of the experts before e
   grid_dependency_wait();
   grid_launch_dependents();
@@ -201,7 +210,7 @@ __global__ void __launch_bounds__(256) swiglu_quant_masked_kernel(
       else hi = mid - 1;
     }
     const int64_t r = static_cast<int64_t>(lo) * max_m + (vr - pre[lo]);
-    swiglu_row_part(y1, I, KB, r, task % warps_per_row, lane, q, s, max_m);
+    swiglu_row_part<kUE8M0>(y1, I, KB, r, task % warps_per_row, lane, q, so);
   }
 }
 
@@ -259,17 +268,34 @@ extern "C" int moe_quant_weight_fp8(const uint16_t* w, int64_t E, int64_t N, int
   if (int st = check_device()) return st;
   const int64_t tiles = E * (N / 128) * (K / 128);
   MOE_CHECK_ARG(tiles < (1ll << 31));
-  return launch_pdl(quant_128x128_kernel, static_cast<unsigned>(tiles), 256, 0, as_stream(stream), w,
-                    N, K, q, s);
+  return launch_pdl(quant_128x128_kernel<false>, static_cast<unsigned>(tiles), 256, 0, as_stream(stream), w,
+                    N, K, q, s, static_cast<uint8_t*>(nullptr));
 }
 
-extern "C" int moe_swiglu_quant(const uint16_t* Y1, int64_t rows, int32_t I, const int32_t* counts,
-                                int32_t max_m, const int32_t* m_indices, uint8_t* q, float* s,
-                                int64_t s_ld, int32_t* err, void* stream) {
-  (void)err;
+extern "C" int moe_quant_weight_fp8_ue8m0(const uint16_t* w, int64_t E, int64_t N, int64_t K, uint8_t* q,
+                                          float* s, uint8_t* e8, void* stream) {
+  MOE_CHECK_ARG(E >= 0 && N > 0 && K > 0 && N % 128 == 0 && K % 128 == 0);
+  if (E == 0) return MOE_OK;
+  MOE_CHECK_ARG(w && q && s && aligned16(w) && aligned16(q));
+  MOE_CHECK_ARG((reinterpret_cast<uintptr_t>(s) & 3u) == 0);
+  if (int st = check_device()) return st;
+  const int64_t tiles = E * (N / 128) * (K / 128);
+  MOE_CHECK_ARG(tiles < (1ll << 31));
+  return launch_pdl(quant_128x128_kernel<true>, static_cast<unsigned>(tiles), 256, 0, as_stream(stream), w,
+                    N, K, q, s, e8);
+}
+
+namespace moe {
+
+// Shared by moe_swiglu_quant and moe_ffn: the scales go to s (fp32, groups of
+// G rows) or, with sf8, as exponent bytes into the packed UE8M0 layout.
+int swiglu_launch(const uint16_t* Y1, int64_t rows, int32_t I, const int32_t* counts, int32_t max_m,
+                  const int32_t* m_indices, uint8_t* q, float* s, int64_t s_ld, bool ue8m0, uint8_t* sf8,
+                  cudaStream_t st) {
   MOE_CHECK_ARG(rows >= 0 && I > 0 && I % 128 == 0);
   if (rows == 0) return MOE_OK;
-  MOE_CHECK_ARG(Y1 && q && s && aligned16(Y1) && aligned16(q) && aligned16(s));
+  MOE_CHECK_ARG(Y1 && q && (s || sf8) && aligned16(Y1) && aligned16(q) && aligned16(s) && aligned16(sf8));
+  MOE_CHECK_ARG(!sf8 || ue8m0);
   int64_t G;
   if (counts != nullptr) {
     MOE_CHECK_ARG(max_m > 0 && rows % max_m == 0);
@@ -278,7 +304,8 @@ extern "C" int moe_swiglu_quant(const uint16_t* Y1, int64_t rows, int32_t I, con
     MOE_CHECK_ARG(s_ld >= rows);
     G = s_ld;
   }
-  if (int st = check_device()) return st;
+  if (int rc = check_device()) return rc;
+  const ScaleOut so{s, sf8, G, static_cast<int32_t>((I / 128 + 3) / 4), static_cast<int32_t>((G + 127) / 128)};
   const int64_t warps = rows * ((I / 128 + 3) / 4);
   if (counts != nullptr) {
     const int64_t E = rows / max_m;
@@ -287,10 +314,21 @@ extern "C" int moe_swiglu_quant(const uint16_t* Y1, int64_t rows, int32_t I, con
     // even a full layout has fewer warp tasks
     const int64_t wave = static_cast<int64_t>(num_sms()) * 8;
     const int64_t need = grid_for_warps(warps);
-    return launch_pdl(swiglu_quant_masked_kernel, static_cast<unsigned>(need < wave ? need : wave), 256, 0,
-                      as_stream(stream), Y1, static_cast<int64_t>(I), counts, static_cast<int32_t>(E),
-                      static_cast<int64_t>(max_m), q, s);
+    auto kern = ue8m0 ? swiglu_quant_masked_kernel<true> : swiglu_quant_masked_kernel<false>;
+    return launch_pdl(kern, static_cast<unsigned>(need < wave ? need : wave), 256, 0, st, Y1,
+                      static_cast<int64_t>(I), counts, static_cast<int32_t>(E), static_cast<int64_t>(max_m), q, so);
   }
-  return launch_pdl(swiglu_quant_kernel, grid_for_warps(warps), 256, 0, as_stream(stream), Y1, rows,
-                    static_cast<int64_t>(I), m_indices, q, s, G);
+  auto kern = ue8m0 ? swiglu_quant_kernel<true> : swiglu_quant_kernel<false>;
+  return launch_pdl(kern, grid_for_warps(warps), 256, 0, st, Y1, rows, static_cast<int64_t>(I), m_indices, q, so);
+}
+
+}  // namespace moe
+
+extern "C" int moe_swiglu_quant(const uint16_t* Y1, int64_t rows, int32_t I, const int32_t* counts,
+                                int32_t max_m, const int32_t* m_indices, uint8_t* q, float* s,
+                                int64_t s_ld, int32_t flags, int32_t* err, void* stream) {
+  (void)err;
+  MOE_CHECK_ARG((flags & ~MOE_QUANT_UE8M0) == 0 && s != nullptr);
+  return swiglu_launch(Y1, rows, I, counts, max_m, m_indices, q, s, s_ld, (flags & MOE_QUANT_UE8M0) != 0, nullptr,
+                       as_stream(stream));
 }

@@ -79,6 +79,11 @@ extern "C" {
 #define MOE_GEMM_CTA_PAIR 0x8         /* tokens-as-M: run each 256x256 tile on a 2-CTA
                                          cluster (one M = 256 UMMA, each SM stages half
                                          of B); needs N % 256 == 0, else ignored        */
+#define MOE_FFN_UE8M0 0x10            /* moe_ffn only: the power-of-two (UE8M0) reading of
+                                         the packed scales end to end -- both activation
+                                         quantisations take power-of-two scales, packed for
+                                         the block-scaled GEMMs, which read the weights'
+                                         packed scales w13_sf / w2_sf                     */
 #define MOE_GEMM_DEBUG_STALL 0x100    /* test only: the TMA producer never issues, so the
                                          consumer's bounded wait expires and the call
                                          reports MOE_DEV_TIMEOUT (no hang, no trap)      */
@@ -151,6 +156,14 @@ float moe_ue8m0_scale(float amax, uint8_t *byte_out);
  */
 int moe_quant_weight_fp8(const uint16_t *w, int64_t E, int64_t N, int64_t K,
                          uint8_t *q, float *s, void *stream);
+
+/*
+ * a3 with power-of-two (UE8M0) tile scales: the rule of moe_quant_fp8_ue8m0
+ * with amax over each 128x128 tile.  q, s as moe_quant_weight_fp8 (s holds
+ * 2^e); e8 (device uint8 [E, N/128, K/128], may be NULL) holds e + 127.
+ */
+int moe_quant_weight_fp8_ue8m0(const uint16_t *w, int64_t E, int64_t N, int64_t K,
+                               uint8_t *q, float *s, uint8_t *e8, void *stream);
 
 /*
  * Rows a contiguous-layout buffer must be able to hold for `assignments`
@@ -231,6 +244,58 @@ int moe_gemm_fp8_masked(const uint8_t *A, const float *sA, const uint8_t *B, con
                         void *stream);
 
 /*
+ * a4 / a6 with power-of-two (UE8M0) block scales applied by the tensor cores
+ * -- the reading of the DeepGEMM bullet ("Deploying DeepSeek on GB200 NVL72
+ * with PD and Large Scale EP (Part I)", Implementation details: an FP8 GEMM on
+ * UMMA whose API quantises and packs the input scales) in which the packed
+ * scales are exponent bytes, four k-blocks per 32-bit word, that the MMA
+ * consumes (tcgen05.mma kind::mxf8f6f4.block_scale).  The product is the same
+ * definition as moe_gemm_fp8_*:
+ *   D[r, n] = bf16_rne( sum_kb  sA[r, kb] * sB[e, n/128, kb] * sum_{k in kb} A[r, k] * B[e, n, k] )
+ * with sA = 2^(a - 127), sB = 2^(b - 127) read from the packed words; the
+ * accumulation is fp32 across all k-blocks in TMEM.
+ *
+ * Packed activation scales (sfA, uint32 words, 16-byte aligned): rows are in
+ * groups of G (masked layout: G = max_m, one group per expert; contiguous:
+ * one group of G = sfA_ld rows, sfA_ld a multiple of 128 >= M_capacity);
+ * within a group, chunks of 128 rows.  For group grp, k-group g (k-blocks
+ * 4g .. 4g+3), chunk c and row i of the chunk:
+ *   word index = ((grp * KG + g) * NC + c) * 128 + 4 * (i % 32) + i / 32,
+ *   KG = ceil(K / 512), NC = ceil(G / 128);
+ * byte b of the word is the exponent byte (e + 127) of k-block 4g + b (0x7F
+ * past the last k-block).  This order puts every row's word where the tensor
+ * cores read it after one 512-byte copy into tensor memory.
+ * Packed weight scales (sfB, 16-byte aligned): for expert e, 128-row block nb
+ * and k-group g, 32 copies of the word whose byte b is the exponent byte of
+ * block (nb, 4g + b): word index ((e * (N/128) + nb) * KG + g) * 32 + j.
+ *
+ * moe_ue8m0_act_words / moe_ue8m0_weight_words: sizes of the two arrays in
+ * words (-1 for bad sizes).  moe_pack_ue8m0_act: power-of-two fp32 scales in
+ * the grouped layout of the fp32 scales (s[((r / G) * KB + kb) * G + r % G],
+ * as moe_quant_fp8 with MOE_QUANT_UE8M0 and moe_permute write them; only the
+ * exponent field is read) -> sfA, for `groups` groups of G rows of which the
+ * first `rows` exist (the rest pack as scale 1).  moe_pack_ue8m0_weight:
+ * power-of-two fp32 weight scales [E, N/128, K/128] (moe_quant_weight_fp8_ue8m0)
+ * -> sfB.
+ * The GEMMs take the arguments of moe_gemm_fp8_contig / moe_gemm_fp8_masked
+ * with the packed arrays in place of the fp32 scales (sfA_ld as above).
+ */
+int64_t moe_ue8m0_act_words(int64_t groups, int64_t G, int64_t K);
+int64_t moe_ue8m0_weight_words(int64_t E, int64_t N, int64_t K);
+int moe_pack_ue8m0_act(const float *s, int64_t groups, int64_t G, int64_t rows, int64_t K,
+                       uint32_t *sfA, void *stream);
+int moe_pack_ue8m0_weight(const float *s, int64_t E, int64_t N, int64_t K, uint32_t *sfB, void *stream);
+int moe_gemm_fp8_contig_ue8m0(const uint8_t *A, int64_t lda, const uint32_t *sfA, int64_t sfA_ld,
+                              const uint8_t *B, const uint32_t *sfB,
+                              const int32_t *offsets, const int32_t *m_indices, int64_t M_capacity,
+                              int32_t E, int32_t N, int32_t K,
+                              uint16_t *D, int64_t ldd, int32_t flags, int32_t *err, void *stream);
+int moe_gemm_fp8_masked_ue8m0(const uint8_t *A, const uint32_t *sfA, const uint8_t *B, const uint32_t *sfB,
+                              const int32_t *counts, int32_t E, int32_t max_m, int32_t N, int32_t K,
+                              int32_t expected_m, uint16_t *D, int32_t flags, int32_t *err,
+                              void *stream);
+
+/*
  * Which masked-GEMM kernel moe_gemm_fp8_masked runs for these arguments
  * (host-side, nothing launched): 0 = tokens-as-M (128 token rows x 256 weight
  * rows per tile); 64 / 128 / 256 = weights-as-M with token tiles of that many
@@ -253,10 +318,12 @@ int moe_gemm_fp8_masked_variant(int32_t max_m, int32_t expected_m, int32_t flags
  *   contig -> counts == NULL, m_indices != NULL,
  *   G = s_ld, row r processed iff r < rows and m_indices[r] >= 0.
  * Unprocessed rows of q and s are left untouched.
+ * flags: 0, or MOE_QUANT_UE8M0 for power-of-two scales (the rule of
+ * moe_quant_fp8_ue8m0; s then holds 2^e).  Unknown bits are refused.
  */
 int moe_swiglu_quant(const uint16_t *Y1, int64_t rows, int32_t I,
                      const int32_t *counts, int32_t max_m, const int32_t *m_indices,
-                     uint8_t *q, float *s, int64_t s_ld, int32_t *err, void *stream);
+                     uint8_t *q, float *s, int64_t s_ld, int32_t flags, int32_t *err, void *stream);
 
 /*
  * a7 -- top-k-weighted combine back to token order (moe_combine).
@@ -301,6 +368,11 @@ int moe_combine(const uint16_t *Y2, int64_t ldy, int64_t y_rows,
  * separate calls), so events 0 and 1 are recorded back to back; with
  * MOE_FFN_FUSE_SWIGLU in gemm_flags and the tokens-as-M kernel serving GEMM1,
  * stages 3 and 4 are fused the same way (events 3 and 4 back to back).
+ * With MOE_FFN_UE8M0 in gemm_flags the chain takes the power-of-two reading of
+ * the scales: x and h are quantised with the rule of moe_quant_fp8_ue8m0 and
+ * their scales written in the packed layout, both GEMMs run block-scaled
+ * (moe_gemm_fp8_*_ue8m0) with the weights' packed scales w13_sf and w2_sf
+ * (w13_s / w2_s are then not read), and MOE_FFN_FUSE_SWIGLU is ignored.
  */
 typedef struct moe_ffn_desc {
   int64_t T;              /* tokens (rows of x and out)                 */
@@ -321,6 +393,8 @@ typedef struct moe_ffn_desc {
   uint16_t *out;          /* [T, H] bf16                                */
   int32_t *err;           /* device error word (may be NULL)            */
   void **stage_events;    /* optional 7 cudaEvent_t                     */
+  const uint32_t *w13_sf; /* MOE_FFN_UE8M0: packed W13 scales (moe_pack_ue8m0_weight) */
+  const uint32_t *w2_sf;  /* MOE_FFN_UE8M0: packed W2 scales                           */
 } moe_ffn_desc;
 
 /* Number of kernels one moe_ffn call with this descriptor launches (the same

@@ -32,12 +32,12 @@ from .fp8 import (bf16_decode, bf16_encode, e4m3_decode, e4m3_encode,
 from .ffn import (quant_1x128, quant_1x128_ue8m0, quant_128x128, quant_128x128_ue8m0, permute,
                   gemm_block_scaled,
                   gemm_masked, gemm_contig, swiglu, swiglu_quant, combine,
-                  ffn_chain, SCALE_FLOOR)
+                  ffn_chain, SCALE_FLOOR, pack_ue8m0_act, pack_ue8m0_weight)
 
 __all__ = [
     "bf16_decode", "bf16_encode", "e4m3_decode", "e4m3_encode", "e4m3_encode_bruteforce",
     "E4M3_MAX", "quant_1x128", "quant_1x128_ue8m0", "quant_128x128", "quant_128x128_ue8m0", "permute",
     "gemm_block_scaled",
     "gemm_masked", "gemm_contig", "swiglu", "swiglu_quant", "combine", "ffn_chain",
-    "SCALE_FLOOR",
+    "SCALE_FLOOR", "pack_ue8m0_act", "pack_ue8m0_weight",
 ]

@@ -345,3 +345,57 @@ def ffn_chain(x_bits, topk_ids, topk_w, expert_begin, E, layout, max_m,
         y2f, _ = gemm_contig(q2, s2, w2_q, w2_s, p["offsets"], p["m_indices"])
     out = combine(y2f, p["dst_row"], topk_w)
     return dict(q=q, s=s, perm=p, y1=y1f, valid=vflat, q2=q2, s2=s2m, y2=y2f, out=out)
+
+
+# ----------------------------------------------------------------------------
+# The packed UE8M0 scale layouts of the block-scaled GEMM (the reading of the
+# DeepGEMM bullet's "packing of the input scales" in which four exponent bytes
+# share a 32-bit word).  Pure layout: no arithmetic on the scales.
+# ----------------------------------------------------------------------------
+def _ue8m0_bytes(s) -> np.ndarray:
+    """Exponent bytes of power-of-two float32 scales (e + 127 for 2^e; 0xFF for inf)."""
+    return ((np.asarray(s, dtype=np.float32).view(np.uint32) >> 23) & 0xFF).astype(np.uint8)
+
+
+def pack_ue8m0_act(s, G: int, rows: int) -> np.ndarray:
+    """Power-of-two activation scales in the grouped layout s[(grp*KB + kb)*G + r]
+    (flattened; groups of G rows, the first ``rows`` rows existing) -> packed words.
+
+    Group grp, k-group g (k-blocks 4g..4g+3), 128-row chunk c, row i of the
+    chunk: word ((grp*KG + g)*NC + c)*128 + 4*(i % 32) + i // 32, whose byte b
+    is the exponent byte of k-block 4g + b (0x7F where there is no such row or
+    k-block).  KG = ceil(KB/4), NC = ceil(G/128).  Returns uint32 [words]."""
+    s = np.asarray(s, dtype=np.float32).reshape(-1)
+    groups = -(-rows // G) if rows else 0
+    KB = s.size // (groups * G) if groups else 0
+    KG, NC = -(-KB // 4), -(-G // 128)
+    byte = np.full((groups, KG * 4, NC * 128), 0x7F, np.uint8)       # [grp, kb, row of group]
+    b = _ue8m0_bytes(s).reshape(groups, KB, G)
+    for grp in range(groups):
+        n = min(G, rows - grp * G)
+        byte[grp, :KB, :n] = b[grp, :, :n]
+    words = np.zeros((groups, KG, NC, 128), np.uint32)
+    i = np.arange(128)
+    pos = 4 * (i % 32) + i // 32
+    for grp in range(groups):
+        for g in range(KG):
+            for c in range(NC):
+                w = np.zeros(128, np.uint32)
+                for bb in range(4):
+                    w |= byte[grp, 4 * g + bb, c * 128:(c + 1) * 128].astype(np.uint32) << np.uint32(8 * bb)
+                words[grp, g, c, pos] = w
+    return words.reshape(-1)
+
+
+def pack_ue8m0_weight(s) -> np.ndarray:
+    """Power-of-two weight scales [E, NB, KB] -> 32 copies per (e, nb, g) of the
+    word whose byte b is the exponent byte of k-block 4g + b (0x7F past KB).
+    Returns uint32 [E*NB*KG*32]."""
+    b = _ue8m0_bytes(s)
+    E, NB, KB = b.shape
+    KG = -(-KB // 4)
+    full = np.full((E, NB, KG * 4), 0x7F, np.uint8)
+    full[:, :, :KB] = b
+    quad = full.reshape(E, NB, KG, 4).astype(np.uint32)
+    w = quad[..., 0] | (quad[..., 1] << 8) | (quad[..., 2] << 16) | (quad[..., 3] << 24)
+    return np.repeat(w[..., None], 32, axis=3).reshape(-1)

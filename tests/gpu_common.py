@@ -99,6 +99,11 @@ def check_tol(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = ""):
 # the largest effect one such flip per routed row can have (computed by the
 # oracle alone, see flip_bound).
 CHAIN_FRAC = 1e-3
+# With power-of-two (UE8M0) scales a block's scale is up to twice the fp32
+# scale, so one E4M3 flip of h moves an output up to twice as far and up to
+# twice as many outputs leave the strict bound; the one-flip bound itself is
+# unchanged (computed from the oracle's own q2 and s2).
+CHAIN_FRAC_UE8M0 = 2e-3
 
 
 def e4m3_flip_step(q2: np.ndarray, s2_cols: np.ndarray) -> np.ndarray:
@@ -154,7 +159,8 @@ def flip_bound(ref: dict, topk_w: np.ndarray, w2q, w2s) -> np.ndarray:
     return out
 
 
-def check_tol_chain(got_bits: np.ndarray, ref_bits: np.ndarray, extra: np.ndarray, what: str = ""):
+def check_tol_chain(got_bits: np.ndarray, ref_bits: np.ndarray, extra: np.ndarray, what: str = "",
+                    max_frac: float = CHAIN_FRAC):
     got = oracle.bf16_decode(got_bits)
     ref = oracle.bf16_decode(ref_bits)
     assert np.isfinite(got).all(), f"{what}: non-finite GPU output"
@@ -168,7 +174,7 @@ def check_tol_chain(got_bits: np.ndarray, ref_bits: np.ndarray, extra: np.ndarra
         i = np.unravel_index(np.argmax(err - strict_b - extra), err.shape)
         raise AssertionError(f"{what}: {beyond.sum()} outputs beyond the one-flip bound; worst at {i}: "
                              f"gpu {got[i]!r} ref {ref[i]!r} strict {strict_b[i]!r} flip {extra[i]!r}")
-    assert frac <= CHAIN_FRAC, f"{what}: {frac:.2e} of outputs outside the strict bound"
+    assert frac <= max_frac, f"{what}: {frac:.2e} of outputs outside the strict bound"
     return frac
 
 

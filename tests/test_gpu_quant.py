@@ -252,3 +252,21 @@ def test_quant_flag_selects_power_of_two_scales(lib):
     torch.cuda.synchronize()
     rq, rs, _ = oracle.quant_1x128_ue8m0(oracle.bf16_decode(xb).astype(np.float32))
     assert np.array_equal(u8(q), rq) and np.array_equal(s.cpu().numpy(), rs)
+
+
+def test_weight_quant_ue8m0_bitexact(lib):
+    # power-of-two tile scales: codes, scales and exponent bytes equal the
+    # oracle's for every expert of the tiny config and one full-size W2 expert
+    for name, which, experts in (("c1", "w13", range(4)), ("c1", "w2", range(4)), ("c2", "w2", (1,))):
+        cfg = synth.get_config(name)
+        for e in experts:
+            wb = synth.make_expert_weights(cfg, which, e, device="cuda")
+            N, K = wb.shape
+            q = torch.full((1, N, K), SENTINEL_U8, dtype=torch.uint8, device="cuda")
+            s = torch.full((1, N // 128, K // 128), SENTINEL_F32, dtype=torch.float32, device="cuda")
+            e8 = torch.full((1, N // 128, K // 128), 0xA5, dtype=torch.uint8, device="cuda")
+            lib.moe_quant_weight_fp8_ue8m0(wb[None], q, s, e8)
+            torch.cuda.synchronize()
+            rq, rs, rb = oracle.quant_128x128_ue8m0(oracle.bf16_decode(bits(wb)).astype(np.float32))
+            assert np.array_equal(u8(q)[0], rq), (name, which, e)
+            assert np.array_equal(s.cpu().numpy()[0], rs) and np.array_equal(e8.cpu().numpy()[0], rb)

@@ -459,3 +459,64 @@ def test_combine_shared_row_and_accumulate():
                     acc += float(w[t, j]) * yd[dst[t, j], h]
             acc += sd[t, h]
             assert got[t, h] == bf16_decode(bf16_encode(np.array([acc])))[0]
+
+
+# ----------------------------------------------------------------------------- UE8M0 packing
+# The packed layouts are pinned against the two placement rules measured on the
+# tensor cores (not against their own formula):
+#  copy rule: a 32 x 16-byte shared-memory source goes to TMEM lanes i, 32+i,
+#    64+i, 96+i, columns 0..3 (row i -> its 4 words); with a core-matrix stride
+#    of 0 the 8-row core matrix repeats, so lane i takes source row i % 8;
+#  read rule: the MMA takes row m of A from lane m, column m // 32, and column n
+#    of B from lane n % 32, column n // 32; the scale-factor id picks the byte.
+def _tmem_after_copy(src_words, repeat8=False):
+    """[128 lanes, 4 columns] after one copy of a 512-byte (or 128-byte) source."""
+    w = np.asarray(src_words, np.uint32).reshape(-1, 4)
+    return np.array([w[(lane % 32) % 8] if repeat8 else w[lane % 32] for lane in range(128)])
+
+
+def test_ue8m0_act_packing_meets_the_tensor_core_placement():
+    rng = np.random.default_rng(3)
+    for G, rows, KB in ((128, 128, 8), (300, 900, 5), (16, 64, 2)):
+        groups = -(-rows // G)
+        e = rng.integers(-30, 30, (groups, KB, G))
+        s = np.exp2(e.astype(np.float64)).astype(np.float32)
+        words = oracle.pack_ue8m0_act(s, G, rows)
+        KG, NC = -(-KB // 4), -(-G // 128)
+        assert words.size == groups * KG * NC * 128
+        for grp in range(groups):
+            for g in range(KG):
+                for c in range(NC):
+                    chunk = words[((grp * KG + g) * NC + c) * 128:((grp * KG + g) * NC + c + 1) * 128]
+                    tm = _tmem_after_copy(chunk)
+                    for m in range(128):
+                        r = c * 128 + m                     # row of the group
+                        word = int(tm[m, m // 32])          # what the MMA reads for row m
+                        for sf_id in range(4):
+                            kb = 4 * g + sf_id
+                            byte = (word >> (8 * sf_id)) & 0xFF
+                            if r < G and grp * G + r < rows and kb < KB:
+                                assert byte == e[grp, kb, r] + 127
+                            else:
+                                assert byte == 0x7F
+
+
+def test_ue8m0_weight_packing_meets_the_tensor_core_placement():
+    rng = np.random.default_rng(4)
+    E, NB, KB = 3, 2, 6
+    e = rng.integers(-20, 20, (E, NB, KB))
+    words = oracle.pack_ue8m0_weight(np.exp2(e.astype(np.float64)).astype(np.float32))
+    KG = -(-KB // 4)
+    assert words.size == E * NB * KG * 32
+    for ex in range(E):
+        for g in range(KG):
+            # a 256-column tile: block 0's record to columns 0..3, block 1's to 4..7
+            cols = np.concatenate([_tmem_after_copy(words[((ex * NB + nb) * KG + g) * 32:
+                                                          ((ex * NB + nb) * KG + g + 1) * 32], repeat8=True)
+                                   for nb in range(NB)], axis=1)
+            for n in range(NB * 128):
+                word = int(cols[n % 32, n // 32])
+                for sf_id in range(4):
+                    kb = 4 * g + sf_id
+                    byte = (word >> (8 * sf_id)) & 0xFF
+                    assert byte == (e[ex, n // 128, kb] + 127 if kb < KB else 0x7F)
