@@ -144,7 +144,7 @@ def gemm2_variant(wl):
     """The GEMM2 kernel moe_ffn runs for this workload."""
     import fp8_grouped_expert_x128_gb300 as moe
     if is_ue8m0(wl):
-        return _ue8m0_variant(wl)
+        return _ue8m0_variant(wl) + ("<combine1>" if combine_fused(wl) else "")
     if wl["layout"] == moe.MOE_LAYOUT_MASKED:
         v = moe.moe_gemm_fp8_masked_variant(wl["cfg"].max_m, wl["expected_m"], wl.get("gemm_flags", 0))
         if v != 0:
@@ -158,7 +158,7 @@ def combine_fused(wl):
     """moe_ffn folds the combine into GEMM2's epilogue for one routing slot per
     token (device output; the tokens-as-M kernel serving GEMM2)."""
     import fp8_grouped_expert_x128_gb300 as moe
-    if wl["k"] != 1 or is_ue8m0(wl):
+    if wl["k"] != 1:
         return False
     if wl["layout"] == moe.MOE_LAYOUT_MASKED:
         return moe.moe_gemm_fp8_masked_variant(wl["cfg"].max_m, wl["expected_m"], wl.get("gemm_flags", 0)) == 0

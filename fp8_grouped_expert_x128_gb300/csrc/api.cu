@@ -214,8 +214,12 @@ FfnFusion ffn_fusion(const moe_ffn_desc* d, bool out_on_host) {
   const bool masked = d->layout == MOE_LAYOUT_MASKED;
   const int32_t gflags = d->gemm_flags & ~MOE_FFN_FUSE_SWIGLU;
   FfnFusion f;
-  if (d->gemm_flags & MOE_FFN_UE8M0) {   // the block-scaled GEMMs have no fused epilogues
-    f.swiglu = f.combine = false;
+  if (d->gemm_flags & MOE_FFN_UE8M0) {
+    // the block-scaled path: no SwiGLU fusion; the single-slot combine goes
+    // into GEMM2's epilogue where the tokens-as-M kernel serves it
+    f.swiglu = false;
+    f.combine = d->k == 1 && !out_on_host &&
+                (!masked || moe_gemm_fp8_masked_variant(d->max_m, d->expected_m, gflags) == 0);
     return f;
   }
   // stages 3+4: on request (MOE_FFN_FUSE_SWIGLU) and where the tokens-as-M
@@ -337,13 +341,19 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
                             st)))
       return rc;
     if ((rc = mark(4))) return rc;
-    rc = masked ? moe_gemm_fp8_masked_ue8m0(a2, sf2, d->w2, d->w2_sf, counts, d->E, d->max_m, d->H, d->I,
-                                            d->expected_m, y2, gflags, d->err, stream)
-                : moe_gemm_fp8_contig_ue8m0(a2, d->I, sf2, p.rows, d->w2, d->w2_sf, offsets, mind, p.rows, d->E,
-                                            d->H, d->I, y2, d->H, gflags, d->err, stream);
+    if (fuse_combine)
+      rc = gemm_ue8m0_combine1(a2, sf2, d->w2, d->w2_sf, masked ? counts : nullptr, masked ? nullptr : offsets,
+                               masked ? nullptr : mind, p.rows, d->E, d->max_m, d->H, d->I, rowsrc, d->topk_w,
+                               d->out, d->H, gflags, d->err, st);
+    else
+      rc = masked ? moe_gemm_fp8_masked_ue8m0(a2, sf2, d->w2, d->w2_sf, counts, d->E, d->max_m, d->H, d->I,
+                                              d->expected_m, y2, gflags, d->err, stream)
+                  : moe_gemm_fp8_contig_ue8m0(a2, d->I, sf2, p.rows, d->w2, d->w2_sf, offsets, mind, p.rows, d->E,
+                                              d->H, d->I, y2, d->H, gflags, d->err, stream);
     if (rc) return rc;
     if ((rc = mark(5))) return rc;
-    if ((rc = moe_combine(y2, d->H, p.rows, dst, d->topk_w, d->T, d->k, d->H, nullptr, 0, 0, d->out, d->H, d->err,
+    if (!fuse_combine &&
+        (rc = moe_combine(y2, d->H, p.rows, dst, d->topk_w, d->T, d->k, d->H, nullptr, 0, 0, d->out, d->H, d->err,
                           stream)))
       return rc;
     return mark(6);

@@ -97,6 +97,14 @@ int gemm_contig_swiglu(const uint8_t* A, int64_t lda, const float* sA, int64_t s
                        uint8_t* Q2, float* S2, int64_t s2_ld, int32_t flags, int32_t* err,
                        cudaStream_t st);
 
+// Block-scaled (UE8M0) GEMM2 with the single-slot combine in its epilogue
+// (moe_ffn with MOE_FFN_UE8M0, k = 1); contiguous when offsets != NULL.
+int gemm_ue8m0_combine1(const uint8_t* A, const uint32_t* sfA, const uint8_t* B, const uint32_t* sfB,
+                        const int32_t* counts, const int32_t* offsets, const int32_t* m_indices, int64_t rows,
+                        int32_t E, int32_t max_m, int32_t N, int32_t K, const int32_t* row_src,
+                        const float* topk_w, uint16_t* out, int64_t ldo, int32_t flags, int32_t* err,
+                        cudaStream_t st);
+
 // Encode a 2-D K-major uint8 tensor map with 128-byte swizzle:
 // global [rows, cols] (row stride ld bytes), box [box_rows, 128 bytes].
 int make_tmap_u8_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
@@ -208,6 +216,28 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// ---- cp.async: a 4-byte global -> shared copy that does not block the issuing
+// thread; src_bytes = 0 reads nothing and writes zeros.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+// One arrival on `bar` from this thread once all of its earlier cp.async
+// copies have landed (counted against the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Global -> shared bulk copy (16-byte aligned, a multiple of 16 bytes) that
+// completes `bytes` of transaction count on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
 }
 
 // ---- tcgen05 (5th-generation tensor cores, accumulators in TMEM)

@@ -826,16 +826,22 @@ template <int BNT>
 struct WeightsM {
   static constexpr uint32_t kWBytes = 128 * BK;                // weight tile
   static constexpr uint32_t kTBytes = BNT * BK;                // token tile (max)
-  static constexpr uint32_t kStage = kWBytes + kTBytes;
-  static constexpr int kStages = (196608 / kStage) > 8 ? 8 : (196608 / kStage);
+  // per stage after the two tiles: the k-block's token scales (BNT floats,
+  // one bulk copy) and the weight block's scale (one float, cp.async)
+  static constexpr uint32_t kOffSa = kWBytes + kTBytes;
+  static constexpr uint32_t kOffSb = kOffSa + BNT * 4;
+  static constexpr uint32_t kStage = (kOffSb + 16 + 1023) / 1024 * 1024;   // stages stay 1 KB aligned
+  // stages fill what shared memory is left after the barriers and the
+  // largest schedule (kMaxExperts), at most 8
+  static constexpr uint32_t kStageBudget = 232448 - 1024 - 16 * 8 * 2 - 16 - 4 * (3 * kMaxExperts + 1);
+  static constexpr int kStages = (kStageBudget / kStage) > 8 ? 8 : (kStageBudget / kStage);
   static constexpr int kBufs = (512 / BNT) > 8 ? 8 : (512 / BNT);
   static constexpr int kHalf = BNT / 2;                        // columns per epilogue warpgroup
   static constexpr bool kSplitRegs = BNT > 128;                // 128 accumulators/thread need the split
   static constexpr int kPair = 2;                              // TMEM loads in flight
-  static constexpr size_t kScaleBufBytes = sizeof(float) * kEpiWarps * 2 * kHalf;
   static constexpr size_t smem_bytes(int E) {
     return 1024 + static_cast<size_t>(kStages) * kStage + (2 * kStages + 2 * kBufs) * 8 + 16 +
-           sizeof(int32_t) * (3 * E + 1) + 16 + kScaleBufBytes;
+           sizeof(int32_t) * (3 * E + 1);
   }
 };
 
@@ -888,8 +894,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int32_t* sched_mem = reinterpret_cast<int32_t*>(tmem_slot + 4);
   const Sched sched{sched_mem, sched_mem + p.E + 1, sched_mem + 2 * p.E + 1};
-  float* sa_stage = reinterpret_cast<float*>(
-      (reinterpret_cast<uintptr_t>(sched_mem + 3 * p.E + 1) + 15) & ~static_cast<uintptr_t>(15));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars);
@@ -901,9 +905,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = abort_flag;
 
   if (threadIdx.x == 0) {
+    // a stage is full once its copies landed (the producer's expect-tx arrival
+    // and its cp.async arrival) and empty once the MMAs that read it are done
+    // and every epilogue warp has read its scales
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, 2);
+      mbar_init(empty0 + 8 * s, 1 + kEpiWarps);
     }
     for (int b = 0; b < C::kBufs; ++b) {
       mbar_init(tfull0 + 8 * b, 1);
@@ -951,8 +958,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t st_base = smem_u32(smem + s * C::kStage);
-          mbar_arrive_expect_tx(full0 + 8 * s, C::kWBytes + ncols * BK);
+          mbar_arrive_expect_tx(full0 + 8 * s, C::kWBytes + ncols * BK + ncols * 4);
           tma_load_2d_hint(st_base, &tmW, full0 + 8 * s, kb * BK, w_row, pol_w);
+          // this k-block's scales: the tile's token scales (ncols floats, 16-byte
+          // aligned since max_m and the tile start are multiples of 16) and the
+          // weight block's scale
+          bulk_g2s(st_base + C::kOffSa, p.sA + (static_cast<int64_t>(e) * KB + kb) * p.max_m + j * BNT, ncols * 4,
+                   full0 + 8 * s);
+          cp_async_4(st_base + C::kOffSb, p.sB + (static_cast<int64_t>(e) * nblk + nb) * KB + kb, 4u);
+          cp_async_mbar_arrive(full0 + 8 * s);
           // rows [0, ncols) in boxes of 128 while they last, then at most one
           // each of 64, 32 and 16 (ncols is a multiple of 16)
           for (int r = 0; r < ncols;) {
@@ -971,6 +985,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             p.wait_limit_ns / 10);
         }
       }
+      cp_async_wait_all();   // no copy may land after the CTA has gone
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -1018,7 +1033,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;             // TMEM lanes = weight rows q*32 .. q*32+31
     const int g = (warp - kEpiWarp0) >> 2;  // token columns [g*kHalf, (g+1)*kHalf)
-    float* my_sa = sa_stage + (warp - kEpiWarp0) * 2 * C::kHalf;
     uint32_t acc_it = 0;
     TileCursor cur;
     bool ok = true;
@@ -1035,94 +1049,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int col0 = g ? cols_g0 : 0;
       const int my_cols = g ? ncols - cols_g0 : cols_g0;
       const int nchunk = my_cols / 16;
-      const float* sa_base = p.sA + static_cast<int64_t>(e) * KB * p.max_m + j * BNT + col0;
-      const float* sb_ptr = p.sB + (static_cast<int64_t>(e) * nblk + nb) * KB;
-      // Token scales run kScaleAhead k-blocks ahead of their use: one float4
-      // per lane in a register ring, parked in this warp's shared double buffer
-      // one k-block before use already multiplied by that k-block's weight
-      // scale (sB * sA, the same product the definition forms), so no global
-      // load latency and no scale product sits on the per-k-block path.  The k-block loop is unrolled by the ring depth, so
-      // each ring entry is loaded once and read kScaleAhead k-blocks later with
-      // no register moves in between (a move would wait for its load).
-      const bool ld_lane = lane * 4 < my_cols;
-      auto load_sa4 = [&](int k) {
-        return (ld_lane && k < KB)
-                   ? __ldg(reinterpret_cast<const float4*>(sa_base + static_cast<int64_t>(k) * p.max_m) + lane)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      };
-      auto load_sb = [&](int k) { return k < KB ? __ldg(sb_ptr + k) : 0.f; };
-      // pa[m] holds the token scales of the next k-block = m (mod 4) still to be
-      // parked; rs[m] the weight scale of the next k-block = m (mod 4) to use
-      float4 pa[kScaleAhead];
-      float rs[kScaleAhead];
-      static_assert(kScaleAhead == 4, "ring indexing below assumes 4");
-      pa[1] = load_sa4(1); pa[2] = load_sa4(2); pa[3] = load_sa4(3); pa[0] = load_sa4(4);
-#pragma unroll
-      for (int m = 0; m < kScaleAhead; ++m) rs[m] = load_sb(m);
-      auto park = [&](float* dst, float4 a, float sb) {
-        if (ld_lane)
-          reinterpret_cast<float4*>(dst)[lane] =
-              make_float4(__fmul_rn(sb, a.x), __fmul_rn(sb, a.y), __fmul_rn(sb, a.z), __fmul_rn(sb, a.w));
-      };
-      {
-        const float4 pa0 = load_sa4(0);
-        __syncwarp();
-        park(my_sa, pa0, rs[0]);
-        __syncwarp();
-      }
       float2 acc[C::kHalf / 2];
 #pragma unroll
       for (int i = 0; i < C::kHalf / 2; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll 1
-      for (int kb0 = 0; ok && kb0 < KB; kb0 += kScaleAhead) {
+      for (int kb = 0; ok && kb < KB; ++kb) {
+        const uint32_t b = acc_it % C::kBufs, tph = (acc_it / C::kBufs) & 1;
+        const uint32_t s = acc_it % C::kStages, sph = (acc_it / C::kStages) & 1;
+        ++acc_it;
+        int got = 1;
+        if (lane == 0) got = mbar_wait_bounded(tfull0 + 8 * b, tph, abort, p.err, p.wait_limit_ns);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        // the stage's copies landed before its MMAs were issued; waiting on its
+        // (already completed) full phase orders this warp's scale reads after them
+        if (got) got = mbar_wait_bounded(full0 + 8 * s, sph, abort, p.err, p.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // this k-block's scales from the stage: sB * sA per token column (the
+        // product the definition forms), no global load on this path
+        const uint8_t* stg = smem + s * C::kStage;
+        const float sbv = *reinterpret_cast<const float*>(stg + C::kOffSb);
+        const float* sa_cur = reinterpret_cast<const float*>(stg + C::kOffSa) + col0;
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BNT + col0;
 #pragma unroll
-        for (int m = 0; m < kScaleAhead; ++m) {
-          const int kb = kb0 + m;
-          if (kb >= KB) break;
-          const uint32_t b = acc_it % C::kBufs, tph = (acc_it / C::kBufs) & 1;
-          ++acc_it;
-          rs[m] = load_sb(kb + kScaleAhead);
-          int got = 1;
-          if (lane == 0) got = mbar_wait_bounded(tfull0 + 8 * b, tph, abort, p.err, p.wait_limit_ns);
-          got = __shfl_sync(0xffffffffu, got, 0);
-          if (!got) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BNT + col0;
-          const float* sa_cur = my_sa + (kb & 1) * C::kHalf;
+        for (int ch = 0; ch < C::kHalf / 16; ch += C::kPair) {
+          if (ch < nchunk) {
+            uint32_t r[C::kPair][16];
+            tmem_ld_32x32b_x16(tbase + ch * 16, r[0]);
+            if (C::kPair == 2 && ch + 1 < nchunk) tmem_ld_32x32b_x16(tbase + (ch + 1) * 16, r[C::kPair - 1]);
+            tmem_ld_wait();
 #pragma unroll
-          for (int ch = 0; ch < C::kHalf / 16; ch += C::kPair) {
-            if (ch < nchunk) {
-              uint32_t r[C::kPair][16];
-              tmem_ld_32x32b_x16(tbase + ch * 16, r[0]);
-              if (C::kPair == 2 && ch + 1 < nchunk) tmem_ld_32x32b_x16(tbase + (ch + 1) * 16, r[C::kPair - 1]);
-              tmem_ld_wait();
+            for (int h = 0; h < C::kPair; ++h) {
+              if (ch + h < nchunk) {
 #pragma unroll
-              for (int h = 0; h < C::kPair; ++h) {
-                if (ch + h < nchunk) {
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) {
-                    const int c = (ch + h) * 16 + 2 * i;
-                    const float2 s2 = *reinterpret_cast<const float2*>(sa_cur + c);
-                    acc[c / 2] = __ffma2_rn(
-                        s2, make_float2(__uint_as_float(r[h][2 * i]), __uint_as_float(r[h][2 * i + 1])), acc[c / 2]);
-                  }
+                for (int i4 = 0; i4 < 4; ++i4) {
+                  const int c = (ch + h) * 16 + 4 * i4;
+                  const float4 a4 = *reinterpret_cast<const float4*>(sa_cur + c);   // broadcast read
+                  const float2 s01 = make_float2(__fmul_rn(sbv, a4.x), __fmul_rn(sbv, a4.y));
+                  const float2 s23 = make_float2(__fmul_rn(sbv, a4.z), __fmul_rn(sbv, a4.w));
+                  acc[c / 2] = __ffma2_rn(
+                      s01, make_float2(__uint_as_float(r[h][4 * i4]), __uint_as_float(r[h][4 * i4 + 1])), acc[c / 2]);
+                  acc[c / 2 + 1] = __ffma2_rn(
+                      s23, make_float2(__uint_as_float(r[h][4 * i4 + 2]), __uint_as_float(r[h][4 * i4 + 3])),
+                      acc[c / 2 + 1]);
                 }
               }
             }
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty0 + 8 * b);
-          // park the next k-block's token scales, then refill that ring entry
-          const int mn = (m + 1) % kScaleAhead;
-          if (kb + 1 < KB) {
-            park(my_sa + ((kb + 1) & 1) * C::kHalf, pa[mn], rs[mn]);   // rs[mn]: sB of k-block kb + 1
-            __syncwarp();
-          }
-          pa[mn] = load_sa4(kb + 1 + kScaleAhead);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(tempty0 + 8 * b);   // the accumulator buffer is free
+          mbar_arrive(empty0 + 8 * s);    // this warp is done with the stage's scales
         }
       }
       if (!ok) break;

@@ -60,6 +60,12 @@ struct BsArgs {
   int32_t* err;
   uint64_t wait_limit_ns;
   int32_t flags;
+  // one routing slot per token (tokens-as-M kernel): write out[token] =
+  // bf16(w * bf16(D)) instead of D, the combine's arithmetic for one slot
+  const int32_t* row_src;
+  const float* topk_w;
+  uint16_t* out;
+  int64_t ldo;
 };
 
 // Instruction descriptor, kind::mxf8f6f4 with block scaling: D fp32, A = B =
@@ -99,14 +105,6 @@ __device__ __forceinline__ uint64_t sdesc_cp_src(uint32_t saddr, uint32_t sbo) {
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;   // descriptor version; no swizzle
   return d;
-}
-
-// Global -> shared bulk copy (16-byte aligned, multiple of 16 bytes) that
-// completes `bytes` of transaction count on `bar`.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-               : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -279,6 +277,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t gr = static_cast<int64_t>(sched.rbase[e]) + r_local;
       bool row_ok = r_local < sched.rext[e];
       if (row_ok && p.layout == MOE_LAYOUT_CONTIG) row_ok = __ldg(p.m_indices + gr) >= 0;
+      // single-slot combine: the row's token and weight, loaded while the tile computes
+      int64_t tok = 0;
+      float wtok = 0.f;
+      if (p.out != nullptr && row_ok) {
+        tok = __ldg(p.row_src + gr);
+        wtok = __ldg(p.topk_w + tok);
+      }
       int got = 1;
       if (lane == 0) got = mbar_wait_bounded(tfull, tile_no & 1, abort, p.err, p.wait_limit_ns);
       got = __shfl_sync(0xffffffffu, got, 0);
@@ -302,14 +307,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty);
       if (active && row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(p.D + gr * p.ldd + nt * BN + g * 128);
+        const bool to_out = p.out != nullptr;
+        uint4* dst = reinterpret_cast<uint4*>(to_out ? p.out + tok * p.ldo + nt * BN + g * 128
+                                                     : p.D + gr * p.ldd + nt * BN + g * 128);
+        auto rb = [](float x) { return __bfloat162float(__float2bfloat16_rn(x)); };
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           uint32_t o[4];
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
-            const __nv_bfloat162 bb =
-                __floats2bfloat162_rn(__uint_as_float(v[c * 8 + 2 * h]), __uint_as_float(v[c * 8 + 2 * h + 1]));
+            const float a0 = __uint_as_float(v[c * 8 + 2 * h]), a1 = __uint_as_float(v[c * 8 + 2 * h + 1]);
+            const __nv_bfloat162 bb = to_out ? __floats2bfloat162_rn(fmaf(wtok, rb(a0), 0.f), fmaf(wtok, rb(a1), 0.f))
+                                             : __floats2bfloat162_rn(a0, a1);
             o[h] = *reinterpret_cast<const uint32_t*>(&bb);
           }
           dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -701,6 +710,51 @@ __global__ void __launch_bounds__(256) pack_ue8m0_weight_kernel(const float* __r
 inline int32_t kgroups(int64_t K) { return static_cast<int32_t>((K / 128 + 3) / 4); }
 
 }  // namespace
+
+// GEMM2 of the UE8M0 FFN with the single-slot combine in the epilogue (k = 1,
+// tokens-as-M kernel): routed row r goes to out[row_src[r]] scaled by
+// topk_w[row_src[r]].  Contiguous layout when offsets != NULL, else masked.
+int gemm_ue8m0_combine1(const uint8_t* A, const uint32_t* sfA, const uint8_t* B, const uint32_t* sfB,
+                        const int32_t* counts, const int32_t* offsets, const int32_t* m_indices, int64_t rows,
+                        int32_t E, int32_t max_m, int32_t N, int32_t K, const int32_t* row_src,
+                        const float* topk_w, uint16_t* out, int64_t ldo, int32_t flags, int32_t* err,
+                        cudaStream_t st) {
+  MOE_CHECK_ARG(E >= 1 && E <= kMaxExperts && N > 0 && N % 128 == 0 && K > 0 && K % 128 == 0 && rows > 0);
+  MOE_CHECK_ARG(A && sfA && B && sfB && row_src && topk_w && out && aligned16(out) && ldo >= N && ldo % 8 == 0);
+  if (int rc = check_device()) return rc;
+  BsArgs a{};
+  a.sfA = sfA;
+  a.KG = kgroups(K);
+  a.sfB = sfB;
+  a.E = E;
+  a.N = N;
+  a.K = K;
+  a.err = err;
+  a.flags = flags & ~MOE_GEMM_DEBUG_STALL;
+  a.row_src = row_src;
+  a.topk_w = topk_w;
+  a.out = out;
+  a.ldo = ldo;
+  if (offsets != nullptr) {
+    MOE_CHECK_ARG(m_indices && rows % BM == 0);
+    a.sf_G = rows;
+    a.sf_NC = static_cast<int32_t>(rows / BM);
+    a.offsets = offsets;
+    a.m_indices = m_indices;
+    a.M_capacity = rows;
+    a.layout = MOE_LAYOUT_CONTIG;
+    return launch_ue8m0(A, rows, K, B, (rows / BM) * ((N + BN - 1) / BN), a, st);
+  }
+  MOE_CHECK_ARG(counts && max_m > 0 && rows == static_cast<int64_t>(E) * max_m);
+  a.sf_G = max_m;
+  a.sf_NC = (max_m + BM - 1) / BM;
+  a.counts = counts;
+  a.max_m = max_m;
+  a.layout = MOE_LAYOUT_MASKED;
+  return launch_ue8m0(A, rows, K, B, static_cast<int64_t>(E) * ((max_m + BM - 1) / BM) * ((N + BN - 1) / BN), a,
+                      st);
+}
+
 }  // namespace moe
 
 using namespace moe;
