@@ -424,24 +424,28 @@ def _sum_over_ranks(world, v):
     return float(t.item())
 
 
+def kernel_source(kernel_label: str) -> str:
+    """The source file that holds a GEMM kernel (by its label)."""
+    return "gemm_bs.cu" if "ue8m0" in kernel_label else "gemm.cu"
+
+
 def recorded_traffic(kernel_label: str, workload: str, which: str = "gemm1"):
     """DRAM bytes (read + write) per launch of this kernel (as GEMM1 or GEMM2) on
     this workload from the ncu capture recorded in profiles/traffic.json, or
-    None when there is no capture or gemm.cu has changed since it was taken.
-    A record may hold a capture of a cut-down case scaled to the full launch
-    (its "scaled_from" field says how)."""
+    None when there is no capture or the kernel's source file has changed since
+    it was taken.  A record may hold a capture of a cut-down case scaled to the
+    full launch (its "scaled_from" field says how)."""
     import hashlib
     path = os.path.join(HERE, "profiles", "traffic.json")
-    src = os.path.join(HERE, "fp8_grouped_expert_x128_gb300", "csrc", "gemm.cu")
     if not os.path.exists(path):
         return None
-    with open(src, "rb") as f:
+    src_name = kernel_source(kernel_label)
+    with open(os.path.join(HERE, "fp8_grouped_expert_x128_gb300", "csrc", src_name), "rb") as f:
         sha = hashlib.sha256(f.read()).hexdigest()
     with open(path) as f:
         rec = json.load(f)
-    r = rec.get(f"{kernel_label}@{workload}:{which}") or (rec.get(f"{kernel_label}@{workload}")
-                                                          if which == "gemm1" else None)
-    if not r or r.get("gemm_cu_sha256") != sha:
+    r = rec.get(f"{kernel_label}@{workload}:{which}")
+    if not r or r.get("src") != src_name or r.get("src_sha256") != sha:
         return None
     return r["dram_read_bytes"] + r["dram_write_bytes"]
 
