@@ -78,6 +78,20 @@ int make_tmap_u8_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
+int make_tmap_b16_out(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld_bytes) {
+  std::call_once(g_encode_once, load_encode);
+  if (g_encode == nullptr) return MOE_ERR_CUDA;
+  if (!aligned16(base) || ld_bytes % 16 != 0 || rows == 0 || cols == 0) return MOE_ERR_INVALID_ARG;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {ld_bytes};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides,
+                              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
 namespace {
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }

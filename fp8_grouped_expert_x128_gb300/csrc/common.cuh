@@ -109,6 +109,10 @@ int gemm_ue8m0_combine1(const uint8_t* A, const uint32_t* sfA, const uint8_t* B,
 // global [rows, cols] (row stride ld bytes), box [box_rows, 128 bytes].
 int make_tmap_u8_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                        uint64_t ld_bytes, uint32_t box_rows);
+// 2-D map over a row-major bf16 (16-bit) matrix for TMA stores of 32 x 32
+// boxes from shared memory in the 64-byte swizzle (a 64-byte row's 16-byte
+// chunk c sits at c ^ ((row >> 1) & 3)).  Same rules and codes as above.
+int make_tmap_b16_out(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld_bytes);
 
 // ---------------------------------------------------------------- device side
 // Default limit of one pipeline wait.  Waits normally last microseconds; past
@@ -239,6 +243,30 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
                : "memory");
 }
+
+// Shared -> global TMA store of one box, tracked by the issuing thread's bulk
+// groups.  The writes to shared memory it reads must be made visible to the
+// async proxy first (fence_proxy_async_shared by each writing thread).
+__device__ __forceinline__ void tma_store_2d(const void* map, uint32_t src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's bulk stores have read their shared-memory source
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// all but the most recent of this thread's bulk store groups have read their source
+__device__ __forceinline__ void bulk_wait_read_le1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// this thread's bulk stores are complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // ---- tcgen05 (5th-generation tensor cores, accumulators in TMEM)
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

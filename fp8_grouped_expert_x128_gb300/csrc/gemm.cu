@@ -22,8 +22,13 @@
 //    two TMEM buffers (2 x 256 columns), and the epilogue warps read it with
 //    tcgen05.ld, multiply by sA[row, kb] * sB[nb, kb] and accumulate in fp32
 //    registers while the tensor cores fill the other buffer;
+//  * output: bf16 tiles go through per-warp shared-memory staging, as TMA
+//    tensor stores (32 x 32 boxes) where a warp's 32 rows are all valid,
+//    otherwise as 64-byte row segments from 8 lanes per row;
 //  * every wait is bounded (see common.cuh): a stalled pipeline flags
 //    MOE_DEV_TIMEOUT and the CTA unwinds, frees its TMEM and returns.
+#include <cstring>
+
 #include "gemm_common.cuh"
 
 namespace moe {
@@ -77,6 +82,10 @@ struct GemmArgs {
   const float* topk_w;
   uint16_t* out;
   int64_t ldo;
+  // plain mode: bf16 D goes out through TMA stores (tmD) for warps whose 32
+  // rows are all valid
+  int32_t tma_store;
+  int32_t ostage_slots;   // 2 KB output staging slots per epilogue warp (1 or 2)
 };
 
 // kSwiGLU: the 256-wide B tile is 128 gate rows + the matching 128 up rows
@@ -86,20 +95,24 @@ struct GemmArgs {
 template <bool kSwiGLU>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_tokens_m_kernel(const __grid_constant__ CUtensorMap tmA,
-                             const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
+                             const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmD,   // bf16 D, when p.tma_store
+                             const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* a_tiles = smem;
   uint8_t* b_tiles = smem + kStages * kATileBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  // output staging, 1 KB aligned (the TMA store's 64-byte swizzle pattern):
+  // kEpiWarps x ostage_slots x kOutStageBytes; SwiGLU mode (no bf16 output)
+  // keeps its per-row amax exchange there instead, [tile parity][g][row]
+  uint8_t* ostage = smem + kStages * kStageBytes;
+  float* xch = reinterpret_cast<float*>(ostage);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ostage + kEpiWarps * p.ostage_slots * kOutStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 8);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int32_t* sched_mem = reinterpret_cast<int32_t*>(tmem_slot + 4);
   const Sched sched{sched_mem, sched_mem + p.E + 1, sched_mem + 2 * p.E + 1};
-  // SwiGLU mode: per-row amax of each warpgroup's 64 columns, [tile parity][g][row]
-  float* xch = reinterpret_cast<float*>(sched_mem + ((3 * p.E + 1 + 3) & ~3));
-  uint8_t* ostage = reinterpret_cast<uint8_t*>(xch + 2 * 256);   // kEpiWarps x kOutStageBytes
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars);
@@ -131,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (p.tma_store) tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -366,9 +380,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint16_t* row_base = to_out ? p.out + tok * p.ldo + n0 : p.D + gr * p.ldd + n0;
           const float w = wtok;
           auto rb = [](float v) { return __bfloat162float(__float2bfloat16_rn(v)); };
-          const uint32_t stg = smem_u32(ostage + (warp - kEpiWarp0) * kOutStageBytes);
+          const int slots = p.ostage_slots;
+          const uint32_t stg0 = smem_u32(ostage + (warp - kEpiWarp0) * slots * kOutStageBytes);
+          // D rows all valid for this warp: each quarter leaves as one TMA
+          // store of a 32 x 32 box (the staging layout is the map's 64-byte
+          // swizzle), issued by lane 0; otherwise 8 lanes per row store it
+          const bool by_tma = p.tma_store && !to_out && __all_sync(0xffffffffu, row_ok);
+          const int32_t d_row0 = static_cast<int32_t>(gr - lane);
 #pragma unroll
           for (int qc = 0; qc < 4; ++qc) {
+            // the staging slot is free once the TMA store from it has read it:
+            // with two slots, all but the latest store
+            const uint32_t stg = stg0 + (slots == 2 ? (qc & 1) : 0) * kOutStageBytes;
+            if (lane == 0 && p.tma_store) {
+              if (slots == 2)
+                bulk_wait_read_le1();
+              else
+                bulk_wait_read_all();
+            }
+            __syncwarp();
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               const int v = qc * 4 + c;       // 16-byte chunk of the row: columns 8v .. 8v+7
@@ -381,6 +411,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 o[h] = *reinterpret_cast<const uint32_t*>(&bb);
               }
               st_shared_v4(stg + out_stage_slot(lane, c), make_uint4(o[0], o[1], o[2], o[3]));
+            }
+            if (by_tma) {
+              fence_proxy_async_shared();   // this lane's staging writes, visible to the TMA
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmD, stg, n0 + qc * 32, d_row0);
+                bulk_commit_group();
+              }
+              continue;
             }
             __syncwarp();
 #pragma unroll
@@ -452,6 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    // the TMA stores issued by this warp are complete before the CTA ends
+    if (p.tma_store && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -462,19 +503,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-size_t tokens_m_smem_bytes(int E) {
+size_t tokens_m_smem_bytes(int E, int slots) {
   return 1024 + static_cast<size_t>(kStages) * kStageBytes + (2 * kStages + 8) * 8 + 16 +
-         sizeof(int32_t) * (3 * E + 1 + 3) + sizeof(float) * 2 * 256 + kEpiWarps * kOutStageBytes;
+         sizeof(int32_t) * (3 * E + 1) + kEpiWarps * slots * kOutStageBytes;
 }
+// two output staging slots per warp (a quarter is written while the previous
+// one's TMA store reads the other) where shared memory allows, else one
+int tokens_m_slots(int E) { return tokens_m_smem_bytes(E, 2) <= kMaxSmemPerBlock ? 2 : 1; }
 
 int launch_tokens_m(const uint8_t* A, int64_t a_rows, int64_t lda, const uint8_t* B,
                     int64_t tiles_upper, GemmArgs& args, cudaStream_t stream, bool swiglu = false) {
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmD;
   if (int st = make_tmap_u8_sw128(&tmA, A, a_rows, args.K, lda, BM)) return st;
   if (int st = make_tmap_u8_sw128(&tmB, B, static_cast<uint64_t>(args.E) * args.N, args.K, args.K,
                                   swiglu ? 128 : BN))
     return st;
-  const size_t smem = tokens_m_smem_bytes(args.E);
+  // plain bf16 D (a_rows rows of ldd) leaves through TMA stores when it can
+  // be mapped; otherwise, and for the fused modes, through the LSU path
+  std::memset(&tmD, 0, sizeof(tmD));
+  args.tma_store = 0;
+  if (!swiglu && args.out == nullptr && args.D != nullptr &&
+      make_tmap_b16_out(&tmD, args.D, static_cast<uint64_t>(a_rows), args.N, static_cast<uint64_t>(args.ldd) * 2) ==
+          MOE_OK)
+    args.tma_store = 1;
+  args.ostage_slots = tokens_m_slots(args.E);
+  const size_t smem = tokens_m_smem_bytes(args.E, args.ostage_slots);
   if (args.wait_limit_ns == 0) args.wait_limit_ns = kWaitLimitNs;
   int64_t grid = num_sms();
   if (tiles_upper < grid) grid = tiles_upper;
@@ -482,11 +535,11 @@ int launch_tokens_m(const uint8_t* A, int64_t a_rows, int64_t lda, const uint8_t
   if (swiglu) {
     if (int st = prepare_kernel(gemm_fp8_tokens_m_kernel<true>, smem, true)) return st;
     return launch_pdl(gemm_fp8_tokens_m_kernel<true>, static_cast<unsigned>(grid), kThreads, smem, stream, tmA,
-                      tmB, args);
+                      tmB, tmD, args);
   } else {
     if (int st = prepare_kernel(gemm_fp8_tokens_m_kernel<false>, smem, true)) return st;
     return launch_pdl(gemm_fp8_tokens_m_kernel<false>, static_cast<unsigned>(grid), kThreads, smem, stream, tmA,
-                      tmB, args);
+                      tmB, tmD, args);
   }
 }
 
@@ -833,7 +886,7 @@ struct WeightsM {
   static constexpr uint32_t kStage = (kOffSb + 16 + 1023) / 1024 * 1024;   // stages stay 1 KB aligned
   // stages fill what shared memory is left after the barriers and the
   // largest schedule (kMaxExperts), at most 8
-  static constexpr uint32_t kStageBudget = 232448 - 1024 - 16 * 8 * 2 - 16 - 4 * (3 * kMaxExperts + 1);
+  static constexpr uint32_t kStageBudget = kMaxSmemPerBlock - 1024 - 16 * 8 * 2 - 16 - 4 * (3 * kMaxExperts + 1);
   static constexpr int kStages = (kStageBudget / kStage) > 8 ? 8 : (kStageBudget / kStage);
   static constexpr int kBufs = (512 / BNT) > 8 ? 8 : (512 / BNT);
   static constexpr int kHalf = BNT / 2;                        // columns per epilogue warpgroup

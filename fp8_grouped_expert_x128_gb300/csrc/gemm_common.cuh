@@ -68,6 +68,7 @@ int prepare_kernel(F kernel, size_t smem, bool split_regs) {
   return MOE_OK;
 }
 constexpr uint32_t kTmemCols = 512;
+constexpr size_t kMaxSmemPerBlock = 232448;   // 227 KB opt-in dynamic shared memory per block
 constexpr int kMaxExperts = 1024;
 
 // Token-side tensor maps: the same [E*max_m, K] matrix with boxes of 16 << i
