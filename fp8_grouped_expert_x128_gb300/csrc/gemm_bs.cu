@@ -24,6 +24,8 @@
 //  * weight scales are per 128 x 128 block, the same word for 128 rows: a
 //    128-byte record of 32 copies, copied with a core-matrix stride of 0 so all
 //    32 lanes read it, gives the 4 columns of a 128-row block.
+#include <cstring>
+
 #include "gemm_common.cuh"
 
 namespace moe {
@@ -66,6 +68,8 @@ struct BsArgs {
   const float* topk_w;
   uint16_t* out;
   int64_t ldo;
+  // plain D leaves through TMA stores (tmD) for warps whose 32 rows are all valid
+  int32_t tma_store;
 };
 
 // Instruction descriptor, kind::mxf8f6f4 with block scaling: D fp32, A = B =
@@ -109,11 +113,14 @@ __device__ __forceinline__ uint64_t sdesc_cp_src(uint32_t saddr, uint32_t sbo) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_ue8m0_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmD,   // bf16 D, when p.tma_store
                           const BsArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBsStages * kBsStage);
+  // output staging after the stages, 1 KB aligned: kEpiWarps x kOutStageBytes
+  uint8_t* ostage = smem + kBsStages * kBsStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ostage + kEpiWarps * kOutStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBsBars);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int32_t* sched_mem = reinterpret_cast<int32_t*>(tmem_slot + 4);
@@ -144,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (p.tma_store) tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -306,25 +314,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty);
-      if (active && row_ok) {
+      if (active) {
+        // the warp's 32 rows x 128 columns leave in four 32-column quarters
+        // through its 2 KB of staging: as one TMA store of the 32 x 32 box when
+        // all 32 rows are valid D rows, else 8 lanes per row store 64-byte
+        // segments (also the single-slot combine's scattered output rows)
         const bool to_out = p.out != nullptr;
-        uint4* dst = reinterpret_cast<uint4*>(to_out ? p.out + tok * p.ldo + nt * BN + g * 128
-                                                     : p.D + gr * p.ldd + nt * BN + g * 128);
+        const int n0 = nt * BN + g * 128;
+        uint16_t* row_base = to_out ? p.out + tok * p.ldo + n0 : p.D + gr * p.ldd + n0;
         auto rb = [](float x) { return __bfloat162float(__float2bfloat16_rn(x)); };
+        const uint32_t stg = smem_u32(ostage + (warp - kEpiWarp0) * kOutStageBytes);
+        const bool by_tma = p.tma_store && !to_out && __all_sync(0xffffffffu, row_ok);
+        const int32_t d_row0 = static_cast<int32_t>(gr - lane);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          uint32_t o[4];
+        for (int qc = 0; qc < 4; ++qc) {
+          if (lane == 0 && p.tma_store) bulk_wait_read_all();   // the last TMA store has read the slot
+          __syncwarp();
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const float a0 = __uint_as_float(v[c * 8 + 2 * h]), a1 = __uint_as_float(v[c * 8 + 2 * h + 1]);
-            const __nv_bfloat162 bb = to_out ? __floats2bfloat162_rn(fmaf(wtok, rb(a0), 0.f), fmaf(wtok, rb(a1), 0.f))
-                                             : __floats2bfloat162_rn(a0, a1);
-            o[h] = *reinterpret_cast<const uint32_t*>(&bb);
+          for (int c = 0; c < 4; ++c) {
+            const int cc = qc * 4 + c;   // 16-byte chunk of the row: columns 8cc .. 8cc+7
+            uint32_t o[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const float a0 = __uint_as_float(v[cc * 8 + 2 * h]), a1 = __uint_as_float(v[cc * 8 + 2 * h + 1]);
+              const __nv_bfloat162 bb = to_out ? __floats2bfloat162_rn(fmaf(wtok, rb(a0), 0.f), fmaf(wtok, rb(a1), 0.f))
+                                               : __floats2bfloat162_rn(a0, a1);
+              o[h] = *reinterpret_cast<const uint32_t*>(&bb);
+            }
+            st_shared_v4(stg + out_stage_slot(lane, c), make_uint4(o[0], o[1], o[2], o[3]));
           }
-          dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+          if (by_tma) {
+            fence_proxy_async_shared();   // this lane's staging writes, visible to the TMA
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmD, stg, n0 + qc * 32, d_row0);
+              bulk_commit_group();
+            }
+            continue;
+          }
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = 8 * j + (lane >> 2), c = lane & 3;   // row of the warp, chunk of the quarter
+            const uint4 val = ld_shared_v4(stg + out_stage_slot(r, c));
+            const bool ok_r = __shfl_sync(0xffffffffu, row_ok, r);
+            uint16_t* base_r =
+                reinterpret_cast<uint16_t*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(row_base), r));
+            if (ok_r) *reinterpret_cast<uint4*>(base_r + qc * 32 + c * 8) = val;
+          }
+          __syncwarp();
         }
       }
     }
+    // the TMA stores issued by this warp are complete before the CTA ends
+    if (p.tma_store && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -630,14 +673,22 @@ int launch_ue8m0_weights_m(const uint8_t* A, const uint8_t* B, BsArgs& a, cudaSt
 }
 
 size_t ue8m0_smem_bytes(int E) {
-  return 1024 + static_cast<size_t>(kBsStages) * kBsStage + kBsBars * 8 + 16 + sizeof(int32_t) * (3 * E + 1);
+  return 1024 + static_cast<size_t>(kBsStages) * kBsStage + kEpiWarps * kOutStageBytes + kBsBars * 8 + 16 +
+         sizeof(int32_t) * (3 * E + 1);
 }
 
 int launch_ue8m0(const uint8_t* A, int64_t a_rows, int64_t lda, const uint8_t* B, int64_t tiles_upper, BsArgs& a,
                  cudaStream_t stream) {
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmD;
   if (int st = make_tmap_u8_sw128(&tmA, A, a_rows, a.K, lda, BM)) return st;
   if (int st = make_tmap_u8_sw128(&tmB, B, static_cast<uint64_t>(a.E) * a.N, a.K, a.K, BN)) return st;
+  // plain bf16 D (a_rows rows of ldd) leaves through TMA stores when it can be
+  // mapped; the single-slot combine's output rows through the LSU path
+  std::memset(&tmD, 0, sizeof(tmD));
+  a.tma_store = 0;
+  if (a.out == nullptr && a.D != nullptr &&
+      make_tmap_b16_out(&tmD, a.D, static_cast<uint64_t>(a_rows), a.N, static_cast<uint64_t>(a.ldd) * 2) == MOE_OK)
+    a.tma_store = 1;
   const size_t smem = ue8m0_smem_bytes(a.E);
   if (a.wait_limit_ns == 0) a.wait_limit_ns = kWaitLimitNs;
   if (a.flags & MOE_GEMM_DEBUG_STALL) a.wait_limit_ns = 200ull * 1000ull * 1000ull;
@@ -645,7 +696,7 @@ int launch_ue8m0(const uint8_t* A, int64_t a_rows, int64_t lda, const uint8_t* B
   int64_t grid = num_sms();
   if (tiles_upper < grid) grid = tiles_upper;
   if (grid < 1) grid = 1;
-  return launch_pdl(gemm_fp8_ue8m0_kernel, static_cast<unsigned>(grid), kThreads, smem, stream, tmA, tmB, a);
+  return launch_pdl(gemm_fp8_ue8m0_kernel, static_cast<unsigned>(grid), kThreads, smem, stream, tmA, tmB, tmD, a);
 }
 
 // ---------------------------------------------------------------- packing

@@ -68,6 +68,24 @@ int prepare_kernel(F kernel, size_t smem, bool split_regs) {
   return MOE_OK;
 }
 constexpr uint32_t kTmemCols = 512;
+// Output staging of the tokens-as-M epilogues: per epilogue warp, 32 rows x
+// 32 bf16 columns (64 bytes per row), the row's 16-byte chunk c kept in slot
+// c ^ ((row >> 1) & 3): conflict-free both when a lane writes its own row's
+// chunks and when 8 lanes read two rows' four chunks.
+constexpr uint32_t kOutStageBytes = 32 * 64;
+__device__ __forceinline__ uint32_t out_stage_slot(int row, int chunk) {
+  return static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
 constexpr size_t kMaxSmemPerBlock = 232448;   // 227 KB opt-in dynamic shared memory per block
 constexpr int kMaxExperts = 1024;
 
