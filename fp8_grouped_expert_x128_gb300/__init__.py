@@ -42,6 +42,7 @@ MOE_GEMM_FORCE_WEIGHTS_M = 0x2
 MOE_FFN_FUSE_SWIGLU = 0x4
 MOE_GEMM_CTA_PAIR = 0x8
 MOE_FFN_UE8M0 = 0x10
+MOE_GEMM_EARLY_WEIGHTS = 0x20
 MOE_GEMM_DEBUG_STALL = 0x100
 MOE_QUANT_UE8M0 = 0x1
 MOE_COMBINE_ACCUMULATE = 0x1

@@ -330,6 +330,12 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
   const int32_t gflags = d->gemm_flags & ~(MOE_FFN_FUSE_SWIGLU | MOE_FFN_UE8M0);
   const FfnFusion fusion = ffn_fusion(d, out_on_host);
   const bool fuse_combine = fusion.combine;
+  // The routing arrays are written by the index kernel: two launches before
+  // GEMM1 when there are tokens (the quant-scatter runs in between) and more
+  // before GEMM2, so both GEMMs may build their schedule and start streaming
+  // weights before they wait for the kernel just ahead of them.
+  const int32_t g1flags = gflags | (d->T > 0 ? MOE_GEMM_EARLY_WEIGHTS : 0);
+  const int32_t g2flags = gflags | MOE_GEMM_EARLY_WEIGHTS;
   // stages 1+2: routing index pass, then each routed token row is quantised
   // straight into its expert slot (no token-order FP8 copy in between)
   if ((rc = mark(0))) return rc;
@@ -345,9 +351,9 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
     const uint32_t* sf1 = reinterpret_cast<const uint32_t*>(sa1);
     const uint32_t* sf2 = reinterpret_cast<const uint32_t*>(sa2);
     rc = masked ? moe_gemm_fp8_masked_ue8m0(a1, sf1, d->w13, d->w13_sf, counts, d->E, d->max_m, 2 * d->I, d->H,
-                                            d->expected_m, y1, gflags, d->err, stream)
+                                            d->expected_m, y1, g1flags, d->err, stream)
                 : moe_gemm_fp8_contig_ue8m0(a1, d->H, sf1, p.rows, d->w13, d->w13_sf, offsets, mind, p.rows, d->E,
-                                            2 * d->I, d->H, y1, 2 * d->I, gflags, d->err, stream);
+                                            2 * d->I, d->H, y1, 2 * d->I, g1flags, d->err, stream);
     if (rc) return rc;
     if ((rc = mark(3))) return rc;
     if ((rc = swiglu_launch(y1, p.rows, d->I, masked ? counts : nullptr, masked ? d->max_m : 0,
@@ -358,12 +364,12 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
     if (fuse_combine)
       rc = gemm_ue8m0_combine1(a2, sf2, d->w2, d->w2_sf, masked ? counts : nullptr, masked ? nullptr : offsets,
                                masked ? nullptr : mind, p.rows, d->E, d->max_m, d->H, d->I, rowsrc, d->topk_w,
-                               d->out, d->H, gflags, d->err, st);
+                               d->out, d->H, g2flags, d->err, st);
     else
       rc = masked ? moe_gemm_fp8_masked_ue8m0(a2, sf2, d->w2, d->w2_sf, counts, d->E, d->max_m, d->H, d->I,
-                                              d->expected_m, y2, gflags, d->err, stream)
+                                              d->expected_m, y2, g2flags, d->err, stream)
                   : moe_gemm_fp8_contig_ue8m0(a2, d->I, sf2, p.rows, d->w2, d->w2_sf, offsets, mind, p.rows, d->E,
-                                              d->H, d->I, y2, d->H, gflags, d->err, stream);
+                                              d->H, d->I, y2, d->H, g2flags, d->err, stream);
     if (rc) return rc;
     if ((rc = mark(5))) return rc;
     if (!fuse_combine &&
@@ -376,20 +382,20 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
   if (fuse_swiglu) {
     if (masked)
       rc = gemm_masked_swiglu(a1, sa1, d->w13, d->w13_s, counts, d->E, d->max_m, 2 * d->I, d->H,
-                              a2, sa2, gflags, d->err, st);
+                              a2, sa2, g1flags, d->err, st);
     else
       rc = gemm_contig_swiglu(a1, d->H, sa1, p.s_ld1, d->w13, d->w13_s, offsets, mind, p.rows, d->E,
-                              2 * d->I, d->H, a2, sa2, p.s_ld2, gflags, d->err, st);
+                              2 * d->I, d->H, a2, sa2, p.s_ld2, g1flags, d->err, st);
     if (rc) return rc;
     if ((rc = mark(3))) return rc;
     if ((rc = mark(4))) return rc;
   } else {
     if (masked)
       rc = moe_gemm_fp8_masked(a1, sa1, d->w13, d->w13_s, counts, d->E, d->max_m, 2 * d->I, d->H,
-                               d->expected_m, y1, gflags, d->err, stream);
+                               d->expected_m, y1, g1flags, d->err, stream);
     else
       rc = moe_gemm_fp8_contig(a1, d->H, sa1, p.s_ld1, d->w13, d->w13_s, offsets, mind, p.rows, d->E,
-                               2 * d->I, d->H, y1, 2 * d->I, gflags, d->err, stream);
+                               2 * d->I, d->H, y1, 2 * d->I, g1flags, d->err, stream);
     if (rc) return rc;
     if ((rc = mark(3))) return rc;
     if ((rc = moe_swiglu_quant(y1, p.rows, d->I, masked ? counts : nullptr, masked ? d->max_m : 0,
@@ -399,16 +405,16 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
   }
   if (fuse_combine && masked)
     rc = gemm_masked_combine1(a2, sa2, d->w2, d->w2_s, counts, d->E, d->max_m, d->H, d->I, rowsrc,
-                              d->topk_w, d->out, d->H, gflags, d->err, st);
+                              d->topk_w, d->out, d->H, g2flags, d->err, st);
   else if (fuse_combine)
     rc = gemm_contig_combine1(a2, d->I, sa2, p.s_ld2, d->w2, d->w2_s, offsets, mind, p.rows, d->E, d->H,
-                              d->I, rowsrc, d->topk_w, d->out, d->H, gflags, d->err, st);
+                              d->I, rowsrc, d->topk_w, d->out, d->H, g2flags, d->err, st);
   else if (masked)
     rc = moe_gemm_fp8_masked(a2, sa2, d->w2, d->w2_s, counts, d->E, d->max_m, d->H, d->I,
-                             d->expected_m, y2, gflags, d->err, stream);
+                             d->expected_m, y2, g2flags, d->err, stream);
   else
     rc = moe_gemm_fp8_contig(a2, d->I, sa2, p.s_ld2, d->w2, d->w2_s, offsets, mind, p.rows, d->E,
-                             d->H, d->I, y2, d->H, gflags, d->err, stream);
+                             d->H, d->I, y2, d->H, g2flags, d->err, stream);
   if (rc) return rc;
   if ((rc = mark(5))) return rc;
   if (!fuse_combine &&

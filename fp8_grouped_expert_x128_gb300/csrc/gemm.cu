@@ -132,14 +132,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  // the local set-up above overlaps the previous kernel; the schedule reads
-  // the counts / offsets it wrote
-  grid_dependency_wait();
-  grid_launch_dependents();
+  // The local set-up above overlaps the previous kernel.  The schedule reads
+  // the counts / offsets: after waiting for that kernel, or before it when the
+  // caller says they were complete earlier (MOE_GEMM_EARLY_WEIGHTS), and then
+  // the producer also issues its first stages' weight tiles before waiting.
+  const bool early = (p.flags & MOE_GEMM_EARLY_WEIGHTS) != 0;
+  if (!early) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+  }
   if (warp == 0) build_schedule(p, sched, n_tiles);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  const bool early_producer = early && warp == 0 && lane == 0 && !(p.flags & MOE_GEMM_DEBUG_STALL);
+  if (early && !early_producer) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+  }
   const uint32_t tmem_base = *tmem_slot;
   const int total = sched.tile0[p.E];
   if (warp < kEpiWarp0) {
@@ -150,28 +160,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       TileCursor cur;
       bool ok = true;
+      // plain: 256 consecutive weight rows; SwiGLU: gate rows then the up rows
+      // of the same 128 intermediate columns
+      auto load_b = [&](uint32_t s, int kb, int b_row) {
+        tma_load_2d(smem_u32(b_tiles + s * kBTileBytes), &tmB, full0 + 8 * s, kb * BK, b_row);
+        if (kSwiGLU)
+          tma_load_2d(smem_u32(b_tiles + s * kBTileBytes + 128 * BK), &tmB, full0 + 8 * s, kb * BK, b_row + I2);
+      };
+      auto b_row_of = [&](int e, int l) {
+        return kSwiGLU ? e * p.N + (l % n_tiles) * 128 : e * p.N + (l % n_tiles) * BN;
+      };
+      // early: the weight tiles of the first kStages k-blocks (stages still
+      // empty), each stage expecting its A tile too, then the wait
+      uint32_t pre = 0;
+      if (early_producer) {
+        TileCursor c0;
+        for (int t = blockIdx.x; t < total && pre < static_cast<uint32_t>(kStages); t += gridDim.x) {
+          c0.seek(sched, t);
+          const int b_row = b_row_of(c0.e, t - sched.tile0[c0.e]);
+          for (int kb = 0; kb < KB && pre < static_cast<uint32_t>(kStages); ++kb, ++pre) {
+            mbar_arrive_expect_tx(full0 + 8 * pre, kStageBytes);
+            load_b(pre, kb, b_row);
+          }
+        }
+        grid_dependency_wait();
+        grid_launch_dependents();
+      }
       for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
         cur.seek(sched, t);
         const int l = t - sched.tile0[cur.e];
         const int a_row = sched.rbase[cur.e] + (l / n_tiles) * BM;
-        // plain: 256 consecutive weight rows; SwiGLU: gate rows then the up rows
-        // of the same 128 intermediate columns
-        const int b_row = kSwiGLU ? cur.e * p.N + (l % n_tiles) * 128 : cur.e * p.N + (l % n_tiles) * BN;
+        const int b_row = b_row_of(cur.e, l);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+          if (it < pre) {   // weights already on their way
+            tma_load_2d(smem_u32(a_tiles + s * kATileBytes), &tmA, full0 + 8 * s, kb * BK, a_row);
+            continue;
+          }
           if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, p.err, p.wait_limit_ns)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(full0 + 8 * s, kStageBytes);
           tma_load_2d(smem_u32(a_tiles + s * kATileBytes), &tmA, full0 + 8 * s, kb * BK, a_row);
-          if (kSwiGLU) {
-            tma_load_2d(smem_u32(b_tiles + s * kBTileBytes), &tmB, full0 + 8 * s, kb * BK, b_row);
-            tma_load_2d(smem_u32(b_tiles + s * kBTileBytes + 128 * BK), &tmB, full0 + 8 * s, kb * BK,
-                        b_row + I2);
-          } else {
-            tma_load_2d(smem_u32(b_tiles + s * kBTileBytes), &tmB, full0 + 8 * s, kb * BK, b_row);
-          }
+          load_b(s, kb, b_row);
         }
       }
       if (!ok) {
@@ -889,7 +921,7 @@ __device__ void build_schedule_wm(const GemmArgs& p, const Sched& s, int nblk) {
   int local = 0;
   bool overflow = false, bad = false;
   for (int e = e0; e < e1; ++e) {
-    int c = p.counts[e];
+    int c = __ldcg(p.counts + e);   // from L2: may be read before the grid dependency wait
     if (c > p.max_m) { overflow = true; c = p.max_m; }
     if (c < 0) { bad = true; c = 0; }
     s.rbase[e] = e * p.max_m;
@@ -960,12 +992,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  grid_dependency_wait();
-  grid_launch_dependents();
+  // the schedule reads the counts after waiting for the previous kernel, or
+  // before it with MOE_GEMM_EARLY_WEIGHTS (then the producer also issues its
+  // first stages' weight tiles before waiting)
+  const bool early = (p.flags & MOE_GEMM_EARLY_WEIGHTS) != 0;
+  if (!early) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+  }
   if (warp == 0) build_schedule_wm<BNT>(p, sched, nblk);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  const bool early_producer = early && warp == 0 && lane == 0 && !(p.flags & MOE_GEMM_DEBUG_STALL);
+  if (early && !early_producer) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+  }
   const uint32_t tmem_base = *tmem_slot;
   const int total = sched.tile0[p.E];
   if (warp < kEpiWarp0) {
@@ -977,39 +1020,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       TileCursor cur;
       bool ok = true;
+      struct Tile {
+        int e, j, nb, ncols, t_row, w_row;
+      };
+      auto tile_of = [&](int t, TileCursor& c) {
+        c.seek(sched, t);
+        Tile tl;
+        tl.e = c.e;
+        const int l = t - sched.tile0[tl.e];
+        tl.j = l / nblk;
+        tl.nb = l % nblk;
+        tl.ncols = (min(BNT, sched.rext[tl.e] - tl.j * BNT) + 15) & ~15;
+        tl.t_row = sched.rbase[tl.e] + tl.j * BNT;
+        tl.w_row = tl.e * p.N + tl.nb * 128;
+        return tl;
+      };
+      // a stage's weight half: the weight tile and the weight block's scale
+      // (a 4-byte cp.async that arrives on the stage's barrier), with the
+      // stage's whole byte count expected
+      auto issue_w = [&](uint32_t s, int kb, const Tile& tl) {
+        const uint32_t st_base = smem_u32(smem + s * C::kStage);
+        mbar_arrive_expect_tx(full0 + 8 * s, C::kWBytes + tl.ncols * BK + tl.ncols * 4);
+        tma_load_2d_hint(st_base, &tmW, full0 + 8 * s, kb * BK, tl.w_row, pol_w);
+        cp_async_4(st_base + C::kOffSb, p.sB + (static_cast<int64_t>(tl.e) * nblk + tl.nb) * KB + kb, 4u);
+        cp_async_mbar_arrive(full0 + 8 * s);
+      };
+      // its token half: the token scales (ncols floats, 16-byte aligned since
+      // max_m and the tile start are multiples of 16) and the token rows
+      // [0, ncols) in boxes of 128 while they last, then at most one each of
+      // 64, 32 and 16 (ncols is a multiple of 16)
+      auto issue_t = [&](uint32_t s, int kb, const Tile& tl) {
+        const uint32_t st_base = smem_u32(smem + s * C::kStage);
+        bulk_g2s(st_base + C::kOffSa, p.sA + (static_cast<int64_t>(tl.e) * KB + kb) * p.max_m + tl.j * BNT,
+                 tl.ncols * 4, full0 + 8 * s);
+        for (int r = 0; r < tl.ncols;) {
+          const int left = tl.ncols - r;
+          const int i = left >= 128 ? 3 : left >= 64 ? 2 : left >= 32 ? 1 : 0;
+          tma_load_2d(st_base + C::kWBytes + r * BK, &tmT.box[i], full0 + 8 * s, kb * BK, tl.t_row + r);
+          r += 16 << i;
+        }
+      };
+      uint32_t pre = 0;   // stages whose weight half went out before the wait
+      if (early_producer) {
+        TileCursor c0;
+        for (int t = blockIdx.x; t < total && pre < static_cast<uint32_t>(C::kStages); t += gridDim.x) {
+          const Tile tl = tile_of(t, c0);
+          for (int kb = 0; kb < KB && pre < static_cast<uint32_t>(C::kStages); ++kb, ++pre) issue_w(pre, kb, tl);
+        }
+        grid_dependency_wait();
+        grid_launch_dependents();
+      }
       for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-        cur.seek(sched, t);
-        const int e = cur.e;
-        const int l = t - sched.tile0[e];
-        const int j = l / nblk, nb = l % nblk;
-        const int ntok = min(BNT, sched.rext[e] - j * BNT);
-        const int ncols = (ntok + 15) & ~15;
-        const int t_row = sched.rbase[e] + j * BNT;
-        const int w_row = e * p.N + nb * 128;
+        const Tile tl = tile_of(t, cur);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1;
-          if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, p.err, p.wait_limit_ns)) {
-            ok = false;
-            break;
+          if (it >= pre) {
+            if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, p.err, p.wait_limit_ns)) {
+              ok = false;
+              break;
+            }
+            issue_w(s, kb, tl);
           }
-          const uint32_t st_base = smem_u32(smem + s * C::kStage);
-          mbar_arrive_expect_tx(full0 + 8 * s, C::kWBytes + ncols * BK + ncols * 4);
-          tma_load_2d_hint(st_base, &tmW, full0 + 8 * s, kb * BK, w_row, pol_w);
-          // this k-block's scales: the tile's token scales (ncols floats, 16-byte
-          // aligned since max_m and the tile start are multiples of 16) and the
-          // weight block's scale
-          bulk_g2s(st_base + C::kOffSa, p.sA + (static_cast<int64_t>(e) * KB + kb) * p.max_m + j * BNT, ncols * 4,
-                   full0 + 8 * s);
-          cp_async_4(st_base + C::kOffSb, p.sB + (static_cast<int64_t>(e) * nblk + nb) * KB + kb, 4u);
-          cp_async_mbar_arrive(full0 + 8 * s);
-          // rows [0, ncols) in boxes of 128 while they last, then at most one
-          // each of 64, 32 and 16 (ncols is a multiple of 16)
-          for (int r = 0; r < ncols;) {
-            const int left = ncols - r;
-            const int i = left >= 128 ? 3 : left >= 64 ? 2 : left >= 32 ? 1 : 0;
-            tma_load_2d(st_base + C::kWBytes + r * BK, &tmT.box[i], full0 + 8 * s, kb * BK, t_row + r);
-            r += 16 << i;
-          }
+          issue_t(s, kb, tl);
         }
       }
       if (!ok) {

@@ -157,12 +157,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  grid_dependency_wait();
-  grid_launch_dependents();
+  // the schedule reads the counts / offsets after waiting for the previous
+  // kernel, or before it with MOE_GEMM_EARLY_WEIGHTS (then the producer also
+  // issues its first stages' weight tiles and weight scales before waiting)
+  const bool early = (p.flags & MOE_GEMM_EARLY_WEIGHTS) != 0;
+  if (!early) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+  }
   if (warp == 0) build_schedule(p, sched, n_tiles);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  const bool early_producer = early && warp == 0 && lane == 0 && !(p.flags & MOE_GEMM_DEBUG_STALL);
+  if (early && !early_producer) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+  }
   const uint32_t tmem_base = *tmem_slot;
   const int total = sched.tile0[p.E];
   // No register split here: the epilogue holds one tile's 128 fp32 values per
@@ -174,37 +185,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t it = 0;
         TileCursor cur;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-          cur.seek(sched, t);
-          const int e = cur.e;
+        struct Tile {
+          int a_row, b_row;
+          const uint32_t* sfa;   // the tile's 128-row chunk of its scale group
+          const uint32_t* sfb0;  // the one or two 128-row weight blocks of its columns
+          const uint32_t* sfb1;
+        };
+        auto tile_of = [&](int t, TileCursor& c) {
+          c.seek(sched, t);
+          const int e = c.e;
           const int l = t - sched.tile0[e];
           const int mt = l / n_tiles, nt = l % n_tiles;
           const bool half = (nt == n_tiles - 1) && (p.N % BN) != 0;
-          const int a_row = sched.rbase[e] + mt * BM;
-          const int b_row = e * p.N + nt * BN;
-          // the tile's scale records: its 128-row chunk of its scale group, and
-          // the one or two 128-row weight blocks of its columns
-          const int64_t grp = a_row / p.sf_G, r_in = a_row - grp * p.sf_G;
-          const uint32_t* sfa = p.sfA + (grp * p.KG * p.sf_NC + r_in / BM) * 128;
-          const uint32_t* sfb0 = p.sfB + (static_cast<int64_t>(e) * NB + 2 * nt) * p.KG * 32;
-          const uint32_t* sfb1 = half ? sfb0 : sfb0 + static_cast<int64_t>(p.KG) * 32;
+          Tile tl;
+          tl.a_row = sched.rbase[e] + mt * BM;
+          tl.b_row = e * p.N + nt * BN;
+          const int64_t grp = tl.a_row / p.sf_G, r_in = tl.a_row - grp * p.sf_G;
+          tl.sfa = p.sfA + (grp * p.KG * p.sf_NC + r_in / BM) * 128;
+          tl.sfb0 = p.sfB + (static_cast<int64_t>(e) * NB + 2 * nt) * p.KG * 32;
+          tl.sfb1 = half ? tl.sfb0 : tl.sfb0 + static_cast<int64_t>(p.KG) * 32;
+          return tl;
+        };
+        // a stage's weight half (the B tile and, every fourth k-block, the
+        // weight scale records) with the stage's whole byte count expected ...
+        auto issue_b = [&](uint32_t s, int kb, const Tile& tl) {
+          const bool sf = (kb & 3) == 0;
+          const uint32_t st = smem_u32(smem + s * kBsStage);
+          mbar_arrive_expect_tx(full0 + 8 * s, kBsA + kBsB + (sf ? kBsSfA + 2 * kBsSfB : 0));
+          tma_load_2d(st + kBsA, &tmB, full0 + 8 * s, kb * BK, tl.b_row);
+          if (sf) {
+            bulk_g2s(st + kBsOffSfB0, tl.sfb0 + (kb >> 2) * 32, kBsSfB, full0 + 8 * s);
+            bulk_g2s(st + kBsOffSfB1, tl.sfb1 + (kb >> 2) * 32, kBsSfB, full0 + 8 * s);
+          }
+        };
+        // ... and its activation half (the A tile and the activation scale chunk)
+        auto issue_a = [&](uint32_t s, int kb, const Tile& tl) {
+          const uint32_t st = smem_u32(smem + s * kBsStage);
+          tma_load_2d(st, &tmA, full0 + 8 * s, kb * BK, tl.a_row);
+          if ((kb & 3) == 0)
+            bulk_g2s(st + kBsOffSfA, tl.sfa + static_cast<int64_t>(kb >> 2) * p.sf_NC * 128, kBsSfA, full0 + 8 * s);
+        };
+        uint32_t pre = 0;   // stages whose weight half went out before the wait
+        if (early_producer) {
+          TileCursor c0;
+          for (int t = blockIdx.x; t < total && pre < static_cast<uint32_t>(kBsStages); t += gridDim.x) {
+            const Tile tl = tile_of(t, c0);
+            for (int kb = 0; kb < KB && pre < static_cast<uint32_t>(kBsStages); ++kb, ++pre) issue_b(pre, kb, tl);
+          }
+          grid_dependency_wait();
+          grid_launch_dependents();
+        }
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+          const Tile tl = tile_of(t, cur);
           for (int kb = 0; kb < KB; ++kb, ++it) {
             const uint32_t s = it % kBsStages, ph = (it / kBsStages) & 1;
-            if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, p.err, p.wait_limit_ns)) {
-              ok = false;
-              break;
+            if (it >= pre) {
+              if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, p.err, p.wait_limit_ns)) {
+                ok = false;
+                break;
+              }
+              issue_b(s, kb, tl);
             }
-            const bool sf = (kb & 3) == 0;
-            const uint32_t st = smem_u32(smem + s * kBsStage);
-            mbar_arrive_expect_tx(full0 + 8 * s, kBsA + kBsB + (sf ? kBsSfA + 2 * kBsSfB : 0));
-            tma_load_2d(st, &tmA, full0 + 8 * s, kb * BK, a_row);
-            tma_load_2d(st + kBsA, &tmB, full0 + 8 * s, kb * BK, b_row);
-            if (sf) {
-              const int g = kb >> 2;
-              bulk_g2s(st + kBsOffSfA, sfa + static_cast<int64_t>(g) * p.sf_NC * 128, kBsSfA, full0 + 8 * s);
-              bulk_g2s(st + kBsOffSfB0, sfb0 + g * 32, kBsSfB, full0 + 8 * s);
-              bulk_g2s(st + kBsOffSfB1, sfb1 + g * 32, kBsSfB, full0 + 8 * s);
-            }
+            issue_a(s, kb, tl);
           }
         }
         if (!ok) {
@@ -412,7 +454,7 @@ __device__ void build_schedule_wm_bs(const BsArgs& p, const Sched& s, int nblk) 
   int local = 0;
   bool overflow = false, bad = false;
   for (int e = e0; e < e1; ++e) {
-    int c = p.counts[e];
+    int c = __ldcg(p.counts + e);   // from L2: may be read before the grid dependency wait
     if (c > p.max_m) { overflow = true; c = p.max_m; }
     if (c < 0) { bad = true; c = 0; }
     s.rbase[e] = e * p.max_m;
@@ -480,12 +522,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  grid_dependency_wait();
-  grid_launch_dependents();
+  // the schedule reads the counts after waiting for the previous kernel, or
+  // before it with MOE_GEMM_EARLY_WEIGHTS (then the producer also issues its
+  // first stages' weight tiles and weight scale records before waiting)
+  const bool early = (p.flags & MOE_GEMM_EARLY_WEIGHTS) != 0;
+  if (!early) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+  }
   if (warp == 0) build_schedule_wm_bs<BNT>(p, sched, nblk);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  const bool early_producer = early && warp == 0 && lane == 0 && !(p.flags & MOE_GEMM_DEBUG_STALL);
+  if (early && !early_producer) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+  }
   const uint32_t tmem_base = *tmem_slot;
   const int total = sched.tile0[p.E];
   if (warp < kEpiWarp0) {
@@ -496,38 +549,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t it = 0;
         TileCursor cur;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-          cur.seek(sched, t);
-          const int e = cur.e;
+        struct Tile {
+          int ncols, t_row, w_row;
+          const uint32_t* sfw;   // the weight block's scale records
+          const uint32_t* sft;   // the tokens' packed scale chunk
+        };
+        auto tile_of = [&](int t, TileCursor& c) {
+          c.seek(sched, t);
+          const int e = c.e;
           const int l = t - sched.tile0[e];
           const int j = l / nblk, nb = l % nblk;
-          const int ntok = min(BNT, sched.rext[e] - j * BNT);
-          const int ncols = (ntok + 15) & ~15;
-          const int t_row = sched.rbase[e] + j * BNT;
-          const int w_row = e * p.N + nb * 128;
-          const uint32_t* sfw = p.sfB + (static_cast<int64_t>(e) * nblk + nb) * p.KG * 32;
-          const uint32_t* sft = p.sfA + (static_cast<int64_t>(e) * p.KG * p.sf_NC + (j * BNT) / 128) * 128;
+          Tile tl;
+          tl.ncols = (min(BNT, sched.rext[e] - j * BNT) + 15) & ~15;
+          tl.t_row = sched.rbase[e] + j * BNT;
+          tl.w_row = e * p.N + nb * 128;
+          tl.sfw = p.sfB + (static_cast<int64_t>(e) * nblk + nb) * p.KG * 32;
+          tl.sft = p.sfA + (static_cast<int64_t>(e) * p.KG * p.sf_NC + (j * BNT) / 128) * 128;
+          return tl;
+        };
+        // a stage's weight half (the weight tile and, every fourth k-block,
+        // its scale record) with the stage's whole byte count expected ...
+        auto issue_w = [&](uint32_t s, int kb, const Tile& tl) {
+          const bool sf = (kb & 3) == 0;
+          const uint32_t st = smem_u32(smem + s * C::kStage);
+          mbar_arrive_expect_tx(full0 + 8 * s, C::kW + tl.ncols * BK + (sf ? 128 + 512 : 0));
+          tma_load_2d_hint(st, &tmW, full0 + 8 * s, kb * BK, tl.w_row, pol_w);
+          if (sf) bulk_g2s(st + C::kOffSfW, tl.sfw + (kb >> 2) * 32, 128, full0 + 8 * s);
+        };
+        // ... and its token half (the token rows and their scale chunk)
+        auto issue_t = [&](uint32_t s, int kb, const Tile& tl) {
+          const uint32_t st = smem_u32(smem + s * C::kStage);
+          for (int r = 0; r < tl.ncols;) {
+            const int left = tl.ncols - r;
+            const int i = left >= 128 ? 3 : left >= 64 ? 2 : left >= 32 ? 1 : 0;
+            tma_load_2d(st + C::kW + r * BK, &tmT.box[i], full0 + 8 * s, kb * BK, tl.t_row + r);
+            r += 16 << i;
+          }
+          if ((kb & 3) == 0)
+            bulk_g2s(st + C::kOffSfT, tl.sft + static_cast<int64_t>(kb >> 2) * p.sf_NC * 128, 512, full0 + 8 * s);
+        };
+        uint32_t pre = 0;   // stages whose weight half went out before the wait
+        if (early_producer) {
+          TileCursor c0;
+          for (int t = blockIdx.x; t < total && pre < static_cast<uint32_t>(C::kStages); t += gridDim.x) {
+            const Tile tl = tile_of(t, c0);
+            for (int kb = 0; kb < KB && pre < static_cast<uint32_t>(C::kStages); ++kb, ++pre) issue_w(pre, kb, tl);
+          }
+          grid_dependency_wait();
+          grid_launch_dependents();
+        }
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+          const Tile tl = tile_of(t, cur);
           for (int kb = 0; kb < KB; ++kb, ++it) {
             const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1;
-            if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, p.err, p.wait_limit_ns)) {
-              ok = false;
-              break;
+            if (it >= pre) {
+              if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, p.err, p.wait_limit_ns)) {
+                ok = false;
+                break;
+              }
+              issue_w(s, kb, tl);
             }
-            const bool sf = (kb & 3) == 0;
-            const uint32_t st = smem_u32(smem + s * C::kStage);
-            mbar_arrive_expect_tx(full0 + 8 * s, C::kW + ncols * BK + (sf ? 128 + 512 : 0));
-            tma_load_2d_hint(st, &tmW, full0 + 8 * s, kb * BK, w_row, pol_w);
-            for (int r = 0; r < ncols;) {
-              const int left = ncols - r;
-              const int i = left >= 128 ? 3 : left >= 64 ? 2 : left >= 32 ? 1 : 0;
-              tma_load_2d(st + C::kW + r * BK, &tmT.box[i], full0 + 8 * s, kb * BK, t_row + r);
-              r += 16 << i;
-            }
-            if (sf) {
-              const int g = kb >> 2;
-              bulk_g2s(st + C::kOffSfW, sfw + g * 32, 128, full0 + 8 * s);
-              bulk_g2s(st + C::kOffSfT, sft + static_cast<int64_t>(g) * p.sf_NC * 128, 512, full0 + 8 * s);
-            }
+            issue_t(s, kb, tl);
           }
         }
         if (!ok) {

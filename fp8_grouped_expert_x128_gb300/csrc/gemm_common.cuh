@@ -123,14 +123,14 @@ __device__ void build_schedule(const Args& p, const Sched& s, int n_tiles) {
   for (int e = e0; e < e1; ++e) {
     int rb, rx;
     if (p.layout == MOE_LAYOUT_MASKED) {
-      int c = p.counts[e];
+      int c = __ldcg(p.counts + e);   // from L2: may be read before the grid dependency wait
       if (c > p.max_m) { overflow = true; c = p.max_m; }
       if (c < 0) { bad = true; c = 0; }
       rb = e * p.max_m;
       rx = c;
     } else {
-      rb = p.offsets[e];
-      rx = p.offsets[e + 1] - rb;
+      rb = __ldcg(p.offsets + e);
+      rx = __ldcg(p.offsets + e + 1) - rb;
       // a segment must start on a 128-row boundary and lie inside the
       // M_capacity rows of A, D and m_indices; otherwise it is skipped
       if (rb < 0 || (rb % BM) != 0 || rx < 0 || (rx % BM) != 0 ||

@@ -84,6 +84,17 @@ extern "C" {
                                          quantisations take power-of-two scales, packed for
                                          the block-scaled GEMMs, which read the weights'
                                          packed scales w13_sf / w2_sf                     */
+#define MOE_GEMM_EARLY_WEIGHTS 0x20   /* the routing arrays the GEMM reads (masked counts;
+                                         contiguous offsets and m_indices) were complete
+                                         before the kernel launched just before this call on
+                                         the stream began, i.e. that kernel does not write
+                                         them: the GEMM then builds its tile schedule and
+                                         starts streaming weight tiles (and their scales)
+                                         before it waits for that kernel (programmatic
+                                         dependent launch), and loads the activations and
+                                         their scales after.  moe_ffn sets it for both of
+                                         its GEMMs.  Wrong results if the arrays are written
+                                         by the immediately preceding kernel.             */
 #define MOE_GEMM_DEBUG_STALL 0x100    /* test only: the TMA producer never issues, so the
                                          consumer's bounded wait expires and the call
                                          reports MOE_DEV_TIMEOUT (no hang, no trap)      */

@@ -176,3 +176,18 @@ def test_ue8m0_scale_rule_matches_the_oracle(so):
         s, b = moe.moe_ue8m0_scale(float(a))
         assert np.float32(s) == rs and b == int(rb), (a, s, b, rs, rb)
     assert moe.moe_ue8m0_scale(float("inf")) == (float("inf"), 0xFF)
+
+
+def test_binding_constants_equal_the_header(so):
+    """Every MOE_* value the Python binding names is the header's #define."""
+    import fp8_grouped_expert_x128_gb300 as lib
+    text = open(os.path.join(ROOT, "include", "moe_fp8.h")).read()
+    defines = {m.group(1): int(m.group(2), 0)
+               for m in re.finditer(r"^#define\s+(MOE_\w+)\s+\(?(-?(?:0x[0-9a-fA-F]+|\d+))\)?", text, flags=re.M)}
+    named = [n for n in dir(lib) if n.startswith("MOE_") and isinstance(getattr(lib, n), int)]
+    assert len(named) >= 10
+    for n in named:
+        assert n in defines, f"{n} is not in the header"
+        assert getattr(lib, n) == defines[n], n
+    for flag in ("MOE_GEMM_EARLY_WEIGHTS", "MOE_FFN_UE8M0", "MOE_QUANT_UE8M0", "MOE_COMBINE_ACCUMULATE"):
+        assert flag in named

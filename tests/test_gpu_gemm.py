@@ -350,3 +350,38 @@ def test_gemm_pair_random_scales(lib):
     assert st == 0
     ref, valid = oracle.gemm_masked(A, sA, B, sB, counts)
     _check_masked(got, ref, valid, "pair masked random")
+
+
+@pytest.mark.parametrize("K", [256, 640])
+@pytest.mark.parametrize("flags,hint", MASKED_KERNELS, ids=MASKED_IDS)
+def test_gemm_early_weights_flag_is_bit_identical_masked(lib, flags, hint, K):
+    """MOE_GEMM_EARLY_WEIGHTS (counts complete before the previous kernel) only
+    moves the schedule and the first stages' weight copies ahead of the grid
+    dependency wait: the result is the same bits.  K = 256 spreads the early
+    stages over several tiles, K = 640 keeps them in one."""
+    rng = np.random.default_rng(17)
+    E, max_m, N = 3, 256, 384
+    counts = [200, 0, 77]
+    A, B = rand_codes(rng, (E, max_m, K)), rand_codes(rng, (E, N, K))
+    sA = np.exp(rng.uniform(-6, 2, (E, K // 128, max_m))).astype(np.float32)
+    sB = np.exp(rng.uniform(-6, 2, (E, N // 128, K // 128))).astype(np.float32)
+    ref, st0 = _masked(lib, A, sA, B, sB, counts, flags=flags, expected_m=hint)
+    got, st1 = _masked(lib, A, sA, B, sB, counts, flags=flags | lib.MOE_GEMM_EARLY_WEIGHTS, expected_m=hint)
+    assert st0 == 0 and st1 == 0
+    assert np.array_equal(got, ref)
+
+
+def test_gemm_early_weights_flag_is_bit_identical_contig(lib):
+    rng = np.random.default_rng(18)
+    N, K, M_cap = 384, 384, 768
+    offsets = [0, 256, 256, 640]
+    mi = -np.ones(M_cap, np.int64)
+    mi[0:130] = 0
+    mi[256:556] = 2
+    A, B = rand_codes(rng, (M_cap, K)), rand_codes(rng, (3, N, K))
+    sA = np.exp(rng.uniform(-6, 2, (K // 128, M_cap))).astype(np.float32)
+    sB = np.exp(rng.uniform(-6, 2, (3, N // 128, K // 128))).astype(np.float32)
+    ref, st0 = _contig(lib, A, sA, B, sB, offsets, mi)
+    got, st1 = _contig(lib, A, sA, B, sB, offsets, mi, flags=lib.MOE_GEMM_EARLY_WEIGHTS)
+    assert st0 == 0 and st1 == 0
+    assert np.array_equal(got, ref)

@@ -55,14 +55,14 @@ def _masked(lib, A, sA, B, sB, counts, flags=0, hint=0):
     return bits(g.t), st
 
 
-def _contig(lib, A, sA, B, sB, offsets, mi):
+def _contig(lib, A, sA, B, sB, offsets, mi, flags=0):
     M_cap, K = A.shape
     N = B.shape[1]
     g = Guarded((M_cap, N), torch.bfloat16, SENTINEL_BF16)
     err = lib.new_error_word()
     lib.moe_gemm_fp8_contig_ue8m0(to_dev(A), _i32(_sfa_contig(sA, M_cap)), M_cap, to_dev(B),
                                   _i32(oracle.pack_ue8m0_weight(sB)), to_dev(np.asarray(offsets, np.int32)),
-                                  to_dev(np.asarray(mi, np.int32)), g.t, err=err)
+                                  to_dev(np.asarray(mi, np.int32)), g.t, flags=flags, err=err)
     st, _ = lib.moe_read_device_status(err)
     assert g.intact(), "a store landed past the end of D"
     return bits(g.t), st
@@ -241,3 +241,36 @@ def test_all_experts_decode_shape_weights_m(lib):
     ref, valid = oracle.gemm_masked(A, sA, B, sB, counts)
     check_tol(got[valid], ref[valid], "ue8m0 all-experts shape")
     assert (got[~valid] == SENTINEL_BF16).all()
+
+
+@pytest.mark.parametrize("K", [256, 640])
+@pytest.mark.parametrize("flags,hint", KERNELS, ids=KERNEL_IDS)
+def test_early_weights_flag_is_bit_identical_masked(lib, flags, hint, K):
+    """MOE_GEMM_EARLY_WEIGHTS (counts complete before the previous kernel) only
+    moves the schedule and the first stages' weight copies ahead of the grid
+    dependency wait: the result is the same bits.  K = 256 spreads the early
+    stages over several tiles, K = 640 keeps them in one."""
+    rng = np.random.default_rng(47)
+    E, max_m, N = 3, 256, 384
+    counts = [200, 0, 77]
+    A, B = rand_codes(rng, (E, max_m, K)), rand_codes(rng, (E, N, K))
+    sA, sB = _pow2(rng, (E, K // 128, max_m), -6, 2), _pow2(rng, (E, N // 128, K // 128), -6, 2)
+    ref, st0 = _masked(lib, A, sA, B, sB, counts, flags=flags, hint=hint)
+    got, st1 = _masked(lib, A, sA, B, sB, counts, flags=flags | lib.MOE_GEMM_EARLY_WEIGHTS, hint=hint)
+    assert st0 == 0 and st1 == 0
+    assert np.array_equal(got, ref)
+
+
+def test_early_weights_flag_is_bit_identical_contig(lib):
+    rng = np.random.default_rng(48)
+    N, K, M_cap = 384, 384, 768
+    offsets = [0, 256, 256, 640]
+    mi = -np.ones(M_cap, np.int64)
+    mi[0:130] = 0
+    mi[256:556] = 2
+    A, B = rand_codes(rng, (M_cap, K)), rand_codes(rng, (3, N, K))
+    sA, sB = _pow2(rng, (K // 128, M_cap), -6, 2), _pow2(rng, (3, N // 128, K // 128), -6, 2)
+    ref, st0 = _contig(lib, A, sA, B, sB, offsets, mi)
+    got, st1 = _contig(lib, A, sA, B, sB, offsets, mi, flags=lib.MOE_GEMM_EARLY_WEIGHTS)
+    assert st0 == 0 and st1 == 0
+    assert np.array_equal(got, ref)
