@@ -252,3 +252,33 @@ def test_ffn_refuses_pageable_host_buffers(lib):
         with pytest.raises(lib.MoeError) as ei:
             lib.moe_ffn(desc, ws)
         assert ei.value.status == lib.MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("reading", ["fp32", "ue8m0"])
+@pytest.mark.parametrize("layout", ["masked", "contig"])
+@pytest.mark.parametrize("case", ["no_tokens", "no_local_slot"])
+def test_ffn_degenerate_batches(lib, case, layout, reading):
+    """The degenerate batches of the method, through moe_ffn on the tiny config
+    in both layouts and both scale readings: no tokens at all (T = 0: the call
+    succeeds and writes nothing), and tokens none of whose slots is local (every
+    output row is the empty combine, +0.0, and no expert runs)."""
+    wl = build_workload("c1", ue8m0=reading == "ue8m0")
+    if layout == "contig":
+        wl["cfg"] = dataclasses.replace(wl["cfg"], layout="contig")
+        wl["layout"] = lib.MOE_LAYOUT_CONTIG
+    H, E = wl["cfg"].H, wl["cfg"].E
+    ids = wl["topk_ids"]
+    if case == "no_local_slot":
+        ids = (ids - wl["routing"]["expert_begin"]) % E + wl["routing"]["expert_begin"] + E   # all remote
+    T = 0 if case == "no_tokens" else wl["T"]
+    g = Guarded((T, H), torch.bfloat16, SENTINEL_BF16)
+    err = lib.new_error_word()
+    # row slices of the (contiguous) inputs keep a valid base pointer at T = 0
+    desc = make_desc(wl, g.t, err=err, x=wl["x"][:T], ids=ids[:T], w=wl["topk_w"][:T])
+    ws = lib.alloc_workspace(desc)
+    lib.moe_ffn(desc, ws)
+    st, _ = lib.moe_read_device_status(err)
+    assert st == lib.MOE_OK
+    assert g.intact(), "moe_ffn wrote past out"
+    if T:
+        assert (bits(g.t) == 0).all(), "a token with no local slot must come out +0.0"
