@@ -259,11 +259,13 @@ FfnFusion ffn_fusion(const moe_ffn_desc* d, bool out_on_host) {
 
 extern "C" int moe_ffn_kernel_count(const moe_ffn_desc* d) {
   FfnPlan p;
-  if (plan_ffn(d, &p) != MOE_OK || d->out == nullptr) return MOE_ERR_INVALID_ARG;
+  if (plan_ffn(d, &p) != MOE_OK) return MOE_ERR_INVALID_ARG;
+  if (d->T == 0) return 0;                                                // an empty batch launches nothing
+  if (d->out == nullptr) return MOE_ERR_INVALID_ARG;
   bool out_on_host = false;
   if (int rc = check_placement(d->out, true, &out_on_host)) return rc;
   const FfnFusion f = ffn_fusion(d, out_on_host);
-  int n = d->T == 0 ? 1 : 2;                                              // index pass (+ quant-scatter)
+  int n = 2;                                                              // index pass + quant-scatter
   n += f.swiglu ? 1 : 2;                                                  // GEMM1 (+ SwiGLU)
   n += 1;                                                                 // GEMM2
   n += f.combine ? 0 : 1;                                                 // combine
@@ -283,17 +285,24 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
   MOE_CHECK_ARG(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255) == 0);
   MOE_CHECK_ARG(workspace_bytes >= p.total);
   const bool ue8m0 = p.ue8m0;
-  MOE_CHECK_ARG(d->x && d->topk_ids && d->topk_w && d->w13 && d->w2 && d->out);
+  MOE_CHECK_ARG(d->w13 && d->w2);
   if (ue8m0)
     MOE_CHECK_ARG(d->w13_sf && d->w2_sf && aligned16(d->w13_sf) && aligned16(d->w2_sf));
   else
     MOE_CHECK_ARG(d->w13_s && d->w2_s);
+  // An empty batch (T = 0) reads and writes no token, so its token I/O may be
+  // null (as an empty framework tensor's is): nothing is launched, only the
+  // stage events are recorded.
+  const bool empty = d->T == 0;
+  if (!empty) MOE_CHECK_ARG(d->x && d->topk_ids && d->topk_w && d->out);
   if (int st = check_device()) return st;
-  const void* io[3] = {d->x, d->topk_ids, d->topk_w};
-  for (const void* ptr : io)
-    if (int rc = check_placement(ptr, true)) return rc;
   bool out_on_host = false;
-  if (int rc = check_placement(d->out, true, &out_on_host)) return rc;
+  if (!empty) {
+    const void* io[3] = {d->x, d->topk_ids, d->topk_w};
+    for (const void* ptr : io)
+      if (int rc = check_placement(ptr, true)) return rc;
+    if (int rc = check_placement(d->out, true, &out_on_host)) return rc;
+  }
   const void* on_device[5] = {d->w13, ue8m0 ? static_cast<const void*>(d->w13_sf) : d->w13_s, d->w2,
                               ue8m0 ? static_cast<const void*>(d->w2_sf) : d->w2_s, workspace};
   for (const void* ptr : on_device)
@@ -327,14 +336,19 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
     return MOE_OK;
   };
   int rc;
+  if (empty) {
+    for (int i = 0; i < 7; ++i)
+      if ((rc = mark(i))) return rc;
+    return MOE_OK;
+  }
   const int32_t gflags = d->gemm_flags & ~(MOE_FFN_FUSE_SWIGLU | MOE_FFN_UE8M0);
   const FfnFusion fusion = ffn_fusion(d, out_on_host);
   const bool fuse_combine = fusion.combine;
   // The routing arrays are written by the index kernel: two launches before
-  // GEMM1 when there are tokens (the quant-scatter runs in between) and more
-  // before GEMM2, so both GEMMs may build their schedule and start streaming
-  // weights before they wait for the kernel just ahead of them.
-  const int32_t g1flags = gflags | (d->T > 0 ? MOE_GEMM_EARLY_WEIGHTS : 0);
+  // GEMM1 (the quant-scatter runs in between; T > 0 here) and more before
+  // GEMM2, so both GEMMs may build their schedule and start streaming weights
+  // before they wait for the kernel just ahead of them.
+  const int32_t g1flags = gflags | MOE_GEMM_EARLY_WEIGHTS;
   const int32_t g2flags = gflags | MOE_GEMM_EARLY_WEIGHTS;
   // stages 1+2: routing index pass, then each routed token row is quantised
   // straight into its expert slot (no token-order FP8 copy in between)

@@ -386,7 +386,9 @@ int moe_combine(const uint16_t *Y2, int64_t ldy, int64_t y_rows,
  * (w13_s / w2_s are then not read), and MOE_FFN_FUSE_SWIGLU is ignored.
  */
 typedef struct moe_ffn_desc {
-  int64_t T;              /* tokens (rows of x and out)                 */
+  int64_t T;              /* tokens (rows of x and out); T = 0 is an
+                             empty batch: the token I/O may then be null
+                             and moe_ffn launches nothing               */
   int32_t H, I, k;        /* hidden, intermediate, routing slots/token  */
   int32_t expert_begin;   /* global id of local expert 0               */
   int32_t E;              /* local experts                              */

@@ -191,3 +191,23 @@ def test_binding_constants_equal_the_header(so):
         assert getattr(lib, n) == defines[n], n
     for flag in ("MOE_GEMM_EARLY_WEIGHTS", "MOE_FFN_UE8M0", "MOE_QUANT_UE8M0", "MOE_COMBINE_ACCUMULATE"):
         assert flag in named
+
+
+def test_empty_batch_launches_nothing(so):
+    """T = 0 is a valid empty batch: host-only, the plan launches no kernel and
+    the token I/O may be empty tensors (null pointers)."""
+    import torch
+    import fp8_grouped_expert_x128_gb300 as moe
+    E, H, I, k = 4, 256, 128, 2
+    x = torch.empty((0, H), dtype=torch.bfloat16)
+    ids = torch.empty((0, k), dtype=torch.int32)
+    w = torch.empty((0, k), dtype=torch.float32)
+    w13 = torch.zeros((E, 2 * I, H), dtype=torch.uint8)
+    w2 = torch.zeros((E, H, I), dtype=torch.uint8)
+    s13 = torch.ones((E, 2 * I // 128, H // 128))
+    s2 = torch.ones((E, H // 128, I // 128))
+    out = torch.empty((0, H), dtype=torch.bfloat16)
+    for layout in (moe.MOE_LAYOUT_MASKED, moe.MOE_LAYOUT_CONTIG):
+        d = moe.make_ffn_desc(x, ids, w, w13, s13, w2, s2, out, 0, E, layout, max_m=128)
+        assert moe.moe_ffn_kernel_count(d) == 0
+        assert moe.moe_ffn_workspace_size(d) > 0

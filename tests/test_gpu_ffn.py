@@ -259,9 +259,10 @@ def test_ffn_refuses_pageable_host_buffers(lib):
 @pytest.mark.parametrize("case", ["no_tokens", "no_local_slot"])
 def test_ffn_degenerate_batches(lib, case, layout, reading):
     """The degenerate batches of the method, through moe_ffn on the tiny config
-    in both layouts and both scale readings: no tokens at all (T = 0: the call
-    succeeds and writes nothing), and tokens none of whose slots is local (every
-    output row is the empty combine, +0.0, and no expert runs)."""
+    in both layouts and both scale readings: no tokens at all (T = 0, empty
+    token tensors whose pointers are null: the call succeeds, launches nothing
+    and writes nothing), and tokens none of whose slots is local (every output
+    row is the empty combine, +0.0, and no expert runs)."""
     wl = build_workload("c1", ue8m0=reading == "ue8m0")
     if layout == "contig":
         wl["cfg"] = dataclasses.replace(wl["cfg"], layout="contig")
@@ -273,9 +274,10 @@ def test_ffn_degenerate_batches(lib, case, layout, reading):
     T = 0 if case == "no_tokens" else wl["T"]
     g = Guarded((T, H), torch.bfloat16, SENTINEL_BF16)
     err = lib.new_error_word()
-    # row slices of the (contiguous) inputs keep a valid base pointer at T = 0
     desc = make_desc(wl, g.t, err=err, x=wl["x"][:T], ids=ids[:T], w=wl["topk_w"][:T])
     ws = lib.alloc_workspace(desc)
+    if T == 0:
+        assert lib.moe_ffn_kernel_count(desc) == 0
     lib.moe_ffn(desc, ws)
     st, _ = lib.moe_read_device_status(err)
     assert st == lib.MOE_OK
