@@ -224,6 +224,16 @@ struct FfnFusion {
   bool combine;   // single-slot combine in GEMM2's epilogue (no combine kernel)
 };
 
+// The index pass runs inside the quant-scatter kernel (no index kernel) for the
+// masked layout when there are few routing ids (each CTA scans the ids before
+// its token) and few slots per token.  Measured: the all-experts layer at
+// T = 1 / 64 gains 4 µs per step; at ~4000 ids (c2) the scans cost 7 µs more
+// than the index kernel they replace.
+constexpr int64_t kFuseIndexMaxIds = 1024;
+bool ffn_fuse_index(const moe_ffn_desc* d) {
+  return d->layout == MOE_LAYOUT_MASKED && d->T > 0 && d->T * d->k <= kFuseIndexMaxIds && d->k <= 16;
+}
+
 FfnFusion ffn_fusion(const moe_ffn_desc* d, bool out_on_host) {
   const bool masked = d->layout == MOE_LAYOUT_MASKED;
   const int32_t gflags = d->gemm_flags & ~MOE_FFN_FUSE_SWIGLU;
@@ -265,7 +275,7 @@ extern "C" int moe_ffn_kernel_count(const moe_ffn_desc* d) {
   bool out_on_host = false;
   if (int rc = check_placement(d->out, true, &out_on_host)) return rc;
   const FfnFusion f = ffn_fusion(d, out_on_host);
-  int n = 2;                                                              // index pass + quant-scatter
+  int n = ffn_fuse_index(d) ? 1 : 2;                                      // (index pass +) quant-scatter
   n += f.swiglu ? 1 : 2;                                                  // GEMM1 (+ SwiGLU)
   n += 1;                                                                 // GEMM2
   n += f.combine ? 0 : 1;                                                 // combine
@@ -344,11 +354,14 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
   const int32_t gflags = d->gemm_flags & ~(MOE_FFN_FUSE_SWIGLU | MOE_FFN_UE8M0);
   const FfnFusion fusion = ffn_fusion(d, out_on_host);
   const bool fuse_combine = fusion.combine;
-  // The routing arrays are written by the index kernel: two launches before
-  // GEMM1 (the quant-scatter runs in between; T > 0 here) and more before
-  // GEMM2, so both GEMMs may build their schedule and start streaming weights
-  // before they wait for the kernel just ahead of them.
-  const int32_t g1flags = gflags | MOE_GEMM_EARLY_WEIGHTS;
+  // The routing arrays are written by the index pass: by a separate kernel two
+  // launches before GEMM1 (the quant-scatter runs in between; T > 0 here), or
+  // inside the quant-scatter kernel just before GEMM1 for small masked batches,
+  // and in either case before GEMM2's predecessor; a GEMM whose routing arrays
+  // are final may build its schedule and start streaming weights before it
+  // waits for the kernel just ahead of it.
+  const bool fuse_index = ffn_fuse_index(d);
+  const int32_t g1flags = gflags | (fuse_index ? 0 : MOE_GEMM_EARLY_WEIGHTS);
   const int32_t g2flags = gflags | MOE_GEMM_EARLY_WEIGHTS;
   // stages 1+2: routing index pass, then each routed token row is quantised
   // straight into its expert slot (no token-order FP8 copy in between)
@@ -357,7 +370,7 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
   if ((rc = permute_launch(nullptr, nullptr, 0, d->x, d->H, d->topk_ids, d->T, d->H, d->k,
                            d->expert_begin, d->E, d->layout, d->max_m, a1, ue8m0 ? nullptr : sa1, p.s_ld1, counts,
                            offsets, mind, rowsrc, dst, p.rows, d->err, st, fuse_combine ? d->out : nullptr,
-                           d->H, ue8m0 ? reinterpret_cast<uint8_t*>(sa1) : nullptr)))
+                           d->H, ue8m0 ? reinterpret_cast<uint8_t*>(sa1) : nullptr, fuse_index)))
     return rc;
   if ((rc = mark(2))) return rc;
   if (ue8m0) {

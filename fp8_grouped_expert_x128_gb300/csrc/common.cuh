@@ -68,7 +68,8 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
                    uint8_t* q_out, float* s_out, int64_t s_out_ld, int32_t* counts,
                    int32_t* offsets, int32_t* m_indices, int32_t* row_src, int32_t* dst_row,
                    int64_t rows_capacity, int32_t* err, cudaStream_t st,
-                   uint16_t* zero_out = nullptr, int64_t ldo = 0, uint8_t* sf8_out = nullptr);
+                   uint16_t* zero_out = nullptr, int64_t ldo = 0, uint8_t* sf8_out = nullptr,
+                   bool fuse_index = false);
 
 // SwiGLU + 1x128 requantisation (moe_swiglu_quant and moe_ffn): fp32 scales
 // in groups of G rows, or (sf8) exponent bytes in the packed UE8M0 layout.

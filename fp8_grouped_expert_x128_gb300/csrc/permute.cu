@@ -246,11 +246,30 @@ __global__ void __launch_bounds__(128) permute_scatter_kernel(
 // 4 pairs per warp, so each row finishes sooner.
 // kUE8M0: power-of-two block scales, their exponent bytes written to the
 // packed layout of the block-scaled GEMM (ScaleOut with sf8).
-template <int kQsWarps, int kQsPairs, bool kUE8M0>
-__global__ void __launch_bounds__(32 * kQsWarps, kQsWarps == 4 ? 6 : 4) quant_scatter_kernel(
+// kRank (masked layout, small batches, k <= kRankMaxK): the kernel also does the
+// index pass's work, so no separate index kernel runs.  For its token t each CTA
+// counts, over the assignments before each of the token's slots, those routed
+// to the same expert -- the slot's rank in ascending assignment order, the
+// index pass's definition -- with every thread scanning a strided share of the
+// routing ids (four per 16-byte load, all loads of a pass in flight); CTA 0
+// also builds the per-expert counts (clamped to max_m, overflow flagged).
+// Unused slab rows' row_src entries are left as they are (moe_ffn reads
+// row_src only for rows below a count).
+constexpr int kRankMaxK = 16;
+struct RankArgs {
+  const int32_t* topk_ids;
+  int32_t expert_begin, E, max_m;
+  int32_t* counts;
+  int32_t* row_src;
+  int32_t* dst_row;
+  int32_t* err;
+};
+
+template <int kQsWarps, int kQsPairs, bool kUE8M0, bool kRank = false>
+__global__ void __launch_bounds__(32 * kQsWarps, kRank ? 2 : (kQsWarps == 4 ? 6 : 4)) quant_scatter_kernel(
     const uint16_t* __restrict__ x, int64_t ldx, const int32_t* __restrict__ dst_row,
     int64_t T, int32_t k, int64_t H, uint8_t* __restrict__ q_out, const ScaleOut so,
-    uint16_t* __restrict__ zero_out, int64_t ldo) {
+    uint16_t* __restrict__ zero_out, int64_t ldo, const RankArgs ra) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t KB = H / 128, NP = (KB + 1) / 2;
   bool waited = false;
@@ -261,8 +280,89 @@ __global__ void __launch_bounds__(32 * kQsWarps, kQsWarps == 4 ? 6 : 4) quant_sc
       waited = true;
     }
   };
+  __shared__ int32_t s_dst[kRank ? kRankMaxK : 1];
+  __shared__ int32_t s_rank[kRank ? kRankMaxK : 1];
+  __shared__ int32_t s_sid[kRank ? kRankMaxK : 1];
+  if constexpr (kRank) {
+    // x and the routing ids may come from the kernel just before this one
+    wait_index();
+    if (blockIdx.x == 0) {
+      // per-expert counts over all assignments (warp-aggregated shared atomics)
+      __shared__ int32_t hist[kMaxExperts];
+      for (int e = threadIdx.x; e < ra.E; e += blockDim.x) hist[e] = 0;
+      __syncthreads();
+      const int64_t n = T * k;
+      for (int64_t i0 = 0; i0 < n; i0 += blockDim.x) {
+        const int64_t i = i0 + threadIdx.x;
+        int e = i < n ? __ldg(ra.topk_ids + i) - ra.expert_begin : -1;
+        if (e < 0 || e >= ra.E) e = -1;
+        const uint32_t same = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && (same & ((1u << lane) - 1u)) == 0) atomicAdd(&hist[e], __popc(same));
+      }
+      __syncthreads();
+      for (int e = threadIdx.x; e < ra.E; e += blockDim.x) {
+        const int c = hist[e];
+        ra.counts[e] = c < ra.max_m ? c : ra.max_m;
+        if (c > ra.max_m) set_err(ra.err, MOE_DEV_OVERFLOW);
+      }
+    }
+  }
   for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
     const uint16_t* xr = x + t * ldx;
+    if constexpr (kRank) {
+      // the token's slot ranks: assignments [0, t*k + j) routed like slot j
+      if (threadIdx.x < k) {
+        s_sid[threadIdx.x] = __ldg(ra.topk_ids + t * k + threadIdx.x);
+        s_rank[threadIdx.x] = 0;
+      }
+      __syncthreads();
+      int sid[kRankMaxK], c[kRankMaxK];
+#pragma unroll
+      for (int j = 0; j < kRankMaxK; ++j) {
+        sid[j] = j < k ? s_sid[j] : INT32_MIN;
+        c[j] = 0;
+      }
+      const int64_t first = t * k, lim = first + k;   // positions that can precede a slot
+      for (int64_t p0 = static_cast<int64_t>(threadIdx.x) * 4; p0 < lim; p0 += static_cast<int64_t>(blockDim.x) * 4) {
+        int v[4];
+        if (p0 + 4 <= lim && (reinterpret_cast<uintptr_t>(ra.topk_ids + p0) & 15) == 0) {
+          const int4 w = __ldg(reinterpret_cast<const int4*>(ra.topk_ids + p0));
+          v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) v[q] = p0 + q < lim ? __ldg(ra.topk_ids + p0 + q) : INT32_MIN;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int64_t pos = p0 + q;
+#pragma unroll
+          for (int j = 0; j < kRankMaxK; ++j) c[j] += (v[q] == sid[j] && pos < first + j) ? 1 : 0;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kRankMaxK; ++j) {
+        if (j < k) {
+          int cj = c[j];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) cj += __shfl_xor_sync(0xffffffffu, cj, o);
+          if (lane == 0 && cj) atomicAdd(&s_rank[j], cj);
+        }
+      }
+      __syncthreads();
+      if (threadIdx.x < k) {
+        const int j = threadIdx.x;
+        const int e = s_sid[j] - ra.expert_begin;
+        const int rank = s_rank[j];
+        int32_t dst = -1;
+        if (e >= 0 && e < ra.E && rank < ra.max_m) {
+          dst = e * ra.max_m + rank;
+          ra.row_src[dst] = static_cast<int32_t>(first + j);
+        }
+        ra.dst_row[first + j] = dst;
+        s_dst[j] = dst;
+      }
+      __syncthreads();
+    }
     for (int64_t p0 = warp; p0 < NP; p0 += static_cast<int64_t>(kQsWarps) * kQsPairs) {
       uint4 u[kQsPairs];
 #pragma unroll
@@ -288,7 +388,8 @@ __global__ void __launch_bounds__(32 * kQsWarps, kQsWarps == 4 ? 6 : 4) quant_sc
       }
       wait_index();
       // the token's routing slots, one per lane
-      const int32_t dl = lane < k ? __ldg(dst_row + t * k + lane) : -1;
+      int32_t dl = -1;
+      if (lane < k) dl = kRank ? s_dst[lane] : __ldg(dst_row + t * k + lane);
       for (int j2 = 0; j2 < k; ++j2) {
         const int32_t dst = __shfl_sync(0xffffffffu, dl, j2);
         if (dst < 0) continue;
@@ -307,7 +408,7 @@ __global__ void __launch_bounds__(32 * kQsWarps, kQsWarps == 4 ? 6 : 4) quant_sc
       // one slot per token and it is not routed here: the token's output row
       // is zero (what the combine writes for a token without local slots)
       wait_index();
-      if (__ldg(dst_row + t) < 0)
+      if ((kRank ? s_dst[0] : __ldg(dst_row + t)) < 0)
         for (int64_t c = threadIdx.x; c < H / 8; c += blockDim.x)
           reinterpret_cast<uint4*>(zero_out + t * ldo)[c] = make_uint4(0, 0, 0, 0);
     }
@@ -565,7 +666,8 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
                    uint8_t* q_out, float* s_out, int64_t s_out_ld, int32_t* counts,
                    int32_t* offsets, int32_t* m_indices, int32_t* row_src, int32_t* dst_row,
                    int64_t rows_capacity, int32_t* err, cudaStream_t st, uint16_t* zero_out,
-                   int64_t ldo, uint8_t* sf8_out) {
+                   int64_t ldo, uint8_t* sf8_out, bool fuse_index) {
+  // (defaults for zero_out .. fuse_index are in common.cuh)
   MOE_CHECK_ARG(T >= 0 && H > 0 && H % 128 == 0 && k >= 1 && k <= 32);
   MOE_CHECK_ARG(E >= 1 && E <= kMaxExperts);
   MOE_CHECK_ARG(layout == MOE_LAYOUT_MASKED || layout == MOE_LAYOUT_CONTIG);
@@ -590,8 +692,26 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
   }
   MOE_CHECK_ARG(T * k < (1ll << 31));
   if (int rc = check_device()) return rc;
+  // the index pass inside the quant-scatter kernel: masked layout, bf16 rows
+  // to quantise, a few slots per token
+  fuse_index = fuse_index && T > 0 && x != nullptr && layout == MOE_LAYOUT_MASKED && k <= kRankMaxK;
   IndexParams p{topk_ids, T * k, expert_begin, E, layout, max_m, rows_capacity,
                 counts, offsets, m_indices, row_src, dst_row, err};
+  if (fuse_index) {
+    const bool packed = sf8_out != nullptr;
+    auto kern = packed ? quant_scatter_kernel<8, 4, true, true> : quant_scatter_kernel<8, 4, false, true>;
+    const ScaleOut so{s_out, sf8_out, G, static_cast<int32_t>((H / 128 + 3) / 4), static_cast<int32_t>((G + 127) / 128)};
+    static int per_sm[2][64] = {{0}};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    int& occ = per_sm[packed ? 1 : 0][dev];
+    if (occ == 0 && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 256, 0) != cudaSuccess || occ < 1))
+      return MOE_ERR_CUDA;
+    const int64_t wave = static_cast<int64_t>(num_sms()) * occ;
+    const RankArgs ra{topk_ids, expert_begin, E, max_m, counts, row_src, dst_row, err};
+    return launch_pdl(kern, static_cast<unsigned>(T < wave ? T : wave), 256, 0, st, x, ldx, dst_row, T, k,
+                      static_cast<int64_t>(H), q_out, so, k == 1 ? zero_out : nullptr, ldo, ra);
+  }
   size_t smem = sizeof(int32_t) * (2 * E + kIdxWarps * E);
   const size_t ids_bytes = sizeof(int32_t) * static_cast<size_t>(T * k);
   const int ids_in_smem = smem + ids_bytes <= kIdxSmemLimit ? 1 : 0;
@@ -621,7 +741,7 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
       return MOE_ERR_CUDA;
     const int64_t wave = static_cast<int64_t>(num_sms()) * occ;
     return launch_pdl(kern, static_cast<unsigned>(T < wave ? T : wave), threads, 0, st, x, ldx, dst_row, T, k,
-                      static_cast<int64_t>(H), q_out, so, k == 1 ? zero_out : nullptr, ldo);
+                      static_cast<int64_t>(H), q_out, so, k == 1 ? zero_out : nullptr, ldo, RankArgs{});
   }
   return launch_pdl(permute_scatter_kernel, grid, 128, 0, st, q, s, s_ld, dst_row, n, k, H, q_out,
                     s_out, G);
@@ -637,7 +757,7 @@ extern "C" int moe_permute(const uint8_t* q, const float* s, int64_t s_ld, const
                            int64_t rows_capacity, int32_t* err, void* stream) {
   return permute_launch(q, s, s_ld, nullptr, 0, topk_ids, T, H, k, expert_begin, E, layout, max_m,
                         q_out, s_out, s_out_ld, counts, offsets, m_indices, row_src, dst_row,
-                        rows_capacity, err, as_stream(stream), nullptr, 0, nullptr);
+                        rows_capacity, err, as_stream(stream), nullptr, 0, nullptr, false);
 }
 
 extern "C" int moe_combine(const uint16_t* Y2, int64_t ldy, int64_t y_rows, const int32_t* dst_row,
