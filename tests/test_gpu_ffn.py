@@ -284,3 +284,15 @@ def test_ffn_degenerate_batches(lib, case, layout, reading):
     assert g.intact(), "moe_ffn wrote past out"
     if T:
         assert (bits(g.t) == 0).all(), "a token with no local slot must come out +0.0"
+
+
+@pytest.mark.parametrize("name,expected", [("c1", 5), ("c5t1", 5), ("c5", 5), ("c2", 6), ("c4", 6), ("c3", 5)])
+def test_ffn_kernel_count(lib, name, expected):
+    """The kernels one moe_ffn call launches (what bench.py reports per step):
+    small masked batches run the index pass inside the quant-scatter kernel,
+    larger ones as its own kernel; one slot per token (c3) folds the combine
+    into GEMM2's epilogue."""
+    wl = build_workload(name)
+    T, H = wl["T"], wl["cfg"].H
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    assert lib.moe_ffn_kernel_count(make_desc(wl, out)) == expected
