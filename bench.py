@@ -480,6 +480,31 @@ def routing_summary(cfg_name):
                 active_experts=int((counts > 0).sum()))
 
 
+def host_workload(name):
+    """The host-side facts of '<config>' or '<config>:ue8m0' that choose the
+    kernels and their labels (no tensors, no GPU): what build_workload returns
+    minus the device buffers."""
+    import fp8_grouped_expert_x128_gb300 as moe
+    cfg_name, _, variant = name.partition(":")
+    wl = routing_summary(cfg_name)
+    wl["layout"] = moe.MOE_LAYOUT_MASKED if wl["cfg"].layout == "masked" else moe.MOE_LAYOUT_CONTIG
+    wl["expected_m"] = int(math.ceil(wl["rows"] / max(1, wl["active_experts"])))
+    if variant == "ue8m0":
+        wl["ue8m0"] = True
+        wl["gemm_flags"] = moe.MOE_FFN_UE8M0
+    return wl
+
+
+def traffic_name(name):
+    """The workload part of a profiles/traffic.json key ('c3:ue8m0' -> 'c3-ue8m0':
+    the key itself is '<kernel>@<workload>:<gemm1|gemm2>')."""
+    return name.replace(":", "-")
+
+
+DEFAULT_HEADLINE = "c5"
+DEFAULT_EXTRA = "c2,c3,c4,c3:ue8m0,c4:ue8m0,c2:ue8m0,c5:ue8m0"
+
+
 def run_reference(args, world, rank):
     """The reference arm: the CPU oracle, as it stands, on a bounded sample per step."""
     if rank != 0:
@@ -669,7 +694,7 @@ def measure(name, args, dev, world, l2_flush, stream, peaks, peak_src, clk_secon
     rep = {
         "value": units / total_s, "ms_per_step": ms_per_step,
         "stage_ms": {n: round(v, 4) for n, v in zip(STAGES, stage_ms)},
-        "kernels": kernel_rooflines(wl, name.replace(":", "-"), g1_s, g2_s, peaks, peak_src),
+        "kernels": kernel_rooflines(wl, traffic_name(name), g1_s, g2_s, peaks, peak_src),
         "step_roofline": roofline(alg["flops"], alg["step_bytes"], ms_per_step / 1e3, peaks),
         "tflops": alg["flops"] / (ms_per_step / 1e3) / 1e12,
         "weight_gbs": alg["weight_bytes"] / (ms_per_step / 1e3) / 1e9,
@@ -775,10 +800,10 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="c5",
+    ap.add_argument("--workload", default=DEFAULT_HEADLINE,
                     help="the headline workload (default: the all-experts decode layer, the largest "
                          "configuration that fits one GPU)")
-    ap.add_argument("--extra", default="c2,c3,c4,c3:ue8m0,c4:ue8m0,c2:ue8m0,c5:ue8m0",
+    ap.add_argument("--extra", default=DEFAULT_EXTRA,
                     help="comma-separated workloads also measured in the same run, reported under "
                          "'workloads' (not part of the value); '<config>:ue8m0' runs the power-of-two "
                          "reading of the scales end to end (block-scaled GEMMs); empty for none")
