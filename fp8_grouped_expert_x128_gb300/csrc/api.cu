@@ -99,7 +99,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 struct FfnPlan {
   int64_t T_pad, rows, s_ld1, s_ld2;
   bool ue8m0;   // packed power-of-two activation scales (off_sa1 / off_sa2 hold words)
-  size_t off_counts, off_offsets, off_mind, off_rowsrc, off_dst, off_a1, off_sa1,
+  size_t off_counts, off_offsets, off_mind, off_rowsrc, off_dst, off_lrank, off_hist, off_a1, off_sa1,
       off_y1, off_a2, off_sa2, off_y2, total;
 };
 
@@ -132,6 +132,9 @@ int plan_ffn(const moe_ffn_desc* d, FfnPlan* p) {
   p->off_mind = take(sizeof(int32_t) * p->rows);
   p->off_rowsrc = take(sizeof(int32_t) * p->rows);
   p->off_dst = take(sizeof(int32_t) * d->T * d->k);
+  // scratch of the many-CTA index pass (large batches)
+  p->off_lrank = take(sizeof(int32_t) * d->T * d->k);
+  p->off_hist = take(sizeof(int32_t) * static_cast<size_t>(permute_chunk_count(d->T * d->k)) * E);
   p->ue8m0 = (d->gemm_flags & MOE_FFN_UE8M0) != 0;
   // packed UE8M0 scales: masked -> one group of max_m rows per expert;
   // contiguous -> one group of `rows` rows (a multiple of 128)
@@ -230,6 +233,8 @@ struct FfnFusion {
 // T = 1 / 64 gains 4 µs per step; at ~4000 ids (c2) the scans cost 7 µs more
 // than the index kernel they replace.
 constexpr int64_t kFuseIndexMaxIds = 1024;
+// above this many assignments the index pass runs over many CTAs (permute.cu)
+constexpr int64_t kFfnMultiIndexIds = 8192;
 bool ffn_fuse_index(const moe_ffn_desc* d) {
   return d->layout == MOE_LAYOUT_MASKED && d->T > 0 && d->T * d->k <= kFuseIndexMaxIds && d->k <= 16;
 }
@@ -275,7 +280,9 @@ extern "C" int moe_ffn_kernel_count(const moe_ffn_desc* d) {
   bool out_on_host = false;
   if (int rc = check_placement(d->out, true, &out_on_host)) return rc;
   const FfnFusion f = ffn_fusion(d, out_on_host);
-  int n = ffn_fuse_index(d) ? 1 : 2;                                      // (index pass +) quant-scatter
+  // quant-scatter, with the index pass inside it, or before it as one kernel
+  // or (large batches) as two
+  int n = ffn_fuse_index(d) ? 1 : (d->T * d->k > kFfnMultiIndexIds ? 3 : 2);
   n += f.swiglu ? 1 : 2;                                                  // GEMM1 (+ SwiGLU)
   n += 1;                                                                 // GEMM2
   n += f.combine ? 0 : 1;                                                 // combine
@@ -370,7 +377,8 @@ extern "C" int moe_ffn(const moe_ffn_desc* d, void* workspace, size_t workspace_
   if ((rc = permute_launch(nullptr, nullptr, 0, d->x, d->H, d->topk_ids, d->T, d->H, d->k,
                            d->expert_begin, d->E, d->layout, d->max_m, a1, ue8m0 ? nullptr : sa1, p.s_ld1, counts,
                            offsets, mind, rowsrc, dst, p.rows, d->err, st, fuse_combine ? d->out : nullptr,
-                           d->H, ue8m0 ? reinterpret_cast<uint8_t*>(sa1) : nullptr, fuse_index)))
+                           d->H, ue8m0 ? reinterpret_cast<uint8_t*>(sa1) : nullptr, fuse_index,
+                           static_cast<int32_t*>(at(p.off_lrank)), static_cast<int32_t*>(at(p.off_hist)))))
     return rc;
   if ((rc = mark(2))) return rc;
   if (ue8m0) {

@@ -208,6 +208,172 @@ __global__ void __launch_bounds__(kIdxThreads) permute_index_kernel(IndexParams 
   }
 }
 
+// Large batches: the index pass over many CTAs, in two kernels.
+// permute_chunk_rank_kernel: CTA c takes assignments [c, c+1) * kIdxChunk and
+// ranks each among the chunk's assignments to the same expert (the ordered
+// per-warp counting of the one-CTA pass), writing the rank (lrank) and the
+// chunk's per-expert totals (chunk_hist[c][E]).
+// permute_finalize_kernel: every CTA adds up the chunk totals -- each expert's
+// count, segment base (masked: e * max_m; contiguous: exclusive scan of the
+// counts padded to 128) and the total of the chunks before its own -- and for
+// its assignments writes dst_row / row_src / m_indices exactly as the one-CTA
+// pass does; all CTAs share the -1 fill of the rows no assignment uses, and
+// CTA 0 writes counts, offsets and the error flags.
+constexpr int kIdxChunk = kIdxThreads * kIdxPer;
+constexpr int64_t kIdxMultiMinIds = 8192;   // from here on the index pass runs over many CTAs
+constexpr int kFinThreads = 256;
+static_assert(kIdxChunk % kFinThreads == 0, "a finalize CTA stays inside one chunk");
+
+__global__ void __launch_bounds__(kIdxThreads, 1) permute_chunk_rank_kernel(IndexParams p, int32_t* lrank,
+                                                                         int32_t* chunk_hist) {
+  extern __shared__ int32_t sm[];
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int E = p.E;
+  int32_t* cnt = sm;        // [E] running count inside the chunk
+  int32_t* wc = sm + E;     // [kIdxWarps][E]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kIdxChunk;
+  for (int e = tid; e < E; e += kIdxThreads) cnt[e] = 0;
+  for (int x = tid; x < kIdxWarps * E; x += kIdxThreads) wc[x] = 0;
+  __syncthreads();
+  const uint32_t lanes_below = (1u << lane) - 1u;
+  int e_r[kIdxPer], rk_r[kIdxPer];
+#pragma unroll
+  for (int r = 0; r < kIdxPer; ++r) {
+    const int64_t i = c0 + (static_cast<int64_t>(warp) * kIdxPer + r) * 32 + lane;
+    int e = i < p.n_assign ? __ldg(p.topk_ids + i) - p.expert_begin : -1;
+    if (e < 0 || e >= E) e = -1;
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    const int lower = __popc(same & lanes_below);
+    const int before = e >= 0 ? wc[warp * E + e] : 0;
+    __syncwarp();
+    if (e >= 0 && lower == 0) wc[warp * E + e] = before + __popc(same);
+    __syncwarp();
+    e_r[r] = e;
+    rk_r[r] = before + lower;
+  }
+  __syncthreads();
+  for (int ee = warp; ee < E; ee += kIdxWarps) {
+    const int v = wc[lane * E + ee];
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    __syncwarp();
+    wc[lane * E + ee] = incl - v;
+    if (lane == 31) cnt[ee] = incl;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < kIdxPer; ++r) {
+    const int64_t i = c0 + (static_cast<int64_t>(warp) * kIdxPer + r) * 32 + lane;
+    if (i < p.n_assign) lrank[i] = e_r[r] >= 0 ? wc[warp * E + e_r[r]] + rk_r[r] : -1;
+  }
+  for (int e = tid; e < E; e += kIdxThreads) chunk_hist[static_cast<int64_t>(blockIdx.x) * E + e] = cnt[e];
+}
+
+__global__ void __launch_bounds__(kFinThreads) permute_finalize_kernel(IndexParams p, const int32_t* lrank,
+                                                                       const int32_t* chunk_hist, int32_t n_chunks) {
+  extern __shared__ int32_t fsm[];
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int E = p.E;
+  int32_t* tot = fsm;           // [E] count over all chunks
+  int32_t* pre = fsm + E;       // [E] count over the chunks before this CTA's
+  int32_t* base = fsm + 2 * E;  // [E] segment base
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kFinThreads;
+  const int my_chunk = static_cast<int>(i0 / kIdxChunk);
+  for (int e = tid; e < E; e += kFinThreads) {
+    int t = 0, b = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      const int h = __ldg(chunk_hist + static_cast<int64_t>(c) * E + e);
+      if (c < my_chunk) b += h;
+      t += h;
+    }
+    tot[e] = t;
+    pre[e] = b;
+  }
+  __syncthreads();
+  if (p.layout == MOE_LAYOUT_MASKED) {
+    for (int e = tid; e < E; e += kFinThreads) base[e] = e * p.max_m;
+  } else if (tid < 32) {
+    // exclusive scan of the padded counts over the experts, 32 at a time
+    int64_t run = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int64_t padded = e < E ? (static_cast<int64_t>(tot[e]) + 127) / 128 * 128 : 0;
+      int64_t incl = padded;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (e < E) base[e] = static_cast<int32_t>(run + incl - padded);
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (blockIdx.x == 0 && lane == 0) {
+      p.offsets[E] = static_cast<int32_t>(run);
+      if (run > p.rows_capacity) set_err(p.err, MOE_DEV_BAD_INDEX);
+    }
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int e = tid; e < E; e += kFinThreads) {
+      if (p.layout == MOE_LAYOUT_MASKED) {
+        p.counts[e] = tot[e] < p.max_m ? tot[e] : p.max_m;
+        if (tot[e] > p.max_m) set_err(p.err, MOE_DEV_OVERFLOW);
+      } else {
+        p.offsets[e] = base[e];
+        p.counts[e] = tot[e];
+      }
+    }
+  }
+  const int64_t map_rows =
+      p.layout == MOE_LAYOUT_MASKED ? static_cast<int64_t>(E) * p.max_m : p.rows_capacity;
+  // this CTA's assignments
+  const int64_t i = i0 + tid;
+  if (i < p.n_assign) {
+    const int lr = __ldg(lrank + i);
+    int32_t dst = -1;
+    if (lr >= 0) {
+      int e = __ldg(p.topk_ids + i) - p.expert_begin;
+      const int rank = pre[e] + lr;
+      if (p.layout == MOE_LAYOUT_CONTIG || rank < p.max_m) {
+        const int64_t row = static_cast<int64_t>(base[e]) + rank;
+        if (row < map_rows) {
+          dst = static_cast<int32_t>(row);
+          p.row_src[row] = static_cast<int32_t>(i);
+          if (p.layout == MOE_LAYOUT_CONTIG) p.m_indices[row] = e;
+        }
+      }
+    }
+    p.dst_row[i] = dst;
+  }
+  // the rows no assignment uses: each expert's rows past its count up to its
+  // segment end, and (contiguous) the rows past the last segment
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kFinThreads;
+  const int64_t gtid = i0 + tid;
+  for (int e = 0; e < E; ++e) {
+    const int64_t used = p.layout == MOE_LAYOUT_MASKED ? (tot[e] < p.max_m ? tot[e] : p.max_m) : tot[e];
+    const int64_t seg = p.layout == MOE_LAYOUT_MASKED ? p.max_m : (static_cast<int64_t>(tot[e]) + 127) / 128 * 128;
+    for (int64_t r = base[e] + used + gtid; r < base[e] + seg && r < map_rows; r += stride) {
+      p.row_src[r] = -1;
+      if (p.layout == MOE_LAYOUT_CONTIG) p.m_indices[r] = -1;
+    }
+  }
+  if (p.layout == MOE_LAYOUT_CONTIG) {
+    const int64_t end = static_cast<int64_t>(base[E - 1]) + (static_cast<int64_t>(tot[E - 1]) + 127) / 128 * 128;
+    for (int64_t r = end + gtid; r < map_rows; r += stride) {
+      p.row_src[r] = -1;
+      p.m_indices[r] = -1;
+    }
+  }
+}
+
 // One warp per assignment: copy the FP8 row and gather its scales.
 __global__ void __launch_bounds__(128) permute_scatter_kernel(
     const uint8_t* __restrict__ q, const float* __restrict__ s, int64_t s_ld,
@@ -666,8 +832,8 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
                    uint8_t* q_out, float* s_out, int64_t s_out_ld, int32_t* counts,
                    int32_t* offsets, int32_t* m_indices, int32_t* row_src, int32_t* dst_row,
                    int64_t rows_capacity, int32_t* err, cudaStream_t st, uint16_t* zero_out,
-                   int64_t ldo, uint8_t* sf8_out, bool fuse_index) {
-  // (defaults for zero_out .. fuse_index are in common.cuh)
+                   int64_t ldo, uint8_t* sf8_out, bool fuse_index, int32_t* lrank, int32_t* chunk_hist) {
+  // (defaults for zero_out .. chunk_hist are in common.cuh)
   MOE_CHECK_ARG(T >= 0 && H > 0 && H % 128 == 0 && k >= 1 && k <= 32);
   MOE_CHECK_ARG(E >= 1 && E <= kMaxExperts);
   MOE_CHECK_ARG(layout == MOE_LAYOUT_MASKED || layout == MOE_LAYOUT_CONTIG);
@@ -712,6 +878,22 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
     return launch_pdl(kern, static_cast<unsigned>(T < wave ? T : wave), 256, 0, st, x, ldx, dst_row, T, k,
                       static_cast<int64_t>(H), q_out, so, k == 1 ? zero_out : nullptr, ldo, ra);
   }
+  if (lrank != nullptr && chunk_hist != nullptr && T * k > kIdxMultiMinIds) {
+    // many assignments: the index pass over many CTAs (rank per chunk, then finalize)
+    const int64_t n = T * k;
+    const int n_chunks = static_cast<int>((n + kIdxChunk - 1) / kIdxChunk);
+    const size_t rsmem = sizeof(int32_t) * static_cast<size_t>(E + kIdxWarps * E);
+    if (rsmem > 48 * 1024)
+      MOE_CUDA_TRY(cudaFuncSetAttribute(permute_chunk_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(rsmem)));
+    if (int rc = launch_pdl(permute_chunk_rank_kernel, static_cast<unsigned>(n_chunks), kIdxThreads, rsmem, st, p,
+                            lrank, chunk_hist))
+      return rc;
+    if (int rc = launch_pdl(permute_finalize_kernel, static_cast<unsigned>((n + kFinThreads - 1) / kFinThreads),
+                            kFinThreads, sizeof(int32_t) * 3 * static_cast<size_t>(E), st, p,
+                            static_cast<const int32_t*>(lrank), static_cast<const int32_t*>(chunk_hist), n_chunks))
+      return rc;
+  } else {
   size_t smem = sizeof(int32_t) * (2 * E + kIdxWarps * E);
   const size_t ids_bytes = sizeof(int32_t) * static_cast<size_t>(T * k);
   const int ids_in_smem = smem + ids_bytes <= kIdxSmemLimit ? 1 : 0;
@@ -722,6 +904,7 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
                                       static_cast<int>(smem)));
   }
   if (int rc = launch_pdl(permute_index_kernel, 1, kIdxThreads, smem, st, p, ids_in_smem)) return rc;
+  }
   if (T == 0) return MOE_OK;
   const int64_t n = T * k;
   const unsigned grid = static_cast<unsigned>((n + 3) / 4);

@@ -161,18 +161,26 @@ def test_ffn_end_to_end_every_token(lib, name):
 
 
 @pytest.mark.parametrize("name,fuse", [("c1", False), ("c2", False), ("c3", False), ("c2", True), ("c3", True),
-                                       ("c5t1", False), ("c1_overflow", False)])
+                                       ("c5t1", False), ("c1_overflow", False), ("c4_overflow", False),
+                                       ("c3_ragged", False)])
 def test_ffn_equals_the_stage_entry_points(lib, name, fuse):
     """moe_ffn fuses quantisation into the permute (and, with MOE_FFN_FUSE_SWIGLU,
     SwiGLU + requantisation into the tokens-as-M GEMM1 epilogue); its output must
     be bit-identical to the public stage calls made one by one (quant, permute,
-    GEMM1, SwiGLU+quant, GEMM2, combine).
-    c1_overflow: the tiny config with 16 slots per expert, so every expert
-    overflows and the ranks past max_m are dropped the same way on both paths."""
-    overflow = name == "c1_overflow"
-    wl = build_workload("c1" if overflow else name)
+    GEMM1, SwiGLU+quant, GEMM2, combine).  The index pass differs by batch size
+    inside moe_ffn (inside the quant-scatter kernel for c1 / c5t1, one CTA for c2,
+    many CTAs for c3 / c4) and is the one-CTA kernel in moe_permute.
+    c1_overflow / c4_overflow: max_m cut to 16 / 1024, so experts overflow and
+    the ranks past max_m are dropped the same way on both paths.  c3_ragged: the
+    first 30000 prefill tokens, so the last 4096-assignment chunk of the
+    many-CTA index pass is partly empty."""
+    overflow = name.endswith("_overflow")
+    wl = build_workload(name.split("_")[0] if overflow or name.endswith("_ragged") else name)
     if overflow:
-        wl["cfg"] = dataclasses.replace(wl["cfg"], max_m=16)
+        wl["cfg"] = dataclasses.replace(wl["cfg"], max_m=16 if name.startswith("c1") else 1024)
+    if name.endswith("_ragged"):
+        T = 30000
+        wl.update(x=wl["x"][:T], topk_ids=wl["topk_ids"][:T], topk_w=wl["topk_w"][:T], T=T)
     cfg = wl["cfg"]
     if fuse:
         wl["gemm_flags"] = lib.MOE_FFN_FUSE_SWIGLU
@@ -286,12 +294,12 @@ def test_ffn_degenerate_batches(lib, case, layout, reading):
         assert (bits(g.t) == 0).all(), "a token with no local slot must come out +0.0"
 
 
-@pytest.mark.parametrize("name,expected", [("c1", 5), ("c5t1", 5), ("c5", 5), ("c2", 6), ("c4", 6), ("c3", 5)])
+@pytest.mark.parametrize("name,expected", [("c1", 5), ("c5t1", 5), ("c5", 5), ("c2", 6), ("c4", 7), ("c3", 6)])
 def test_ffn_kernel_count(lib, name, expected):
     """The kernels one moe_ffn call launches (what bench.py reports per step):
     small masked batches run the index pass inside the quant-scatter kernel,
-    larger ones as its own kernel; one slot per token (c3) folds the combine
-    into GEMM2's epilogue."""
+    mid-sized ones as one kernel, large ones (c3, c4) as two; one slot per
+    token (c3) folds the combine into GEMM2's epilogue."""
     wl = build_workload(name)
     T, H = wl["T"], wl["cfg"].H
     out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
