@@ -470,6 +470,9 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
 // bytes are the same whichever kernel wrote them.
 constexpr float kQuantFloor = 1e-4f;
 constexpr float kQuantMax = 448.0f;
+// 1/448 rounded to nearest (a compile-time IEEE division), the reciprocal the
+// scale division below is corrected with.
+constexpr float kQuantMaxRcp = 1.0f / 448.0f;
 
 __device__ __forceinline__ float half_warp_max(float v) {
 #pragma unroll
@@ -498,18 +501,29 @@ __device__ __forceinline__ float div_rn_by(float x, float s, float r) {
   return copysignf(fmaf(e, r, y), x);
 }
 
-// Quantise 8 values with scale s into 8 E4M3 bytes (element 0 in the low byte):
-// q = e4m3(x / s), the division correctly rounded in float32.
-__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
-  float q[8];
-  if (isfinite(s)) {
-    const float r = __frcp_rn(s);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = div_rn_by(f[i], s, r);
-  } else {  // only from non-finite inputs
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(f[i], s);
-  }
+// Two float32 lanes in one 64-bit register pair, for the packed f32x2
+// arithmetic of sm_100 and later (each lane an IEEE float32 operation with
+// round-to-nearest-even, subnormals kept: the same results as two scalar ops).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
+  return d;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint2 pack_e4m3x8(const float (&q)[8]) {
   uint32_t lo = 0, hi = 0;
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
@@ -517,6 +531,45 @@ __device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
     hi |= e4m3x2_rn_satfinite(q[4 + 2 * i], q[4 + 2 * i + 1]) << (16 * i);
   }
   return make_uint2(lo, hi);
+}
+
+// Quantise 8 values with scale s into 8 E4M3 bytes (element 0 in the low byte):
+// q = e4m3(x / s), the division correctly rounded in float32.  The steps of
+// div_rn_by on pairs of lanes: y = x*r, e = y*(-s) + x (the same exact product
+// as -y*s), q = e*r + y, then the sign of x.
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
+  float q[8];
+  if (isfinite(s)) {
+    const float r = __frcp_rn(s);
+    const uint64_t r2 = f2_pack(r, r), ns2 = f2_pack(-s, -s);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint64_t x2 = f2_pack(f[2 * i], f[2 * i + 1]);
+      const uint64_t y2 = f2_mul(x2, r2);
+      const uint64_t e2 = f2_fma(y2, ns2, x2);
+      f2_unpack(f2_fma(e2, r2, y2), q[2 * i], q[2 * i + 1]);
+      q[2 * i] = copysignf(q[2 * i], f[2 * i]);
+      q[2 * i + 1] = copysignf(q[2 * i + 1], f[2 * i + 1]);
+    }
+  } else {  // only from non-finite inputs
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(f[i], s);
+  }
+  return pack_e4m3x8(q);
+}
+
+// quant8 for a power-of-two scale s = 2^e (the UE8M0 reading, byte = e + 127,
+// e in [-22, 120]): 1/s = 2^-e is exact, so x * 2^-e, one rounding, is the
+// correctly rounded x / s (zero signs included) and quant8's correction step
+// has nothing to correct.  An infinite s takes quant8's division path.
+__device__ __forceinline__ uint2 quant8_pow2(const float (&f)[8], float s, uint8_t byte) {
+  if (byte == 0xFF) return quant8(f, s);
+  const float r = __uint_as_float(static_cast<uint32_t>(254 - byte) << 23);
+  const uint64_t r2 = f2_pack(r, r);
+  float q[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) f2_unpack(f2_mul(f2_pack(f[2 * i], f[2 * i + 1]), r2), q[2 * i], q[2 * i + 1]);
+  return pack_e4m3x8(q);
 }
 
 // UE8M0 (power-of-two) block scale, the other reading of the packed input
@@ -563,12 +616,24 @@ struct ScaleOut {
   uint8_t* sf8;
   int64_t G;
   int32_t KG, NC;
-  __device__ __forceinline__ void put(int64_t row, int64_t kb, int64_t KB, float sc, uint8_t byte) const {
-    const int64_t grp = row / G, pos = row - grp * G;
+  // The part of a row's scale index that does not depend on kb (one division
+  // per row); put_at adds kb's part.
+  __device__ __forceinline__ int64_t row_base(int64_t row, int64_t KB) const {
+    const int64_t grp = ((row | G) >> 31) == 0
+                            ? static_cast<int64_t>(static_cast<uint32_t>(row) / static_cast<uint32_t>(G))
+                            : row / G;
+    const int64_t pos = row - grp * G;
+    if (sf8 != nullptr) return ue8m0_act_byte(grp, pos, 0, KG, NC);
+    return grp * KB * G + pos;
+  }
+  __device__ __forceinline__ void put_at(int64_t base, int64_t kb, float sc, uint8_t byte) const {
     if (sf8 != nullptr)
-      sf8[ue8m0_act_byte(grp, pos, kb, KG, NC)] = byte;
+      sf8[base + (kb >> 2) * (static_cast<int64_t>(NC) << 9) + (kb & 3)] = byte;
     else
-      s[(grp * KB + kb) * G + pos] = sc;
+      s[base + kb * G] = sc;
+  }
+  __device__ __forceinline__ void put(int64_t row, int64_t kb, int64_t KB, float sc, uint8_t byte) const {
+    put_at(row_base(row, KB), kb, sc, byte);
   }
 };
 
@@ -578,7 +643,7 @@ struct ScaleOut {
 __device__ __forceinline__ float block_scale(float amax) {
   const float a = fmaxf(amax, kQuantFloor);
   if (!isfinite(a)) return __fdiv_rn(a, kQuantMax);
-  return div_rn_by(a, kQuantMax, __frcp_rn(kQuantMax));
+  return div_rn_by(a, kQuantMax, kQuantMaxRcp);
 }
 
 

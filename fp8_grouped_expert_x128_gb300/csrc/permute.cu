@@ -550,22 +550,25 @@ __global__ void __launch_bounds__(32 * kQsWarps, kRank ? 2 : (kQsWarps == 4 ? 6 
         amax = half_warp_max(amax);
         e8b[j] = 0;
         sc[j] = kUE8M0 ? block_scale_ue8m0(amax, &e8b[j]) : block_scale(amax);
-        code[j] = quant8(f, sc[j]);
+        code[j] = kUE8M0 ? quant8_pow2(f, sc[j], e8b[j]) : quant8(f, sc[j]);
       }
       wait_index();
-      // the token's routing slots, one per lane
+      // the token's routing slots, one per lane, with the k-independent part
+      // of each slot's scale index
       int32_t dl = -1;
       if (lane < k) dl = kRank ? s_dst[lane] : __ldg(dst_row + t * k + lane);
+      const int64_t sbl = dl >= 0 ? so.row_base(dl, KB) : 0;
       for (int j2 = 0; j2 < k; ++j2) {
         const int32_t dst = __shfl_sync(0xffffffffu, dl, j2);
         if (dst < 0) continue;
+        const int64_t sb = __shfl_sync(0xffffffffu, sbl, j2);
         uint8_t* qr = q_out + static_cast<int64_t>(dst) * H;
 #pragma unroll
         for (int j = 0; j < kQsPairs; ++j) {
           const int64_t kb = (p0 + j * kQsWarps) * 2 + (lane >> 4);
           if (kb < KB) {
             *reinterpret_cast<uint2*>(qr + kb * 128 + (lane & 15) * 8) = code[j];
-            if ((lane & 15) == 0) so.put(dst, kb, KB, sc[j], e8b[j]);
+            if ((lane & 15) == 0) so.put_at(sb, kb, sc[j], e8b[j]);
           }
         }
       }

@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __rest
   if (!active) return;
   uint8_t byte = 0;
   const float sc = kUE8M0 ? block_scale_ue8m0(amax, &byte) : block_scale(amax);
-  *reinterpret_cast<uint2*>(q + m * ldq + col) = quant8(f, sc);
+  *reinterpret_cast<uint2*>(q + m * ldq + col) = kUE8M0 ? quant8_pow2(f, sc, byte) : quant8(f, sc);
   if ((lane & 15) == 0) {
     s[kb * s_ld + m] = sc;
     if (kUE8M0 && e8 != nullptr) e8[kb * s_ld + m] = byte;
@@ -95,7 +95,8 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const uint16_t* __re
   const float sc = kUE8M0 ? block_scale_ue8m0(amax, &byte) : block_scale(amax);
   uint8_t* qb = q + (e * N + nb * 128) * K + kb * 128 + c8 * 8;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(qb + (r0 + 16 * i) * K) = quant8(f[i], sc);
+  for (int i = 0; i < 8; ++i)
+    *reinterpret_cast<uint2*>(qb + (r0 + 16 * i) * K) = kUE8M0 ? quant8_pow2(f[i], sc, byte) : quant8(f[i], sc);
   if (t == 0) {
     s[(e * NB + nb) * KB + kb] = sc;
     if (kUE8M0 && e8 != nullptr) e8[(e * NB + nb) * KB + kb] = byte;
@@ -141,7 +142,7 @@ __device__ __forceinline__ void swiglu_row_part(const uint16_t* __restrict__ y1,
     if (active) {
       uint8_t byte = 0;
       const float sc = kUE8M0 ? block_scale_ue8m0(amax, &byte) : block_scale(amax);
-      *reinterpret_cast<uint2*>(q + r * I + col) = quant8(h, sc);
+      *reinterpret_cast<uint2*>(q + r * I + col) = kUE8M0 ? quant8_pow2(h, sc, byte) : quant8(h, sc);
       if ((lane & 15) == 0) so.put(r, kb, KB, sc, byte);
     }
   }

@@ -234,10 +234,13 @@ def test_quant_non_finite_inputs(lib):
     x[4, 300] = np.inf
     x[5, 256:] = -np.inf
     xb = oracle.bf16_encode(x)
+    xb[6, 10] = 0xFFC0                  # NaNs with the sign bit set encode to 0x7F too
+    xb[6, 140] = 0xFF81
     _assert_quant_equal(lib, xb)
     _assert_ue8m0_equal(lib, xb)
     q, s = _gpu_quant(lib, xb)
     assert q[0, 7] == 0x7F and (q[1, :128] == 0x7F).all() and np.isinf(s[0, 2])
+    assert q[6, 10] == 0x7F and q[6, 140] == 0x7F
     _, _, e8 = _gpu_quant_ue8m0(lib, xb)
     assert e8[0, 2] == 255 and e8[1, 3] == 255 and e8[2, 5] == 255
 
