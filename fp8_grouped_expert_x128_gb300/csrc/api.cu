@@ -233,8 +233,6 @@ struct FfnFusion {
 // T = 1 / 64 gains 4 µs per step; at ~4000 ids (c2) the scans cost 7 µs more
 // than the index kernel they replace.
 constexpr int64_t kFuseIndexMaxIds = 1024;
-// above this many assignments the index pass runs over many CTAs (permute.cu)
-constexpr int64_t kFfnMultiIndexIds = 8192;
 bool ffn_fuse_index(const moe_ffn_desc* d) {
   return d->layout == MOE_LAYOUT_MASKED && d->T > 0 && d->T * d->k <= kFuseIndexMaxIds && d->k <= 16;
 }
@@ -282,7 +280,7 @@ extern "C" int moe_ffn_kernel_count(const moe_ffn_desc* d) {
   const FfnFusion f = ffn_fusion(d, out_on_host);
   // quant-scatter, with the index pass inside it, or before it as one kernel
   // or (large batches) as two
-  int n = ffn_fuse_index(d) ? 1 : (d->T * d->k > kFfnMultiIndexIds ? 3 : 2);
+  int n = ffn_fuse_index(d) ? 1 : (d->T * d->k > kIdxMultiMinIds ? 3 : 2);
   n += f.swiglu ? 1 : 2;                                                  // GEMM1 (+ SwiGLU)
   n += 1;                                                                 // GEMM2
   n += f.combine ? 0 : 1;                                                 // combine

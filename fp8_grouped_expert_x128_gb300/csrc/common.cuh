@@ -70,8 +70,10 @@ int permute_launch(const uint8_t* q, const float* s, int64_t s_ld, const uint16_
                    int64_t rows_capacity, int32_t* err, cudaStream_t st,
                    uint16_t* zero_out = nullptr, int64_t ldo = 0, uint8_t* sf8_out = nullptr,
                    bool fuse_index = false, int32_t* lrank = nullptr, int32_t* chunk_hist = nullptr);
-// Scratch of the many-CTA index pass (used above 8192 assignments when the
-// caller provides it): lrank [T*k] and chunk_hist [ceil(T*k / 4096)][E] int32.
+// Scratch of the many-CTA index pass (used above kIdxMultiMinIds assignments
+// when the caller provides it): lrank [T*k] and chunk_hist [ceil(T*k / 4096)][E]
+// int32.
+constexpr int64_t kIdxMultiMinIds = 8192;
 inline int64_t permute_chunk_count(int64_t assignments) { return (assignments + 4095) / 4096; }
 
 // SwiGLU + 1x128 requantisation (moe_swiglu_quant and moe_ffn): fp32 scales

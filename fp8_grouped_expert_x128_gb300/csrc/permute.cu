@@ -220,8 +220,8 @@ __global__ void __launch_bounds__(kIdxThreads) permute_index_kernel(IndexParams 
 // pass does; all CTAs share the -1 fill of the rows no assignment uses, and
 // CTA 0 writes counts, offsets and the error flags.
 constexpr int kIdxChunk = kIdxThreads * kIdxPer;
-constexpr int64_t kIdxMultiMinIds = 8192;   // from here on the index pass runs over many CTAs
 constexpr int kFinThreads = 256;
+static_assert(kIdxChunk == 4096, "permute_chunk_count sizes chunk_hist for 4096-id chunks");
 static_assert(kIdxChunk % kFinThreads == 0, "a finalize CTA stays inside one chunk");
 
 __global__ void __launch_bounds__(kIdxThreads, 1) permute_chunk_rank_kernel(IndexParams p, int32_t* lrank,

@@ -411,9 +411,11 @@ typedef struct moe_ffn_desc {
 } moe_ffn_desc;
 
 /* Number of kernels one moe_ffn call with this descriptor launches (the same
- * fusion choices moe_ffn makes: the optional SwiGLU fusion, the single-slot
- * combine in GEMM2), or a negative MOE_ERR_* for a descriptor moe_ffn would
- * refuse.  Host-only, no launch. */
+ * choices moe_ffn makes: the routing index pass inside the quant-scatter for
+ * masked batches of at most 1024 routing ids, as one kernel, or as two kernels
+ * above 8192 ids; the optional SwiGLU fusion; the single-slot combine in
+ * GEMM2), or a negative MOE_ERR_* for a descriptor moe_ffn would refuse.
+ * Host-only, no launch. */
 int moe_ffn_kernel_count(const moe_ffn_desc *desc);
 size_t moe_ffn_workspace_size(const moe_ffn_desc *desc);
 int moe_ffn(const moe_ffn_desc *desc, void *workspace, size_t workspace_bytes, void *stream);
