@@ -432,7 +432,7 @@ struct RankArgs {
 };
 
 template <int kQsWarps, int kQsPairs, bool kUE8M0, bool kRank = false>
-__global__ void __launch_bounds__(32 * kQsWarps, kRank ? 2 : (kQsWarps == 4 ? 6 : 4)) quant_scatter_kernel(
+__global__ void __launch_bounds__(32 * kQsWarps, kRank ? 2 : (kQsWarps == 4 ? 8 : 4)) quant_scatter_kernel(
     const uint16_t* __restrict__ x, int64_t ldx, const int32_t* __restrict__ dst_row,
     int64_t T, int32_t k, int64_t H, uint8_t* __restrict__ q_out, const ScaleOut so,
     uint16_t* __restrict__ zero_out, int64_t ldo, const RankArgs ra) {
